@@ -1,0 +1,175 @@
+"""Pins for the oracle's MoE routing / dispatch / combine, the LL word codec and
+the threadblock-swizzle order.  CPU only."""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from tile_centric_comm_gb300 import synth
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _gold(name):
+    with open(os.path.join(GOLD, name)) as f:
+        return json.load(f)
+
+
+# ------------------------------------------------------------------ MoE ----
+def test_moe_route_golden():
+    g = _gold("moe_route_small.json")
+    r = oracle.moe_route(np.array(g["topk"], np.int32), g["E"])
+    assert r["counts"].tolist() == g["counts"]
+    assert r["base"].tolist() == g["base"]
+    assert r["off"].tolist() == g["off"]
+    assert r["slot"].tolist() == g["slot"]
+    assert r["row_src"].tolist() == g["row_src"]
+    assert r["row_tok"].tolist() == g["row_tok"]
+    assert r["row_k"].tolist() == g["row_k"]
+    epr = g["E"] // g["W"]
+    for d, (lo, hi) in enumerate(g["rank_rows"]):
+        assert r["base"][d * epr] == lo and r["base"][(d + 1) * epr] == hi
+
+
+def _py_route(topk, E):
+    """Independent brute force: list every (src, t, k), sort by (expert, src,
+    t, k), and read the slots off the sorted position."""
+    W, T, KK = topk.shape
+    items = [(int(topk[s, t, k]), s, t, k) for s in range(W) for t in range(T)
+             for k in range(KK)]
+    order = sorted(items)
+    slot = np.zeros((W, T, KK), np.int64)
+    for pos, (_, s, t, k) in enumerate(order):
+        slot[s, t, k] = pos
+    counts = np.zeros((W, E), np.int64)
+    for e, s, _, _ in items:
+        counts[s, e] += 1
+    return slot, counts
+
+
+@pytest.mark.parametrize("W,T,E,k", [(2, 5, 4, 2), (4, 16, 8, 3), (3, 7, 16, 8)])
+def test_moe_route_brute_force(W, T, E, k):
+    inp = synth.moe_inputs(W, T, 4, E, k, seed=W * T)
+    r = oracle.moe_route(inp.topk, E)
+    slot, counts = _py_route(inp.topk, E)
+    assert np.array_equal(r["slot"], slot)
+    assert np.array_equal(r["counts"], counts)
+
+
+def test_moe_route_invariants_full_routing():
+    # full-size routing (8 ranks x 4096 tokens, 256 experts, top-8), tiny hidden
+    inp = synth.moe_inputs(8, 4096, 8, 256, 8, seed=0)
+    W, T, KK, E = 8, 4096, 8, 256
+    r = oracle.moe_route(inp.topk, E)
+    total = W * T * KK
+    assert r["counts"].sum() == total == r["base"][E]
+    assert np.all(np.diff(r["base"]) >= 0)
+    # every (src, t, k) has exactly one slot: the slots are a permutation
+    assert np.array_equal(np.sort(r["slot"].reshape(-1)), np.arange(total))
+    # inside an expert the rows are in (src, t) order and carry that expert
+    e_of_row = np.repeat(np.arange(E), np.diff(r["base"]))
+    assert np.array_equal(inp.topk[r["row_src"], r["row_tok"], r["row_k"]], e_of_row)
+    key = r["row_src"].astype(np.int64) * T + r["row_tok"]
+    for e in range(E):
+        seg = key[r["base"][e]:r["base"][e + 1]]
+        assert np.all(np.diff(seg) > 0)
+    # off is the exclusive scan over source ranks
+    assert np.array_equal(r["off"][0], np.zeros(E, np.int64))
+    assert np.array_equal(r["off"][1:], np.cumsum(r["counts"], axis=0)[:-1])
+    # the Zipf skew: expert 0 is the most loaded, rank 0 hosts the most rows
+    per_rank = [r["base"][(d + 1) * 32] - r["base"][d * 32] for d in range(W)]
+    assert per_rank[0] == max(per_rank)
+
+
+def test_moe_route_rejects_bad_ids():
+    with pytest.raises(ValueError):
+        oracle.moe_route(np.array([[[0, 4]]], np.int32), 4)
+    with pytest.raises(ValueError):
+        oracle.moe_route(np.array([[[-1, 0]]], np.int32), 4)
+
+
+def test_moe_top1_unit_weight_round_trip_is_identity():
+    inp = synth.moe_inputs(4, 64, 32, 16, 8, seed=3, top1_unit=True)
+    r = oracle.moe_route(inp.topk, inp.E)
+    recv = oracle.moe_dispatch(inp.x, r["slot"], inp.W * inp.T)
+    out16, _ = oracle.moe_combine(recv, r["slot"], inp.gate)
+    assert np.array_equal(out16, inp.x)
+
+
+def test_moe_unit_weights_integer_x_gives_k_times_x():
+    inp = synth.moe_inputs(2, 32, 16, 16, 8, seed=5, x_dist="int2")
+    r = oracle.moe_route(inp.topk, inp.E)
+    recv = oracle.moe_dispatch(inp.x, r["slot"], 2 * 32 * 8)
+    ones = np.ones_like(inp.gate)
+    _, out64 = oracle.moe_combine(recv, r["slot"], ones)
+    assert np.array_equal(out64, 8.0 * oracle.bf16_to_f64(inp.x))
+
+
+def test_moe_softmax_gates_round_trip_close_to_x():
+    inp = synth.moe_inputs(2, 64, 64, 32, 8, seed=6)
+    assert np.allclose(inp.gate.sum(-1), 1.0, atol=1e-6)
+    r = oracle.moe_route(inp.topk, inp.E)
+    recv = oracle.moe_dispatch(inp.x, r["slot"], 2 * 64 * 8)
+    _, out64 = oracle.moe_combine(recv, r["slot"], inp.gate)
+    x = oracle.bf16_to_f64(inp.x)
+    assert np.max(np.abs(out64 - x)) <= 1e-5 * np.max(np.abs(x))
+
+
+def test_moe_dispatch_rows_are_source_rows():
+    inp = synth.moe_inputs(2, 8, 16, 8, 3, seed=8)
+    r = oracle.moe_route(inp.topk, inp.E)
+    recv = oracle.moe_dispatch(inp.x, r["slot"], 2 * 8 * 3)
+    assert np.array_equal(recv, inp.x[r["row_src"], r["row_tok"]])
+
+
+def test_moe_combine_closed_form_constant_rows():
+    # y rows are constants c_row: out[src][t][h] = sum_k gate * c[slot]
+    W, T, KK, H = 2, 4, 3, 5
+    g = np.random.default_rng(2)
+    slot = g.permutation(W * T * KK).reshape(W, T, KK).astype(np.int64)
+    c = g.integers(-4, 5, W * T * KK).astype(np.float32)
+    y = synth.f32_to_bf16_bits(np.repeat(c[:, None], H, axis=1))
+    gate = g.standard_normal((W, T, KK)).astype(np.float32)
+    _, out64 = oracle.moe_combine(y, slot, gate)
+    want = (gate.astype(np.float64) * c[slot]).sum(-1)
+    np.testing.assert_allclose(out64, np.repeat(want[..., None], H, -1), rtol=1e-15)
+
+
+# ------------------------------------------------------------------- LL ----
+def test_ll_word_golden():
+    for c in _gold("ll_word.json")["cases"]:
+        w = oracle.ll_pack(np.array([int(c["payload"], 16)], np.uint32), c["flag"])
+        assert int(w[0]) == int(c["word"], 16)
+
+
+def test_ll_round_trip_and_missing_flags():
+    g = np.random.default_rng(0)
+    p = g.integers(0, 2 ** 32, 1000, dtype=np.uint64).astype(np.uint32)
+    w = oracle.ll_pack(p, 12345)
+    back, missing = oracle.ll_unpack(w, 12345)
+    assert missing == 0 and np.array_equal(back, p)
+    w[[3, 500]] = oracle.ll_pack(p[[3, 500]], 12344)   # stale epoch
+    back, missing = oracle.ll_unpack(w, 12345)
+    assert missing == 2
+
+
+# -------------------------------------------------------------- swizzle ----
+def test_swizzle_golden():
+    for c in _gold("swizzle_order.json")["cases"]:
+        pm, pn = oracle.swizzle_order(c["rank"], c["tiles_per_pe"], c["total_m"],
+                                      c["n_tiles"])
+        assert pm.tolist() == c["pid_m"] and pn.tolist() == c["pid_n"]
+
+
+@pytest.mark.parametrize("W,tpp,n", [(8, 8, 20), (2, 1, 2), (8, 16, 28)])
+def test_swizzle_is_permutation_starting_local(W, tpp, n):
+    total = W * tpp
+    for rank in range(W):
+        pm, pn = oracle.swizzle_order(rank, tpp, total, n)
+        ids = pm * n + pn
+        assert np.array_equal(np.sort(ids), np.arange(total * n))
+        # each rank starts on its own (local) rows
+        first = pm[: tpp * n]
+        assert set(first.tolist()) == set(range(rank * tpp, (rank + 1) * tpp))
