@@ -1,0 +1,273 @@
+/*
+ * tdg.h -- C ABI of libtdg: tile-centric overlapped AllGather+GEMM,
+ * GEMM+ReduceScatter and MoE dispatch/combine on one GB300 (sm_103a).
+ *
+ * Model.  W logical ranks live in ONE device allocation that the caller owns:
+ * W equal "regions" (rank r's symmetric heap) followed by W signal areas and
+ * a small status block.  "Communication" moves tiles between regions inside
+ * HBM; every tile carries its own signal.  This follows the programming model
+ * of the Triton-distributed paper summary (hyper.ai, arXiv 2504.19442, section
+ * 方法: symmetric memory, signal exchange, asynchronous tasks) and of
+ * "Triton-distributed 语义" (sections 生产者-消费者模型, 基于信号的同步,
+ * 对称内存模型, 内核设计模式, 线程块交织, 基于令牌的数据依赖).
+ *
+ * Conventions for every entry point:
+ *   - All pointers named dev_* / device are device pointers; host pointers are
+ *     named host_*.  Streams are passed as void* and are cudaStream_t values
+ *     (NULL = the legacy default stream).
+ *   - bf16 = IEEE bfloat16, row-major, no padding between rows.
+ *   - Calls are asynchronous on the given stream(s).  Inputs must stay
+ *     unchanged and outputs untouched until the stream has completed the call.
+ *   - Return value: TDG_OK (0) or a negative TDG_ERR_* code from host-side
+ *     validation; nothing is launched when validation fails.  Faults found on
+ *     the device (a signal wait that ran out of time, an out-of-range index)
+ *     are recorded in the handle's status block and read with tdg_status().
+ *   - The library allocates no device memory.  Each entry point documents
+ *     which caller-provided buffers it uses.
+ *   - A handle is thread-compatible, not thread-safe: do not call into the
+ *     same handle from two host threads at once.
+ */
+#ifndef TDG_H_
+#define TDG_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define TDG_API __attribute__((visibility("default")))
+#else
+#define TDG_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- error codes -------------------------------------------------------- */
+#define TDG_OK 0
+#define TDG_ERR_INVALID -1     /* bad argument: shape, alignment, range, NULL */
+#define TDG_ERR_CUDA -2        /* a CUDA runtime/driver call failed           */
+#define TDG_ERR_NOMEM -3       /* a caller buffer / region / signal area is too small */
+#define TDG_ERR_TIMEOUT -4     /* device: a bounded signal wait ran out of time */
+#define TDG_ERR_UNSUPPORTED -5 /* device or mode not supported here           */
+#define TDG_ERR_DEVICE -6      /* device: a kernel found an out-of-range index  */
+
+/* ---- modes -------------------------------------------------------------- */
+/* SM: producer CTAs and consumer CTAs in one persistent launch (overlapped). */
+#define TDG_MODE_SM 0
+/* CE: copies on the copy engine (side stream) + stream-ordered flag writes;
+ *     the GEMM runs on the main stream and waits on the flags.              */
+#define TDG_MODE_CE 1
+/* LL: low-latency path: 8-byte {payload, flag} words, for small shards.     */
+#define TDG_MODE_LL 2
+/* SERIAL: same kernels, one after the other with no overlap (copy, then
+ *     GEMM, then reduce) -- the measurement twin and the "barrier between
+ *     phases" debugging mode.                                               */
+#define TDG_MODE_SERIAL 3
+
+/* layout of B for the GEMMs */
+#define TDG_B_KN 0 /* B is K x N row-major (N contiguous)  */
+#define TDG_B_NK 1 /* B is N x K row-major (K contiguous)  */
+
+/* ---- symmetric heap ------------------------------------------------------ */
+typedef struct tdg_symm tdg_symm; /* opaque, owned by the library */
+
+/*
+ * Bytes the caller must provide for a symmetric heap of `world` regions of
+ * `region_bytes` each, with `signals_per_rank` 32-bit flag words and as many
+ * 32-bit counter words per rank.  region_bytes must be a multiple of 1024.
+ */
+TDG_API size_t tdg_symm_bytes(int world, size_t region_bytes, size_t signals_per_rank);
+
+/*
+ * Carve caller memory [dev_base, dev_base + bytes) into the heap described
+ * above.  Layout: region r at dev_base + r*region_bytes; then the flag words
+ * of every rank; then the counter words of every rank; then the status block.
+ * The signal areas and the status block are zeroed here (synchronously, with
+ * cudaMemset on the current device).  dev_base must be 1024-byte aligned.
+ * The caller keeps ownership of the memory; tdg_symm_free never frees it.
+ * Returns TDG_OK and *out, or TDG_ERR_INVALID / TDG_ERR_NOMEM / TDG_ERR_CUDA.
+ */
+TDG_API int tdg_symm_alloc(void *dev_base, size_t bytes, int world, size_t region_bytes,
+                   size_t signals_per_rank, tdg_symm **out);
+
+/* Release the handle (host memory only). */
+TDG_API int tdg_symm_free(tdg_symm *h);
+
+/* Base of rank `rank`'s region, or NULL if rank is out of range. */
+TDG_API void *tdg_symm_region(const tdg_symm *h, int rank);
+
+/*
+ * symm_at: translate a pointer inside any region to the same offset inside
+ * region `rank` ("Triton-distributed 语义", 对称内存模型: symm_at(ptr, rank)).
+ * Returns NULL if local_ptr is not inside a region or rank is out of range.
+ */
+TDG_API void *tdg_symm_at(const tdg_symm *h, const void *local_ptr, int rank);
+
+/* Device address of rank `rank`'s flag words / counter words (NULL if out of range). */
+TDG_API uint32_t *tdg_symm_flags(const tdg_symm *h, int rank);
+TDG_API uint32_t *tdg_symm_counters(const tdg_symm *h, int rank);
+
+/* The epoch the next call will use (flags compare against it; never 0). */
+TDG_API uint32_t tdg_symm_epoch(const tdg_symm *h);
+
+/* ---- device status ------------------------------------------------------- */
+typedef struct {
+    int32_t code;   /* TDG_OK, TDG_ERR_TIMEOUT or TDG_ERR_DEVICE              */
+    uint32_t where; /* which wait / check: see TDG_WHERE_*                   */
+    uint32_t index; /* signal or tile index involved                          */
+    uint32_t epoch; /* epoch of the call that failed                          */
+} tdg_fault;
+
+#define TDG_WHERE_AG_FLAG 1    /* consumer waiting on an AllGather tile flag */
+#define TDG_WHERE_PIPE 2       /* an intra-CTA pipeline barrier ran out of time */
+#define TDG_WHERE_LL 3         /* LL receiver waiting on a data+flag word     */
+#define TDG_WHERE_MOE_EXPERT 4 /* an expert id outside [0, E)                 */
+
+/*
+ * Copy the status block to *out (may be NULL) after synchronising `stream`,
+ * and clear it when clear != 0.  Returns the status code (TDG_OK if no device
+ * fault was recorded since the last clear), or TDG_ERR_CUDA.
+ */
+TDG_API int tdg_status(tdg_symm *h, void *stream, tdg_fault *out, int clear);
+
+/* Human-readable text for a TDG_* code (static storage). */
+TDG_API const char *tdg_strerror(int code);
+
+/* Number of SMs and whether the current device runs these kernels (sm_103). */
+TDG_API int tdg_device_info(int *sm_count, int *supported);
+
+/* ---- AllGather + GEMM ----------------------------------------------------- */
+/*
+ * C = concat_rows(A_0, ..., A_{W-1}) @ B, computed by rank `rank`
+ * ("Triton-distributed 语义", 内核设计模式 "AllGather + GEMM 重叠"; paper
+ * summary, 方法: intra-node AllGather on SMs or the copy engine).
+ *
+ * Shard s (Ms x K bf16) sits at region(s) + a_off.  The AllGather writes the
+ * gathered M x K matrix (M = W*Ms) into region(rank) + g_off, shard s at rows
+ * [s*Ms, (s+1)*Ms) -- rank `rank` pulls every shard, its own included.
+ * Producers signal per group of `signal_rows` gathered rows (flag word
+ * g = row / signal_rows of rank `rank`'s flags, set to the call's epoch with
+ * release semantics); the GEMM waits on every group its A tile needs
+ * (bounded acquire spin), so it computes on tiles that have arrived while
+ * others are still in flight.  Tiles are visited in the rank-swizzled order
+ * pid_m = (pid_m + rank*Ms/BM) % m_tiles ("Triton-distributed 语义", 线程块交织)
+ * when swizzle != 0; when Ms is a multiple of BM the local shard is read in
+ * place, with no wait.
+ *
+ * B: K x N (TDG_B_KN) or N x K (TDG_B_NK) bf16, device pointer.
+ * C: M x N bf16 output, device pointer.
+ * Requirements: 1 <= world <= 64; K % 8 == 0; N % 8 == 0; a_off, g_off, B, C
+ * 16-byte aligned; g_off + M*K*2 <= region_bytes; a_off + Ms*K*2 <=
+ * region_bytes; M / signal_rows <= signals_per_rank.  M == 0 or N == 0 is a
+ * no-op; K == 0 writes C = 0.
+ */
+typedef struct {
+    int world, rank;
+    int64_t Ms, K, N;
+    size_t a_off, g_off;
+    const void *B;
+    void *C;
+    int b_layout;        /* TDG_B_KN or TDG_B_NK                            */
+    int mode;            /* TDG_MODE_SM / CE / LL / SERIAL                  */
+    int producers;       /* producer CTAs in SM / LL mode (0 = default)     */
+    int64_t signal_rows; /* rows per signal; 0 = BM if Ms % BM == 0, else Ms */
+    int swizzle;         /* 1 = rank-swizzled tile order, 0 = linear        */
+    uint64_t timeout_ns; /* bound of every device wait; 0 = 2 s             */
+    size_t ll_off;       /* LL mode: LL buffer (M*K*4 bytes) in region(rank) */
+    uint64_t test_skip_notify; /* tests only: producers skip the notify of
+                                  signal groups whose bit (g % 64) is set   */
+} tdg_ag_gemm_args;
+
+TDG_API int tdg_ag_gemm(tdg_symm *h, const tdg_ag_gemm_args *args, void *stream,
+                void *side_stream);
+
+/* ---- GEMM + ReduceScatter -------------------------------------------------- */
+/*
+ * out_o = rows [o*Mo, (o+1)*Mo) of sum_r A_r @ B_r, Mo = M / W, for every
+ * owner o ("Triton-distributed 语义", 内核设计模式 "GEMM + ReduceScatter 重叠";
+ * paper summary, 方法: push-mode ReduceScatter, reduction in parallel,
+ * synchronised by signals).
+ *
+ * A_r (M x K bf16) at region(r) + a_off, B_r (K x N, or N x K with
+ * TDG_B_NK) at region(r) + b_off, out_o (Mo x N bf16) at region(o) + out_off.
+ * Every rank's GEMM pushes each bf16 partial tile (BM x BN, tile-contiguous)
+ * into the owner's staging area, region(o) + stage_off (see
+ * tdg_gemm_rs_stage_bytes), then increments the owner's per-tile arrival
+ * counter with release semantics.  The CTA whose increment completes the
+ * count of W acquires it, sums the W partials in fixed rank order in fp32
+ * and writes the bf16 result, then resets the counter to 0.  SERIAL mode
+ * runs the GEMM for all partials first and the reduction after it.
+ * Requirements: M % W == 0, (M/W) % 128 == 0, K % 8 == 0, N % 8 == 0, the
+ * offsets 16-byte aligned, W*(M/W/128)*ceil(N/256) <= signals_per_rank.
+ */
+typedef struct {
+    int world;
+    int64_t M, K, N;
+    size_t a_off, b_off, stage_off, out_off;
+    int b_layout;
+    int mode;            /* TDG_MODE_SM (overlapped) or TDG_MODE_SERIAL      */
+    uint64_t timeout_ns; /* bound of every device wait; 0 = 2 s             */
+} tdg_gemm_rs_args;
+
+/* Bytes of one owner's staging area for the given shape (all W partials). */
+TDG_API size_t tdg_gemm_rs_stage_bytes(int world, int64_t M, int64_t N);
+
+TDG_API int tdg_gemm_rs(tdg_symm *h, const tdg_gemm_rs_args *args, void *stream);
+
+/* ---- MoE dispatch / combine ------------------------------------------------ */
+/*
+ * Expert-parallel AllToAll as a permutation (paper summary, 实验: AllToAll
+ * dispatch / combine; "Triton-distributed 正把通信纳入编译器的职责范围",
+ * "DITRON 加入三级分块": per-expert sizes known only at run time).
+ *
+ * Rank src holds x_src (T x H bf16) at region(src) + x_off, its routing
+ * topk_src (T x k int32 expert ids) at region(src) + topk_off and gates
+ * (T x k float32) at region(src) + gate_off.  Experts are split evenly:
+ * rank d owns experts [d*E/W, (d+1)*E/W).
+ *
+ * Routing (phase bit TDG_MOE_ROUTE): counts[src*E+e] (int64), the
+ * expert-major exclusive scan base[0..E] (int64, base[E] = W*T*k) and
+ * slot[(src*T+t)*k+kk] (int64): receive row of (src, t, kk); inside one
+ * expert the rows follow (src, t, kk) order.  Optional row_src / row_tok /
+ * row_k (int32 per receive row, may be NULL).
+ * Dispatch (TDG_MOE_DISPATCH): recv[slot(src,t,kk)] = x_src[t] (bit copy).
+ * recv is one expert-major array of W*T*k rows of H bf16; rank d's receive
+ * buffer is rows [base[d*E/W], base[(d+1)*E/W]).
+ * Combine (TDG_MOE_COMBINE): out_src[t] = bf16(sum_kk gate[t][kk] *
+ * y[slot(src,t,kk)]) with an fp32 sum in kk order, written to region(src) +
+ * out_off.  y has the receive layout; y == NULL means y = recv.
+ * workspace: device scratch of tdg_moe_workspace_bytes() bytes.
+ * Requirements: E % W == 0, 1 <= k <= 32, k <= E, H % 8 == 0, offsets and
+ * pointers 16-byte aligned.  An expert id outside [0, E) is reported as
+ * TDG_ERR_DEVICE by tdg_status and that (t, kk) gets slot -1.
+ */
+#define TDG_MOE_ROUTE 1
+#define TDG_MOE_DISPATCH 2
+#define TDG_MOE_COMBINE 4
+#define TDG_MOE_ALL 7
+
+typedef struct {
+    int world;
+    int64_t T;
+    int64_t H;
+    int E, k;
+    size_t x_off, topk_off, gate_off, out_off;
+    void *recv;
+    const void *y;
+    int64_t *counts, *base, *slot;
+    int32_t *row_src, *row_tok, *row_k;
+    void *workspace;
+    size_t workspace_bytes;
+    int phases; /* OR of TDG_MOE_ROUTE / DISPATCH / COMBINE */
+} tdg_moe_args;
+
+TDG_API size_t tdg_moe_workspace_bytes(int world, int64_t T, int E);
+
+TDG_API int tdg_moe_dispatch_combine(tdg_symm *h, const tdg_moe_args *args, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TDG_H_ */

@@ -1,0 +1,111 @@
+"""GPU parity of AllGather+GEMM (through the C ABI) against the CPU oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tile_centric_comm_gb300 import synth, tdg
+from gpu_util import AGCase, assert_close, to_bits
+
+pytestmark = pytest.mark.gpu
+
+
+def _gathered_ok(case, rank):
+    g = to_bits(case.gathered(rank))
+    assert np.array_equal(g, np.concatenate(case.inp.shards)), "gathered buffer differs"
+
+
+def test_tiny_integer_bit_exact_all_modes_and_ranks():
+    # W=2, A_r 64x256, B 256x128, integers in [-2, 2]: bit-exact
+    inp = synth.make("ag_tiny")
+    C64, C16 = oracle.ag_gemm(inp.shards, inp.B)
+    case = AGCase(inp)
+    for mode in ("sm", "serial", "ce"):
+        for rank in range(inp.W):
+            got, _ = case.run(rank=rank, mode=mode)
+            assert np.array_equal(got, C16), (mode, rank)
+            _gathered_ok(case, rank)
+
+
+@pytest.mark.parametrize("b_layout", [tdg.B_KN, tdg.B_NK])
+@pytest.mark.parametrize("W,Ms,K,N", [
+    (4, 256, 320, 520),     # 8 m tiles, 3 n tiles (last one 8 columns), 5 k blocks
+    (3, 96, 136, 264),      # Ms not a multiple of 128: gathered read, ragged m tail
+    (2, 128, 64, 256),      # exactly one k block, full n tile
+])
+def test_float_parity_small(W, Ms, K, N, b_layout):
+    inp = synth.ag_inputs(W, Ms, K, N, "normal", seed=W * 7 + K)
+    C64, C16 = oracle.ag_gemm(inp.shards, inp.B)
+    case = AGCase(inp, b_layout=b_layout)
+    for mode in ("sm", "serial", "ce"):
+        got, _ = case.run(rank=W - 1, mode=mode)
+        assert_close(got, C64)
+        _gathered_ok(case, W - 1)
+
+
+def test_integer_exact_larger_and_swizzle_invariance():
+    # integer inputs, |sums| <= 4K: exact in fp32; output identical for every
+    # rank, swizzle on/off, signal granularity and producer count
+    inp = synth.ag_inputs(4, 256, 512, 384, "int2", seed=3)
+    _, C16 = oracle.ag_gemm(inp.shards, inp.B)
+    case = AGCase(inp)
+    outs = []
+    for rank in range(4):
+        for swz in (True, False):
+            for sig in (0, 64, 256):
+                got, _ = case.run(rank=rank, mode="sm", swizzle=swz, signal_rows=sig,
+                                  producers=4 + rank)
+                outs.append(got)
+    for o in outs:
+        assert np.array_equal(o, C16)
+
+
+def test_timeout_reported_then_next_call_succeeds():
+    # fault injection on the host side: producers skip one notify; the consumer's
+    # bounded wait must run out, report TIMEOUT with the signal index, and the
+    # next call (new epoch) must succeed.
+    inp = synth.ag_inputs(2, 128, 64, 256, "int2", seed=1)
+    _, C16 = oracle.ag_gemm(inp.shards, inp.B)
+    case = AGCase(inp)
+    # rank 0 reads its own shard in place; group 4 (rows 128..159, shard 1) is remote
+    _, st = case.run(rank=0, mode="sm", signal_rows=32, test_skip_notify=1 << 4,
+                     timeout_ns=20_000_000, check_status=False)
+    assert st["code"] == tdg.TDG_ERR_TIMEOUT and st["where"] == "ag_flag" and st["index"] == 4
+    got, st = case.run(rank=0, mode="sm", signal_rows=32)
+    assert st["code"] == 0 and np.array_equal(got, C16)
+
+
+def test_degenerate_shapes():
+    # K == 0 gives C = 0; N == 0 and Ms == 0 are no-ops
+    inp = synth.ag_inputs(2, 64, 8, 16, "int2", seed=2)
+    case = AGCase(inp)
+    tdg.ag_gemm(case.symm, 0, 64, 0, 16, case.a_off, case.g_off, case.B, case.C)
+    torch.cuda.synchronize()
+    assert np.all(to_bits(case.C) == 0)
+    case.C.view(torch.int16).fill_(7)
+    tdg.ag_gemm(case.symm, 0, 64, 8, 0, case.a_off, case.g_off, case.B, case.C)
+    tdg.ag_gemm(case.symm, 0, 0, 8, 16, case.a_off, case.g_off, case.B, case.C)
+    torch.cuda.synchronize()
+    assert np.all(to_bits(case.C) == 7)
+    with pytest.raises(tdg.TdgError):     # K not a multiple of 8
+        tdg.ag_gemm(case.symm, 0, 64, 12, 16, case.a_off, case.g_off, case.B, case.C)
+    with pytest.raises(tdg.TdgError):     # bad rank
+        tdg.ag_gemm(case.symm, 2, 64, 8, 16, case.a_off, case.g_off, case.B, case.C)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["ag_qwen32b_up", "ag_llama70b_gateup"])
+def test_full_size_sampled(name):
+    inp = synth.make(name)
+    case = AGCase(inp)
+    g = np.random.default_rng(0)
+    M, N = case.M, inp.N
+    rows = np.concatenate([g.integers(0, M, 1500), [0, M - 1]])
+    cols = np.concatenate([g.integers(0, N, 1500), [N - 1, 0]])
+    ref = oracle.ag_gemm_sampled(inp.shards, inp.B, rows, cols)
+    for mode in ("sm", "serial"):
+        got, _ = case.run(rank=3, mode=mode)
+        assert_close(got[rows, cols], ref)
+        _gathered_ok(case, 3)
+    del case
+    torch.cuda.empty_cache()

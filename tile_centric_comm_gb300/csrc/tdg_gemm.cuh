@@ -1,0 +1,287 @@
+// tdg_gemm.cuh -- persistent, warp-specialised bf16 GEMM on the 5th-generation
+// tensor cores (tcgen05 + TMEM), the consumer of the AllGather and the producer
+// of the ReduceScatter ("Triton-distributed 语义", 内核设计模式: the consumer
+// waits for each tile and computes on it at once; the GEMM producer signals
+// each finished output tile).
+//
+// One CTA per SM, 6 warps:
+//   warp 0      TMA loader: per tile it first runs the policy's signal wait
+//               (the wait / consume_token pair of the pages), then streams
+//               BK-wide slices of A and B into a STAGES-deep shared-memory ring.
+//   warp 1      MMA issuer: one thread issues tcgen05.mma (M=128, N<=256,
+//               K=16) into one of two TMEM accumulators (2 x 256 fp32 columns)
+//               and frees ring slots with tcgen05.commit.
+//   warps 2..5  epilogue: tcgen05.ld -> bf16 (round to nearest even) ->
+//               128B-swizzled staging -> TMA store; then the policy's
+//               after-tile hook (the GEMM+RS signal and reduction).
+// Tiles are BM x BN = 128 x 256; a tile at the right edge of N issues a
+// narrower MMA (N rounded up to 16) and stores only its valid columns.
+// Operands: A is K-major (rows of K); B is either MN-major (K x N row-major,
+// the transpose bit of the instruction descriptor) or K-major (N x K).
+#pragma once
+
+#include "tdg.h"
+#include "tdg_ptx.cuh"
+
+namespace tdg {
+namespace gm {
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;            // 16 KB
+constexpr int B_BYTES = BN * BK * 2;            // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 48 KB
+constexpr int NUM_THREADS = 192;
+constexpr int EPI_WARP0 = 2;
+constexpr int EPI_WARPS = 4;
+constexpr int EPI_BUF = 32 * 128;               // 32 rows x 64 bf16 (128 B)
+constexpr int OFF_EPI = STAGES * STAGE_BYTES;   // 196608
+constexpr int OFF_BAR = OFF_EPI + EPI_WARPS * 2 * EPI_BUF; // 229376
+constexpr int BAR_BYTES = 256;
+constexpr int SMEM_BYTES = OFF_BAR + BAR_BYTES + 1024;     // + alignment slack
+constexpr uint32_t TMEM_COLS = 512;
+} // namespace gm
+
+struct TileInfo {
+    int m0;      // first output row of the tile
+    int n0;      // first output column
+    int n_valid; // columns of this tile inside N (1..BN)
+    int a_row;   // row coordinate of the tile in the selected A tensor map
+    int a_sel;   // policy-defined: which A map / which rank
+    int owner;   // policy-defined (RS: owner rank)
+    int m_loc;   // policy-defined (RS: m tile inside the owner)
+    int pn;      // n tile index
+};
+
+struct PipeSmem {
+    uint64_t full[gm::STAGES];
+    uint64_t empty[gm::STAGES];
+    uint64_t tfull[2];
+    uint64_t tempty[2];
+    uint64_t drain;     // used only after an abort, to drain issued MMAs
+    uint32_t tmem_base;
+    volatile int abort;
+    int is_last;        // RS: broadcast of the "last arriver" decision
+    uint32_t issued;    // ring fills issued by the loader
+    uint32_t consumed;  // ring fills consumed by the MMA issuer
+};
+
+__device__ __forceinline__ uint8_t *align1024(uint8_t *p)
+{
+    return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+// Policy P provides:
+//   struct Params { ... DevStatus *status; uint32_t epoch; uint64_t timeout_ns; int k_blocks; };
+//   static constexpr int B_MN;                                   // 1: B is K x N
+//   __device__ static int64_t num_items(const Params&);
+//   __device__ static void tile(const Params&, int64_t item, TileInfo&);
+//   __device__ static void before_a(const Params&, const TileInfo&, bool &gave_up);  // lane 0 of warp 0
+//   __device__ static void load_a(const Params&, const TileInfo&, void *dst, uint64_t *bar, int kb);
+//   __device__ static void load_b(const Params&, const TileInfo&, void *dst, uint64_t *bar, int kb);
+//   __device__ static uint32_t b_bytes(const TileInfo&);
+//   __device__ static void store_chunk(const Params&, const TileInfo&, const void *buf, int ch, int q);
+//   __device__ static void after_tile(const Params&, const TileInfo&, int q, int lane);  // per epilogue warp
+template <class P>
+__device__ void gemm_consumer(const typename P::Params &p, uint8_t *smem, int cta, int ncta)
+{
+    using namespace gm;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    PipeSmem *ps = reinterpret_cast<PipeSmem *>(smem + OFF_BAR);
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < STAGES; ++i) {
+            mbar_init(&ps->full[i], 1);
+            mbar_init(&ps->empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&ps->tfull[i], 1);
+            mbar_init(&ps->tempty[i], EPI_WARPS);
+        }
+        mbar_init(&ps->drain, 1);
+        ps->issued = 0;
+        ps->consumed = 0;
+        ps->abort = 0;
+        ps->is_last = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&ps->tmem_base, TMEM_COLS);
+        tmem_relinquish();
+        tc_fence_before();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = ps->tmem_base;
+    const int64_t items = P::num_items(p);
+    const uint64_t tmo = p.timeout_ns;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool gave_up = false;
+            for (int64_t it = cta; it < items && !ps->abort; it += ncta) {
+                TileInfo ti;
+                P::tile(p, it, ti);
+                P::before_a(p, ti, gave_up);
+                const uint32_t bytes = A_BYTES + P::b_bytes(ti);
+                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!mbar_wait(&ps->empty[stage], phase ^ 1u, tmo)) {
+                        report_fault(p.status, TDG_ERR_TIMEOUT, TDG_WHERE_PIPE, 0, p.epoch);
+                        ps->abort = 1;
+                        break;
+                    }
+                    uint8_t *sa = smem + stage * STAGE_BYTES;
+                    mbar_arrive_expect_tx(&ps->full[stage], bytes);
+                    P::load_a(p, ti, sa, &ps->full[stage], kb);
+                    P::load_b(p, ti, sa + A_BYTES, &ps->full[stage], kb);
+                    ps->issued += 1;
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            const uint32_t sbase = smem_u32(smem);
+            for (int64_t it = cta; it < items && !ps->abort; it += ncta) {
+                TileInfo ti;
+                P::tile(p, it, ti);
+                const int n_mma = (ti.n_valid + 15) & ~15;
+                const uint32_t idesc = idesc_bf16(BM, n_mma, P::B_MN);
+                if (!mbar_wait(&ps->tempty[acc], acc_phase ^ 1u, tmo)) {
+                    report_fault(p.status, TDG_ERR_TIMEOUT, TDG_WHERE_PIPE, 1, p.epoch);
+                    ps->abort = 1;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+                bool ok = true;
+                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!mbar_wait(&ps->full[stage], phase, tmo)) {
+                        report_fault(p.status, TDG_ERR_TIMEOUT, TDG_WHERE_PIPE, 2, p.epoch);
+                        ps->abort = 1;
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = sbase + stage * STAGE_BYTES;
+                    const uint32_t b_addr = a_addr + A_BYTES;
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k) {
+                        const uint64_t ad = sdesc_sw128(a_addr + k * 32, 16, 1024);
+                        // MN-major B: 64-column chunks 8 KB apart (LBO), 8 K-rows
+                        // 1 KB apart (SBO); a K step of 16 rows is 2 KB.
+                        // K-major B: same form as A.
+                        const uint64_t bd = P::B_MN ? sdesc_sw128(b_addr + k * 2048, 8192, 1024)
+                                                    : sdesc_sw128(b_addr + k * 32, 16, 1024);
+                        umma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+                    }
+                    umma_commit(&ps->empty[stage]);
+                    ps->consumed += 1;
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok)
+                    break;
+                umma_commit(&ps->tfull[acc]);
+                if (++acc == 2) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
+            }
+            if (ps->abort) {
+                // let every MMA this thread issued finish before TMEM is freed
+                umma_commit(&ps->drain);
+                (void)mbar_wait(&ps->drain, 0, tmo);
+            }
+        }
+        __syncwarp();
+    } else {
+        // epilogue warps: TMEM lane quarter q = warp % 4 (hardware rule)
+        const int q = warp & 3;
+        uint8_t *bufs = smem + OFF_EPI + (warp - EPI_WARP0) * 2 * EPI_BUF;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        int buf = 0;
+        for (int64_t it = cta; it < items; it += ncta) {
+            TileInfo ti;
+            P::tile(p, it, ti);
+            bool ok = mbar_wait(&ps->tfull[acc], acc_phase, tmo);
+            if (!ok || ps->abort) {
+                if (lane == 0 && !ok)
+                    report_fault(p.status, TDG_ERR_TIMEOUT, TDG_WHERE_PIPE, 3, p.epoch);
+                ps->abort = 1;
+                break;
+            }
+            tc_fence_after();
+            const int nch = (ti.n_valid + 63) >> 6;
+            for (int ch = 0; ch < nch; ++ch) {
+                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                       static_cast<uint32_t>(acc * BN + ch * 64);
+                uint32_t r0[32], r1[32];
+                tmem_ld_32x32b_x32(taddr, r0);
+                tmem_ld_32x32b_x32(taddr + 32, r1);
+                tmem_ld_wait();
+                if (lane == 0)
+                    bulk_wait_read<1>();
+                __syncwarp();
+                uint8_t *row = bufs + buf * EPI_BUF + lane * 128;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    uint32_t w0, w1, w2, w3;
+                    const uint32_t *src = (j < 4) ? &r0[j * 8] : &r1[(j - 4) * 8];
+                    w0 = pack_bf16x2(__uint_as_float(src[0]), __uint_as_float(src[1]));
+                    w1 = pack_bf16x2(__uint_as_float(src[2]), __uint_as_float(src[3]));
+                    w2 = pack_bf16x2(__uint_as_float(src[4]), __uint_as_float(src[5]));
+                    w3 = pack_bf16x2(__uint_as_float(src[6]), __uint_as_float(src[7]));
+                    *reinterpret_cast<uint4 *>(row + ((j ^ (lane & 7)) << 4)) = make_uint4(w0, w1, w2, w3);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    P::store_chunk(p, ti, bufs + buf * EPI_BUF, ch, q);
+                    bulk_commit();
+                }
+                buf ^= 1;
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&ps->tempty[acc]);
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+            P::after_tile(p, ti, q, lane);
+        }
+        if (lane == 0)
+            bulk_wait<0>();
+    }
+    __syncthreads();
+    if (ps->abort && threadIdx.x == 0) {
+        // wait (bounded) for ring fills that were issued but never consumed,
+        // so no TMA write lands in shared memory after the CTA has exited
+        for (uint32_t f = ps->consumed; f < ps->issued; ++f)
+            (void)mbar_wait(&ps->full[f % STAGES], (f / STAGES) & 1u, tmo);
+    }
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+} // namespace tdg

@@ -1,0 +1,84 @@
+// tdg_internal.h -- host-side declarations shared by the translation units of
+// libtdg (the handle layout, tensor-map encoding through the driver entry
+// point, launch helpers).  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <stdlib.h>
+
+#include "tdg.h"
+#include "tdg_ptx.cuh"
+
+struct tdg_symm {
+    uint8_t *base;
+    size_t bytes;
+    int world;
+    size_t region_bytes;
+    size_t nsig;            // flag words (and counter words) per rank
+    uint32_t *flags;        // world * nsig
+    uint32_t *counters;     // world * nsig
+    tdg::DevStatus *status; // one status block
+    uint32_t epoch;         // last epoch handed out
+    int device;
+    int sm_count;
+};
+
+namespace tdg_host {
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// next nonzero epoch of the handle
+inline uint32_t next_epoch(tdg_symm *h)
+{
+    h->epoch += 1;
+    if (h->epoch == 0)
+        h->epoch = 1;
+    return h->epoch;
+}
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool aligned16(size_t v) { return (v & 15u) == 0; }
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// dependency on libcuda).  Returns false on failure.
+bool encode_tiled(CUtensorMap *m, CUtensorMapDataType dt, int rank, const void *base,
+                  const uint64_t *dims, const uint64_t *strides_bytes /* rank-1 */,
+                  const uint32_t *box, CUtensorMapSwizzle swz);
+
+// bf16 2-D map: inner (contiguous) extent, outer extent, row pitch in bytes.
+bool map_bf16_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer,
+                 uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);
+// bf16 3-D map (dim 2 stride given in bytes, e.g. the region size).
+bool map_bf16_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2,
+                 uint64_t s1_bytes, uint64_t s2_bytes, uint32_t b0, uint32_t b1, uint32_t b2);
+
+// cuStreamWriteValue32 (stream-ordered flag write, with the default memory
+// barrier before the write).  Returns false when unavailable or failing.
+bool stream_write_u32(cudaStream_t s, uint32_t *dev_addr, uint32_t value);
+
+// Opt a kernel into the large dynamic shared memory it needs (once per
+// function and device).
+cudaError_t set_smem(const void *fn, int bytes);
+
+// Launch with the cooperative attribute (all CTAs co-resident, which the
+// cross-CTA signal waits rely on).
+cudaError_t launch(const void *fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                   void **args, bool cooperative);
+
+int occupancy_ok(const void *fn, int block, int smem, int grid, int sm_count);
+
+inline int cuda_err(cudaError_t e, const char *what)
+{
+    if (e == cudaSuccess)
+        return TDG_OK;
+    if (getenv("TDG_LOG"))
+        fprintf(stderr, "[tdg] %s: %s\n", what, cudaGetErrorString(e));
+    return TDG_ERR_CUDA;
+}
+
+inline uint64_t timeout_or_default(uint64_t t) { return t ? t : 2000000000ull; }
+
+} // namespace tdg_host

@@ -1,0 +1,324 @@
+// tdg_rs.cu -- tile-centric overlapped GEMM + ReduceScatter ("Triton-distributed
+// 语义", 内核设计模式 "GEMM + ReduceScatter 重叠"; paper summary, 方法: push-mode
+// intra-node ReduceScatter, the reduction running in parallel and synchronised
+// by signals).
+//
+// One persistent tcgen05 GEMM runs every rank's partial product.  Work items
+// are (owner o, rank r, m tile inside o, n tile); by default all ranks'
+// items of one owner block run back to back, so every output tile gathers
+// its W partials close together in time.  The epilogue pushes each bf16
+// partial tile (tile-contiguous, 128 x 256) into owner o's staging area
+// (region o) with TMA, waits for the write to complete, fences the async
+// proxy, and increments the owner's per-(tile, row-quarter) arrival counter
+// with acq_rel semantics (the pages' "increment" signal).  The epilogue warp
+// whose increment completes the count of W acquires the other W-1 pushes,
+// sums the W partials of its 32 rows in fixed rank order (fp32, 16-byte
+// coalesced loads), writes the bf16 rows of out_o and resets the counter.
+// No CTA ever spins on another: the last arriver does the work.
+// SERIAL mode: the GEMM stores every partial, then a separate reduction
+// launch (all SMs) sums them -- same arithmetic, no overlap.
+#include "tdg_gemm.cuh"
+#include "tdg_internal.h"
+
+namespace tdg {
+
+struct RsParams {
+    CUtensorMap tmA; // {K, M, W}, plane stride = region bytes, box {64, 128, 1}
+    CUtensorMap tmB; // KN: {N, K, W} box {64, 64, 1}; NK: {K, N, W} box {64, 256, 1}
+    CUtensorMap tmS; // staging {256, rows per owner, W}, box {64, 32, 1}
+    DevStatus *status;
+    uint32_t epoch;
+    uint64_t timeout_ns;
+    int k_blocks;
+    int W;
+    int64_t M, K, N, Mo;
+    int mt;      // m tiles per owner (Mo / 128)
+    int n_tiles;
+    int order;   // 0: owner, rank, m, n (rank outside m, n); 1: rank fastest
+    int fused_reduce;
+    uint8_t *regions;
+    uint64_t region_bytes;
+    uint64_t stage_off, out_off;
+    uint32_t *counters;
+    uint64_t nsig;
+};
+
+__device__ __forceinline__ uint8_t *rs_stage_row(const RsParams &p, int o, int r, int m_loc, int pn, int row)
+{
+    const uint64_t idx = ((uint64_t)r * p.mt + m_loc) * p.n_tiles + pn;
+    return p.regions + (uint64_t)o * p.region_bytes + p.stage_off + (idx * 128 + row) * 512;
+}
+
+// Sum the W partial rows [row0, row0 + 32) of tile (o, m_loc, pn) in rank
+// order and write the bf16 result into out_o.  One warp; lane l owns columns
+// [8l, 8l + 8) of the tile.
+__device__ void rs_reduce_rows(const RsParams &p, int o, int m_loc, int pn, int n_valid, int row0, int lane)
+{
+    const int col = lane * 8;
+    if (col >= n_valid)
+        return;
+    uint8_t *out_base = p.regions + (uint64_t)o * p.region_bytes + p.out_off;
+    const int64_t n0 = (int64_t)pn * gm::BN;
+    for (int rr = 0; rr < 32; rr += 2) {
+        float acc[2][8];
+#pragma unroll
+        for (int a = 0; a < 2; ++a)
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                acc[a][j] = 0.f;
+        for (int r0 = 0; r0 < p.W; r0 += 8) {
+            uint4 v[2][8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                if (r0 + j < p.W) {
+#pragma unroll
+                    for (int a = 0; a < 2; ++a)
+                        v[a][j] = __ldcg(reinterpret_cast<const uint4 *>(
+                            rs_stage_row(p, o, r0 + j, m_loc, pn, row0 + rr + a) + col * 2));
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                if (r0 + j < p.W) {
+#pragma unroll
+                    for (int a = 0; a < 2; ++a) {
+                        const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&v[a][j]);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 f = __bfloat1622float2(h[e]);
+                            acc[a][2 * e] += f.x;
+                            acc[a][2 * e + 1] += f.y;
+                        }
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int a = 0; a < 2; ++a) {
+            const int64_t orow = (int64_t)m_loc * gm::BM + row0 + rr + a;
+            uint4 w;
+            w.x = pack_bf16x2(acc[a][0], acc[a][1]);
+            w.y = pack_bf16x2(acc[a][2], acc[a][3]);
+            w.z = pack_bf16x2(acc[a][4], acc[a][5]);
+            w.w = pack_bf16x2(acc[a][6], acc[a][7]);
+            *reinterpret_cast<uint4 *>(out_base + ((uint64_t)orow * p.N + n0 + col) * 2) = w;
+        }
+    }
+}
+
+template <int BMN> struct RsPolicy {
+    using Params = RsParams;
+    static constexpr int B_MN = BMN;
+
+    __device__ static int64_t num_items(const Params &p)
+    {
+        return (int64_t)p.W * p.W * p.mt * p.n_tiles;
+    }
+
+    __device__ static void tile(const Params &p, int64_t item, TileInfo &t)
+    {
+        const int64_t per_rank = (int64_t)p.mt * p.n_tiles;
+        int o, r;
+        int64_t rem;
+        if (p.order == 1) {
+            r = (int)(item % p.W);
+            const int64_t rest = item / p.W;
+            o = (int)(rest / per_rank);
+            rem = rest % per_rank;
+        } else {
+            const int64_t per_owner = (int64_t)p.W * per_rank;
+            o = (int)(item / per_owner);
+            const int64_t x = item % per_owner;
+            r = (int)(x / per_rank);
+            rem = x % per_rank;
+        }
+        t.owner = o;
+        t.a_sel = r;
+        t.m_loc = (int)(rem / p.n_tiles);
+        t.pn = (int)(rem % p.n_tiles);
+        t.m0 = (o * p.mt + t.m_loc) * gm::BM;
+        t.a_row = t.m0;
+        t.n0 = t.pn * gm::BN;
+        t.n_valid = (int)min((int64_t)gm::BN, p.N - t.n0);
+    }
+
+    __device__ static void before_a(const Params &, const TileInfo &, bool &) {}
+
+    __device__ static void load_a(const Params &p, const TileInfo &t, void *dst, uint64_t *bar, int kb)
+    {
+        tma_load_3d(dst, &p.tmA, bar, kb * gm::BK, t.a_row, t.a_sel);
+    }
+
+    __device__ static void load_b(const Params &p, const TileInfo &t, void *dst, uint64_t *bar, int kb)
+    {
+        if (BMN) {
+            const int nch = (t.n_valid + 63) >> 6;
+            for (int j = 0; j < nch; ++j)
+                tma_load_3d(static_cast<uint8_t *>(dst) + j * 8192, &p.tmB, bar, t.n0 + 64 * j,
+                            kb * gm::BK, t.a_sel);
+        } else {
+            tma_load_3d(dst, &p.tmB, bar, kb * gm::BK, t.n0, t.a_sel);
+        }
+    }
+
+    __device__ static uint32_t b_bytes(const TileInfo &t)
+    {
+        return BMN ? (uint32_t)(((t.n_valid + 63) >> 6) * 8192) : (uint32_t)gm::B_BYTES;
+    }
+
+    // push: the partial tile goes to the owner's staging area
+    __device__ static void store_chunk(const Params &p, const TileInfo &t, const void *buf, int ch, int q)
+    {
+        const uint64_t idx = ((uint64_t)t.a_sel * p.mt + t.m_loc) * p.n_tiles + t.pn;
+        tma_store_3d(&p.tmS, buf, 64 * ch, (int)(idx * 128 + 32 * q), t.owner);
+    }
+
+    __device__ static void after_tile(const Params &p, const TileInfo &t, int q, int lane)
+    {
+        if (!p.fused_reduce)
+            return;
+        uint32_t *ctr = p.counters + (uint64_t)t.owner * p.nsig +
+                        ((uint64_t)t.m_loc * p.n_tiles + t.pn) * 4 + q;
+        uint32_t old = 0;
+        if (lane == 0) {
+            bulk_wait<0>();             // this warp's pushed rows are written ...
+            fence_proxy_async_global(); // ... and ordered before the signal
+            old = atom_add_acq_rel_gpu(ctr, 1u);
+        }
+        old = __shfl_sync(0xffffffffu, old, 0);
+        if (old != (uint32_t)(p.W - 1))
+            return;
+        __threadfence();
+        rs_reduce_rows(p, t.owner, t.m_loc, t.pn, t.n_valid, 32 * q, lane);
+        __syncwarp();
+        if (lane == 0)
+            st_relaxed_gpu(ctr, 0u);
+    }
+};
+
+template <int BMN>
+__global__ void __launch_bounds__(gm::NUM_THREADS, 1) rs_gemm_kernel(const __grid_constant__ RsParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = align1024(smem_raw);
+    gemm_consumer<RsPolicy<BMN>>(p, smem, (int)blockIdx.x, (int)gridDim.x);
+}
+
+// SERIAL reduction: one 4-warp CTA per output tile.
+__global__ void __launch_bounds__(128) rs_reduce_kernel(const __grid_constant__ RsParams p)
+{
+    const int64_t tile = blockIdx.x;
+    const int per_owner = p.mt * p.n_tiles;
+    const int o = (int)(tile / per_owner);
+    const int rem = (int)(tile % per_owner);
+    const int m_loc = rem / p.n_tiles, pn = rem % p.n_tiles;
+    const int n_valid = (int)min((int64_t)gm::BN, p.N - (int64_t)pn * gm::BN);
+    rs_reduce_rows(p, o, m_loc, pn, n_valid, 32 * (threadIdx.x >> 5), threadIdx.x & 31);
+}
+
+} // namespace tdg
+
+using namespace tdg;
+using namespace tdg_host;
+
+extern "C" size_t tdg_gemm_rs_stage_bytes(int world, int64_t M, int64_t N)
+{
+    if (world <= 0 || M <= 0 || N <= 0 || M % world)
+        return 0;
+    const int64_t Mo = M / world;
+    const int64_t mt = (Mo + gm::BM - 1) / gm::BM;
+    const int64_t nt = (N + gm::BN - 1) / gm::BN;
+    return (size_t)world * mt * nt * gm::BM * gm::BN * 2;
+}
+
+extern "C" int tdg_gemm_rs(tdg_symm *h, const tdg_gemm_rs_args *a, void *stream)
+{
+    if (!h || !a)
+        return TDG_ERR_INVALID;
+    const int W = a->world;
+    if (W != h->world || a->M < 0 || a->K < 0 || a->N < 0)
+        return TDG_ERR_INVALID;
+    if (a->mode != TDG_MODE_SM && a->mode != TDG_MODE_SERIAL)
+        return TDG_ERR_INVALID;
+    if (a->b_layout != TDG_B_KN && a->b_layout != TDG_B_NK)
+        return TDG_ERR_INVALID;
+    const int64_t M = a->M, K = a->K, N = a->N;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (M == 0 || N == 0)
+        return TDG_OK;
+    if (M % W)
+        return TDG_ERR_INVALID;
+    const int64_t Mo = M / W;
+    if (Mo % gm::BM || K % 8 || N % 8 || !aligned16(a->a_off) || !aligned16(a->b_off) ||
+        !aligned16(a->stage_off) || !aligned16(a->out_off) || M > INT32_MAX || K > INT32_MAX ||
+        N > INT32_MAX)
+        return TDG_ERR_INVALID;
+    const size_t stage_bytes = tdg_gemm_rs_stage_bytes(W, M, N);
+    const uint64_t R = h->region_bytes;
+    if (a->a_off + (uint64_t)M * K * 2 > R || a->b_off + (uint64_t)K * N * 2 > R ||
+        a->stage_off + stage_bytes > R || a->out_off + (uint64_t)Mo * N * 2 > R)
+        return TDG_ERR_NOMEM;
+    const int mt = (int)(Mo / gm::BM);
+    const int n_tiles = (int)((N + gm::BN - 1) / gm::BN);
+    if ((size_t)mt * n_tiles * 4 > h->nsig)
+        return TDG_ERR_NOMEM;
+    if (K == 0) {
+        for (int o = 0; o < W; ++o) {
+            cudaError_t e = cudaMemsetAsync(h->base + (size_t)o * R + a->out_off, 0, (size_t)Mo * N * 2, s);
+            if (e != cudaSuccess)
+                return cuda_err(e, "rs K==0");
+        }
+        return TDG_OK;
+    }
+
+    RsParams p;
+    memset(&p, 0, sizeof p);
+    bool ok = map_bf16_3d(&p.tmA, h->base + a->a_off, K, M, W, K * 2, R, 64, gm::BM, 1);
+    if (a->b_layout == TDG_B_KN)
+        ok = ok && map_bf16_3d(&p.tmB, h->base + a->b_off, N, K, W, N * 2, R, 64, 64, 1);
+    else
+        ok = ok && map_bf16_3d(&p.tmB, h->base + a->b_off, K, N, W, K * 2, R, 64, 256, 1);
+    const uint64_t rows_per_owner = (uint64_t)W * mt * n_tiles * gm::BM;
+    ok = ok && map_bf16_3d(&p.tmS, h->base + a->stage_off, gm::BN, rows_per_owner, W, gm::BN * 2, R, 64, 32, 1);
+    if (!ok)
+        return TDG_ERR_CUDA;
+    p.status = h->status;
+    p.epoch = next_epoch(h);
+    p.timeout_ns = timeout_or_default(a->timeout_ns);
+    p.k_blocks = (int)((K + gm::BK - 1) / gm::BK);
+    p.W = W;
+    p.M = M;
+    p.K = K;
+    p.N = N;
+    p.Mo = Mo;
+    p.mt = mt;
+    p.n_tiles = n_tiles;
+    p.order = getenv("TDG_RS_ORDER") ? atoi(getenv("TDG_RS_ORDER")) : 0;
+    p.fused_reduce = a->mode == TDG_MODE_SM ? 1 : 0;
+    p.regions = h->base;
+    p.region_bytes = R;
+    p.stage_off = a->stage_off;
+    p.out_off = a->out_off;
+    p.counters = h->counters;
+    p.nsig = h->nsig;
+
+    const void *fn = a->b_layout == TDG_B_KN ? reinterpret_cast<const void *>(&rs_gemm_kernel<1>)
+                                             : reinterpret_cast<const void *>(&rs_gemm_kernel<0>);
+    static bool smem_set[2][64] = {};
+    bool &done = smem_set[a->b_layout & 1][h->device & 63];
+    if (!done) {
+        cudaError_t e = set_smem(fn, gm::SMEM_BYTES);
+        if (e != cudaSuccess)
+            return cuda_err(e, "rs set smem");
+        done = true;
+    }
+    void *args[] = {&p};
+    int rc = cuda_err(launch(fn, dim3(h->sm_count), dim3(gm::NUM_THREADS), gm::SMEM_BYTES, s, args, false),
+                      "rs gemm launch");
+    if (rc != TDG_OK || a->mode == TDG_MODE_SM)
+        return rc;
+    const unsigned tiles = (unsigned)(W * mt * n_tiles);
+    return cuda_err(launch(reinterpret_cast<const void *>(&rs_reduce_kernel), dim3(tiles), dim3(128), 0, s,
+                           args, false),
+                    "rs reduce launch");
+}

@@ -1,0 +1,256 @@
+"""Thin ctypes binding of libtdg (include/tdg.h).  Argument marshalling only:
+every step of the path runs in the library's CUDA kernels.  PyTorch supplies
+device memory and streams.
+
+The library must have been built (``python -m tile_centric_comm_gb300.build``
+or ``__graft_entry__.build()``); when it is missing every call raises -- there
+is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "_build", "libtdg.so")
+
+TDG_OK = 0
+TDG_ERR_INVALID = -1
+TDG_ERR_CUDA = -2
+TDG_ERR_NOMEM = -3
+TDG_ERR_TIMEOUT = -4
+TDG_ERR_UNSUPPORTED = -5
+TDG_ERR_DEVICE = -6
+
+MODE_SM, MODE_CE, MODE_LL, MODE_SERIAL = 0, 1, 2, 3
+MODES = {"sm": MODE_SM, "ce": MODE_CE, "ll": MODE_LL, "serial": MODE_SERIAL}
+B_KN, B_NK = 0, 1
+MOE_ROUTE, MOE_DISPATCH, MOE_COMBINE, MOE_ALL = 1, 2, 4, 7
+WHERE = {1: "ag_flag", 2: "pipe", 3: "ll", 4: "moe_expert"}
+
+# every symbol include/tdg.h declares
+EXPORTS = [
+    "tdg_symm_bytes", "tdg_symm_alloc", "tdg_symm_free", "tdg_symm_region", "tdg_symm_at",
+    "tdg_symm_flags", "tdg_symm_counters", "tdg_symm_epoch", "tdg_status", "tdg_strerror",
+    "tdg_device_info", "tdg_ag_gemm", "tdg_gemm_rs_stage_bytes", "tdg_gemm_rs",
+    "tdg_moe_workspace_bytes", "tdg_moe_dispatch_combine",
+]
+
+_i32, _i64, _u32, _u64 = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32, ctypes.c_uint64
+_sz, _vp = ctypes.c_size_t, ctypes.c_void_p
+
+
+class TdgFault(ctypes.Structure):
+    _fields_ = [("code", _i32), ("where", _u32), ("index", _u32), ("epoch", _u32)]
+
+
+class AgGemmArgs(ctypes.Structure):
+    _fields_ = [("world", ctypes.c_int), ("rank", ctypes.c_int), ("Ms", _i64), ("K", _i64),
+                ("N", _i64), ("a_off", _sz), ("g_off", _sz), ("B", _vp), ("C", _vp),
+                ("b_layout", ctypes.c_int), ("mode", ctypes.c_int), ("producers", ctypes.c_int),
+                ("signal_rows", _i64), ("swizzle", ctypes.c_int), ("timeout_ns", _u64),
+                ("ll_off", _sz), ("test_skip_notify", _u64)]
+
+
+class GemmRsArgs(ctypes.Structure):
+    _fields_ = [("world", ctypes.c_int), ("M", _i64), ("K", _i64), ("N", _i64), ("a_off", _sz),
+                ("b_off", _sz), ("stage_off", _sz), ("out_off", _sz), ("b_layout", ctypes.c_int),
+                ("mode", ctypes.c_int), ("timeout_ns", _u64)]
+
+
+class MoeArgs(ctypes.Structure):
+    _fields_ = [("world", ctypes.c_int), ("T", _i64), ("H", _i64), ("E", ctypes.c_int),
+                ("k", ctypes.c_int), ("x_off", _sz), ("topk_off", _sz), ("gate_off", _sz),
+                ("out_off", _sz), ("recv", _vp), ("y", _vp), ("counts", _vp), ("base", _vp),
+                ("slot", _vp), ("row_src", _vp), ("row_tok", _vp), ("row_k", _vp),
+                ("workspace", _vp), ("workspace_bytes", _sz), ("phases", ctypes.c_int)]
+
+
+class TdgError(RuntimeError):
+    def __init__(self, code, what):
+        self.code = code
+        super().__init__(f"{what}: {strerror(code)} ({code})")
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def lib():
+    """Open libtdg.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"libtdg.so not found at {LIB_PATH}: build it with "
+                    "`python -m tile_centric_comm_gb300.build` (there is no CPU fallback)")
+            L = ctypes.CDLL(LIB_PATH)
+            L.tdg_symm_bytes.restype = _sz
+            L.tdg_symm_bytes.argtypes = [ctypes.c_int, _sz, _sz]
+            L.tdg_symm_alloc.restype = ctypes.c_int
+            L.tdg_symm_alloc.argtypes = [_vp, _sz, ctypes.c_int, _sz, _sz, ctypes.POINTER(_vp)]
+            L.tdg_symm_free.restype = ctypes.c_int
+            L.tdg_symm_free.argtypes = [_vp]
+            for n in ("tdg_symm_region", "tdg_symm_flags", "tdg_symm_counters"):
+                getattr(L, n).restype = _vp
+                getattr(L, n).argtypes = [_vp, ctypes.c_int]
+            L.tdg_symm_at.restype = _vp
+            L.tdg_symm_at.argtypes = [_vp, _vp, ctypes.c_int]
+            L.tdg_symm_epoch.restype = _u32
+            L.tdg_symm_epoch.argtypes = [_vp]
+            L.tdg_status.restype = ctypes.c_int
+            L.tdg_status.argtypes = [_vp, _vp, ctypes.POINTER(TdgFault), ctypes.c_int]
+            L.tdg_strerror.restype = ctypes.c_char_p
+            L.tdg_strerror.argtypes = [ctypes.c_int]
+            L.tdg_device_info.restype = ctypes.c_int
+            L.tdg_device_info.argtypes = [ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]
+            L.tdg_ag_gemm.restype = ctypes.c_int
+            L.tdg_ag_gemm.argtypes = [_vp, ctypes.POINTER(AgGemmArgs), _vp, _vp]
+            L.tdg_gemm_rs_stage_bytes.restype = _sz
+            L.tdg_gemm_rs_stage_bytes.argtypes = [ctypes.c_int, _i64, _i64]
+            L.tdg_gemm_rs.restype = ctypes.c_int
+            L.tdg_gemm_rs.argtypes = [_vp, ctypes.POINTER(GemmRsArgs), _vp]
+            L.tdg_moe_workspace_bytes.restype = _sz
+            L.tdg_moe_workspace_bytes.argtypes = [ctypes.c_int, _i64, ctypes.c_int]
+            L.tdg_moe_dispatch_combine.restype = ctypes.c_int
+            L.tdg_moe_dispatch_combine.argtypes = [_vp, ctypes.POINTER(MoeArgs), _vp]
+            _lib = L
+    return _lib
+
+
+def strerror(code: int) -> str:
+    return lib().tdg_strerror(code).decode()
+
+
+def _check(rc, what):
+    if rc != TDG_OK:
+        raise TdgError(rc, what)
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return _vp(stream.cuda_stream)
+
+
+def device_info():
+    sms, sup = ctypes.c_int(0), ctypes.c_int(0)
+    _check(lib().tdg_device_info(ctypes.byref(sms), ctypes.byref(sup)), "tdg_device_info")
+    return sms.value, bool(sup.value)
+
+
+class Symm:
+    """A symmetric heap of `world` regions carved from one torch allocation."""
+
+    def __init__(self, world: int, region_bytes: int, signals_per_rank: int = 65536,
+                 device=None, buffer=None):
+        import torch
+        region_bytes = (int(region_bytes) + 1023) // 1024 * 1024
+        L = lib()
+        nbytes = L.tdg_symm_bytes(world, region_bytes, signals_per_rank)
+        if buffer is None:
+            buffer = torch.empty(nbytes + 1024, dtype=torch.uint8, device=device or "cuda")
+        self.buf = buffer
+        self.base_off = (-buffer.data_ptr()) % 1024
+        self.base = buffer.data_ptr() + self.base_off
+        self.nbytes = nbytes
+        self.world = world
+        self.region_bytes = region_bytes
+        self.nsig = signals_per_rank
+        h = _vp()
+        _check(L.tdg_symm_alloc(_vp(self.base), nbytes, world, region_bytes, signals_per_rank,
+                                ctypes.byref(h)), "tdg_symm_alloc")
+        self.h = h
+
+    def close(self):
+        if getattr(self, "h", None):
+            lib().tdg_symm_free(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def region_ptr(self, rank: int) -> int:
+        return lib().tdg_symm_region(self.h, rank)
+
+    def view(self, rank: int, off: int, shape, dtype):
+        """A tensor over region `rank` at byte offset `off`."""
+        import torch
+        n = 1
+        for d in shape:
+            n *= int(d)
+        esz = torch.empty((), dtype=dtype).element_size()
+        assert off % esz == 0 and off + n * esz <= self.region_bytes
+        start = self.base_off + rank * self.region_bytes + off
+        return self.buf[start:start + n * esz].view(dtype).view(*shape)
+
+    def flags(self, rank: int, n: int):
+        import torch
+        start = lib().tdg_symm_flags(self.h, rank) - self.buf.data_ptr()
+        return self.buf[start:start + 4 * n].view(torch.int32)
+
+    def counters(self, rank: int, n: int):
+        import torch
+        start = lib().tdg_symm_counters(self.h, rank) - self.buf.data_ptr()
+        return self.buf[start:start + 4 * n].view(torch.int32)
+
+    def at(self, ptr: int, rank: int):
+        return lib().tdg_symm_at(self.h, _vp(ptr), rank)
+
+    def epoch(self) -> int:
+        return lib().tdg_symm_epoch(self.h)
+
+    def status(self, stream=None, clear: bool = True):
+        f = TdgFault()
+        rc = lib().tdg_status(self.h, _stream(stream), ctypes.byref(f), 1 if clear else 0)
+        if rc == TDG_ERR_CUDA:
+            raise TdgError(rc, "tdg_status")
+        return dict(code=f.code, where=WHERE.get(f.where, f.where), index=f.index, epoch=f.epoch)
+
+
+def ag_gemm(symm: Symm, rank: int, Ms: int, K: int, N: int, a_off: int, g_off: int, B, C,
+            mode="sm", b_layout=B_KN, producers=0, signal_rows=0, swizzle=True,
+            timeout_ns=0, ll_off=0, test_skip_notify=0, stream=None, side_stream=None):
+    a = AgGemmArgs(world=symm.world, rank=rank, Ms=Ms, K=K, N=N, a_off=a_off, g_off=g_off,
+                   B=B.data_ptr(), C=C.data_ptr(), b_layout=b_layout, mode=MODES[mode],
+                   producers=producers, signal_rows=signal_rows, swizzle=1 if swizzle else 0,
+                   timeout_ns=timeout_ns, ll_off=ll_off, test_skip_notify=test_skip_notify)
+    side = _vp(side_stream.cuda_stream) if side_stream is not None else _vp(None)
+    _check(lib().tdg_ag_gemm(symm.h, ctypes.byref(a), _stream(stream), side), "tdg_ag_gemm")
+
+
+def gemm_rs_stage_bytes(world: int, M: int, N: int) -> int:
+    return lib().tdg_gemm_rs_stage_bytes(world, M, N)
+
+
+def gemm_rs(symm: Symm, M: int, K: int, N: int, a_off: int, b_off: int, stage_off: int,
+            out_off: int, mode="sm", b_layout=B_KN, timeout_ns=0, stream=None):
+    a = GemmRsArgs(world=symm.world, M=M, K=K, N=N, a_off=a_off, b_off=b_off,
+                   stage_off=stage_off, out_off=out_off, b_layout=b_layout,
+                   mode=MODES[mode], timeout_ns=timeout_ns)
+    _check(lib().tdg_gemm_rs(symm.h, ctypes.byref(a), _stream(stream)), "tdg_gemm_rs")
+
+
+def moe_workspace_bytes(world: int, T: int, E: int) -> int:
+    return lib().tdg_moe_workspace_bytes(world, T, E)
+
+
+def moe_dispatch_combine(symm: Symm, T: int, H: int, E: int, k: int, x_off: int, topk_off: int,
+                         gate_off: int, out_off: int, recv, counts, base, slot, workspace,
+                         y=None, row_src=None, row_tok=None, row_k=None, phases=MOE_ALL,
+                         stream=None):
+    def p(t):
+        return t.data_ptr() if t is not None else None
+    a = MoeArgs(world=symm.world, T=T, H=H, E=E, k=k, x_off=x_off, topk_off=topk_off,
+                gate_off=gate_off, out_off=out_off, recv=p(recv), y=p(y), counts=p(counts),
+                base=p(base), slot=p(slot), row_src=p(row_src), row_tok=p(row_tok),
+                row_k=p(row_k), workspace=p(workspace),
+                workspace_bytes=workspace.numel() * workspace.element_size(), phases=phases)
+    _check(lib().tdg_moe_dispatch_combine(symm.h, ctypes.byref(a), _stream(stream)),
+           "tdg_moe_dispatch_combine")
