@@ -1,0 +1,469 @@
+"""Benchmark of the tile-centric hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl tdg|reference]
+
+Workload (one "step"): the tensor-parallel MLP layer of Qwen-32B over W=8
+logical ranks held in one GPU -- AllGather+GEMM of the up-projection
+(A_r 1024x5120 per rank, B 5120x3200) followed by GEMM+ReduceScatter of the
+down-projection (A_r 8192x3200, B_r 3200x5120 per rank).  Metric: TFLOP/s of
+the two operations together (2*M*N*K counted once per GEMM), with inputs
+resident in HBM; L2 is flushed (256 MB write) before every timed step.  The
+same run also reports the overlap gain against the serial composition (copy,
+then GEMM, then reduce), the end-to-end rate with host buffers, the MoE
+dispatch+combine bandwidth, the roofline of the dominant kernel and the CPU
+oracle's rate on a bounded sample.
+
+--impl reference times the CPU oracle on a bounded sample of the same
+workload each step (the reference arm for this path is the oracle).
+Under torchrun (N > 1) every rank runs its own replica; rank 0 prints the
+JSON line with the max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+AG = dict(W=8, Ms=1024, K=5120, N=3200)          # Qwen-32B MLP up-projection
+RS = dict(W=8, M=8192, K=3200, N=5120)           # Qwen-32B MLP down-projection
+MOE = dict(W=8, T=4096, H=7168, E=256, k=8)      # MoE dispatch + combine
+AG_FLOP = 2 * AG["W"] * AG["Ms"] * AG["K"] * AG["N"]
+RS_FLOP = 2 * RS["W"] * RS["M"] * RS["K"] * RS["N"]
+STEP_FLOP = AG_FLOP + RS_FLOP
+WORKLOAD = ("qwen32b_mlp_tp8: AG-GEMM up-proj (W=8, A_r 1024x5120, B 5120x3200) + "
+            "GEMM-RS down-proj (W=8, A_r 8192x3200, B_r 3200x5120), bf16 in, fp32 accumulate, bf16 out")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="tdg", choices=["tdg", "reference"])
+    ap.add_argument("--mode", default="sm", choices=["sm", "ce"])
+    ap.add_argument("--producers", type=int, default=0)
+    ap.add_argument("--no-extras", action="store_true", help="skip serial/e2e/MoE/CPU legs")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--only", default="", help="debug: 'ag' or 'rs' alone")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm=d["hbm_gbs"], bf16=d["bf16_tflops"], bf16_sus=d["bf16_tflops_sustained"],
+                    src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+class Clocks:
+    """nvidia-smi samples during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        pw = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        loaded = [s for s, p in zip(sm, pw) if p > 300] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(rows), "power_w_max": max(pw) if pw else None}
+
+
+# ------------------------------------------------------------ GPU workload ----
+def _dev_bf16(bits, torch):
+    import numpy as np
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def _align(x, a=1024):
+    return (x + a - 1) // a * a
+
+
+class MLP:
+    """Inputs of both operations resident in two symmetric heaps."""
+
+    def __init__(self, torch, tdg, synth, mode, producers):
+        self.torch, self.tdg, self.mode, self.producers = torch, tdg, mode, producers
+        ag = synth.ag_inputs(AG["W"], AG["Ms"], AG["K"], AG["N"], "normal", seed=0)
+        W, Ms, K, N = AG["W"], AG["Ms"], AG["K"], AG["N"]
+        self.ag_a_off = 0
+        self.ag_g_off = _align(Ms * K * 2)
+        self.ag = tdg.Symm(W, _align(self.ag_g_off + W * Ms * K * 2 + 1024), 65536)
+        self.ag_host = [torch.from_numpy(a.view("int16")).view(torch.bfloat16).pin_memory()
+                        for a in ag.shards]
+        for s in range(W):
+            self.ag.view(s, 0, (Ms, K), torch.bfloat16).copy_(self.ag_host[s])
+        self.ag_B_host = torch.from_numpy(ag.B.view("int16")).view(torch.bfloat16).pin_memory()
+        self.ag_B = self.ag_B_host.cuda()
+        self.ag_C = torch.empty((W * Ms, N), dtype=torch.bfloat16, device="cuda")
+        del ag
+        rs = synth.rs_inputs(RS["W"], RS["M"], RS["K"], RS["N"], "normal", seed=0)
+        W, M, K, N = RS["W"], RS["M"], RS["K"], RS["N"]
+        self.rs_a_off = 0
+        self.rs_b_off = _align(M * K * 2)
+        self.rs_s_off = _align(self.rs_b_off + K * N * 2)
+        self.rs_o_off = _align(self.rs_s_off + tdg.gemm_rs_stage_bytes(W, M, N))
+        self.rs = tdg.Symm(W, _align(self.rs_o_off + (M // W) * N * 2 + 1024), 65536)
+        self.rs_A_host = [torch.from_numpy(a.view("int16")).view(torch.bfloat16).pin_memory() for a in rs.As]
+        self.rs_B_host = [torch.from_numpy(b.view("int16")).view(torch.bfloat16).pin_memory() for b in rs.Bs]
+        for r in range(W):
+            self.rs.view(r, self.rs_a_off, (M, K), torch.bfloat16).copy_(self.rs_A_host[r])
+            self.rs.view(r, self.rs_b_off, (K, N), torch.bfloat16).copy_(self.rs_B_host[r])
+        del rs
+        self.C_host = torch.empty((AG["W"] * AG["Ms"], AG["N"]), dtype=torch.bfloat16).pin_memory()
+        self.out_host = torch.empty((RS["W"], RS["M"] // RS["W"], RS["N"]),
+                                    dtype=torch.bfloat16).pin_memory()
+        self.h2d_bytes = (sum(t.numel() for t in self.ag_host) + self.ag_B_host.numel()
+                          + sum(t.numel() for t in self.rs_A_host)
+                          + sum(t.numel() for t in self.rs_B_host)) * 2
+        self.d2h_bytes = (self.C_host.numel() + self.out_host.numel()) * 2
+
+    def ag_call(self, mode=None, side=None):
+        mode = mode or self.mode
+        if mode == "ce" and side is None:
+            side = self._side()
+        self.tdg.ag_gemm(self.ag, 0, AG["Ms"], AG["K"], AG["N"], self.ag_a_off, self.ag_g_off,
+                         self.ag_B, self.ag_C, mode=mode, producers=self.producers, side_stream=side)
+
+    def _side(self):
+        if not hasattr(self, "_side_stream"):
+            self._side_stream = self.torch.cuda.Stream()
+        return self._side_stream
+
+    def rs_call(self, mode="sm"):
+        self.tdg.gemm_rs(self.rs, RS["M"], RS["K"], RS["N"], self.rs_a_off, self.rs_b_off,
+                         self.rs_s_off, self.rs_o_off, mode=mode)
+
+    def upload(self):
+        """host -> device copies of one step's inputs (pinned, async)."""
+        t = self.torch
+        Ms, K = AG["Ms"], AG["K"]
+        for s in range(AG["W"]):
+            self.ag.view(s, 0, (Ms, K), t.bfloat16).copy_(self.ag_host[s], non_blocking=True)
+        self.ag_B.copy_(self.ag_B_host, non_blocking=True)
+        M, K, N = RS["M"], RS["K"], RS["N"]
+        for r in range(RS["W"]):
+            self.rs.view(r, self.rs_a_off, (M, K), t.bfloat16).copy_(self.rs_A_host[r], non_blocking=True)
+            self.rs.view(r, self.rs_b_off, (K, N), t.bfloat16).copy_(self.rs_B_host[r], non_blocking=True)
+
+    def download(self):
+        self.C_host.copy_(self.ag_C, non_blocking=True)
+        Mo, N = RS["M"] // RS["W"], RS["N"]
+        for o in range(RS["W"]):
+            self.out_host[o].copy_(self.rs.view(o, self.rs_o_off, (Mo, N), self.torch.bfloat16),
+                                   non_blocking=True)
+
+    def check_status(self):
+        for s in (self.ag, self.rs):
+            st = s.status()
+            if st["code"] != 0:
+                raise RuntimeError(f"device fault during the bench: {st}")
+
+
+def timed_steps(torch, fns, steps, warmup, flush):
+    """Run `fns` (list of callables, one part each) per step; flush L2 before
+    every step; return per-part lists of device times (ms) for the timed steps."""
+    n = len(fns)
+    stream = torch.cuda.current_stream()
+    res = [[] for _ in range(n)]
+    for it in range(warmup + steps):
+        flush.zero_()
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+        evs[0].record(stream)
+        for i, f in enumerate(fns):
+            f()
+            evs[i + 1].record(stream)
+        if it >= warmup:
+            res_it = evs
+            torch.cuda.synchronize()
+            for i in range(n):
+                res[i].append(res_it[i].elapsed_time(res_it[i + 1]))
+    torch.cuda.synchronize()
+    return res
+
+
+def cpu_oracle_rate(sample_rows_ag=256, sample_rows_rs=64):
+    """The oracle, as it stands, on a bounded sample of the same workload:
+    full output rows of AG-GEMM and GEMM-RS.  Returns (TFLOP/s, seconds, desc)."""
+    import numpy as np
+    import oracle
+    from tile_centric_comm_gb300 import synth
+    ag = synth.ag_inputs(AG["W"], AG["Ms"], AG["K"], AG["N"], "normal", seed=0)
+    rows = np.repeat(np.arange(sample_rows_ag) * 31 % (AG["W"] * AG["Ms"]), AG["N"])
+    cols = np.tile(np.arange(AG["N"]), sample_rows_ag)
+    t0 = time.perf_counter()
+    oracle.ag_gemm_sampled(ag.shards, ag.B, rows, cols)
+    t_ag = time.perf_counter() - t0
+    del ag
+    rs = synth.rs_inputs(RS["W"], RS["M"], RS["K"], RS["N"], "normal", seed=0)
+    rows = np.repeat(np.arange(sample_rows_rs) * 127 % RS["M"], RS["N"])
+    cols = np.tile(np.arange(RS["N"]), sample_rows_rs)
+    t0 = time.perf_counter()
+    oracle.gemm_rs_sampled(rs.As, rs.Bs, rows, cols)
+    t_rs = time.perf_counter() - t0
+    flop = 2.0 * AG["K"] * AG["N"] * sample_rows_ag + 2.0 * RS["W"] * RS["K"] * RS["N"] * sample_rows_rs
+    desc = (f"{sample_rows_ag} full output rows of the AG-GEMM ({sample_rows_ag}x{AG['N']} outputs) + "
+            f"{sample_rows_rs} full output rows of the GEMM-RS ({sample_rows_rs}x{RS['N']} outputs, "
+            f"W={RS['W']} partial sums each), fp64 plain loops")
+    return flop / (t_ag + t_rs) / 1e12, t_ag + t_rs, desc
+
+
+def omp_threads():
+    v = os.environ.get("OMP_NUM_THREADS")
+    return int(v) if v and v.isdigit() else (os.cpu_count() or 1)
+
+
+class MoEBench:
+    """MoE route + dispatch + combine over 8 ranks x 4096 tokens (HBM bound)."""
+
+    def __init__(self, torch, tdg, synth):
+        self.torch, self.tdg = torch, tdg
+        W, T, H, E, k = MOE["W"], MOE["T"], MOE["H"], MOE["E"], MOE["k"]
+        inp = synth.moe_inputs(W, T, H, E, k, seed=0)
+        self.x_off = 0
+        self.topk_off = _align(T * H * 2)
+        self.gate_off = _align(self.topk_off + T * k * 4)
+        self.out_off = _align(self.gate_off + T * k * 4)
+        self.symm = tdg.Symm(W, _align(self.out_off + T * H * 2 + 1024), 1024)
+        import numpy as np
+        for s in range(W):
+            self.symm.view(s, self.x_off, (T, H), torch.bfloat16).copy_(_dev_bf16(inp.x[s], torch))
+            self.symm.view(s, self.topk_off, (T, k), torch.int32).copy_(torch.from_numpy(np.ascontiguousarray(inp.topk[s])))
+            self.symm.view(s, self.gate_off, (T, k), torch.float32).copy_(torch.from_numpy(np.ascontiguousarray(inp.gate[s])))
+        total = W * T * k
+        self.recv = torch.empty((total, H), dtype=torch.bfloat16, device="cuda")
+        self.counts = torch.empty((W, E), dtype=torch.int64, device="cuda")
+        self.base = torch.empty(E + 1, dtype=torch.int64, device="cuda")
+        self.slot = torch.empty((W, T, k), dtype=torch.int64, device="cuda")
+        self.ws = torch.empty(tdg.moe_workspace_bytes(W, T, E), dtype=torch.uint8, device="cuda")
+        row = H * 2
+        self.bytes_dispatch = W * T * row + total * row      # read x once, write k copies
+        self.bytes_combine = total * row + W * T * row       # read k rows, write one
+
+    def call(self, phases):
+        W, T, H, E, k = MOE["W"], MOE["T"], MOE["H"], MOE["E"], MOE["k"]
+        self.tdg.moe_dispatch_combine(self.symm, T, H, E, k, self.x_off, self.topk_off, self.gate_off,
+                                      self.out_off, self.recv, self.counts, self.base, self.slot,
+                                      self.ws, phases=phases)
+
+
+def run_reference(args, rank):
+    """The reference arm: the CPU oracle on a bounded sample per step."""
+    if rank != 0:
+        return
+    rates, secs = [], []
+    desc = ""
+    for it in range(args.warmup + args.steps):
+        r, s, desc = cpu_oracle_rate(sample_rows_ag=8, sample_rows_rs=2)
+        if it >= args.warmup:
+            rates.append(r)
+            secs.append(s)
+    v = statistics.median(rates)
+    line = {"impl": "reference", "metric": "AG-GEMM+GEMM-RS TFLOP/s (qwen32b_mlp_tp8)", "value": v,
+            "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * statistics.mean(secs), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sample": desc},
+            "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": omp_threads(), "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+    import torch
+    from tile_centric_comm_gb300 import synth, tdg
+    torch.cuda.set_device(local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        pg = dist
+    sms, supported = tdg.device_info()
+    if not supported:
+        raise SystemExit("libtdg kernels need an sm_103 device")
+    pk = peaks()
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.int32, device="cuda")
+    mlp = MLP(torch, tdg, synth, args.mode, args.producers)
+    torch.cuda.synchronize()
+
+    fns = [lambda: mlp.ag_call(), lambda: mlp.rs_call("sm")]
+    if args.only == "ag":
+        fns = fns[:1]
+    elif args.only == "rs":
+        fns = fns[1:]
+
+    def barrier():
+        torch.cuda.synchronize()
+        if pg:
+            pg.barrier()
+        torch.cuda.synchronize()
+
+    barrier()
+    with Clocks(local) as clk:
+        parts = timed_steps(torch, fns, args.steps, args.warmup, flush)
+    barrier()
+    mlp.check_status()
+    clocks = clk.summary()
+    step_ms = [sum(p[i] for p in parts) for i in range(args.steps)]
+    total_ms = sum(step_ms)
+    if pg:
+        t = torch.tensor([total_ms], device="cuda")
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    flop = (AG_FLOP if args.only != "rs" else 0) + (RS_FLOP if args.only != "ag" else 0)
+    value = world * flop * args.steps / (total_ms * 1e-3) / 1e12
+    launches = 2 * args.steps if not args.only else args.steps
+    ag_ms = statistics.mean(parts[0]) if args.only != "rs" else None
+    rs_ms = statistics.mean(parts[-1]) if args.only != "ag" else None
+
+    extras = {}
+    e2e = None
+    cpu = None
+    if not args.no_extras and not args.only:
+        # serial composition: same kernels, copy -> GEMM -> reduce
+        sparts = timed_steps(torch, [lambda: mlp.ag_call("serial"), lambda: mlp.rs_call("serial")],
+                             args.steps, args.warmup, flush)
+        s_ag, s_rs = statistics.mean(sparts[0]), statistics.mean(sparts[1])
+        extras["ag_gemm"] = {"ms": ag_ms, "tflops": AG_FLOP / ag_ms / 1e9, "serial_ms": s_ag,
+                             "overlap_gain_vs_serial": s_ag / ag_ms,
+                             "frac_of_bf16_peak": AG_FLOP / ag_ms / 1e9 / pk["bf16"]}
+        extras["gemm_rs"] = {"ms": rs_ms, "tflops": RS_FLOP / rs_ms / 1e9, "serial_ms": s_rs,
+                             "overlap_gain_vs_serial": s_rs / rs_ms,
+                             "frac_of_bf16_peak": RS_FLOP / rs_ms / 1e9 / pk["bf16"]}
+        extras["overlap_gain_vs_serial"] = (s_ag + s_rs) / (ag_ms + rs_ms)
+        if args.mode == "sm":
+            cparts = timed_steps(torch, [lambda: mlp.ag_call("ce")], args.steps, args.warmup, flush)
+            c_ag = statistics.mean(cparts[0])
+            extras["ag_gemm"]["ce_mode_ms"] = c_ag
+            extras["ag_gemm"]["ce_mode_tflops"] = AG_FLOP / c_ag / 1e9
+        mlp.check_status()
+        # end to end through the public API with host buffers
+        def e2e_step():
+            mlp.upload()
+            mlp.ag_call()
+            mlp.rs_call("sm")
+            mlp.download()
+        eparts = timed_steps(torch, [e2e_step], args.steps, args.warmup, flush)
+        e_ms = statistics.mean(eparts[0])
+        e2e = {"value": STEP_FLOP / e_ms / 1e9, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": mlp.h2d_bytes, "d2h_bytes_per_step": mlp.d2h_bytes,
+               "ms_per_step": e_ms}
+        mlp.check_status()
+        del mlp
+        torch.cuda.empty_cache()
+        # MoE dispatch + combine
+        moe = MoEBench(torch, tdg, synth)
+        moe.call(tdg.MOE_ROUTE)
+        torch.cuda.synchronize()
+        mparts = timed_steps(torch, [lambda: moe.call(tdg.MOE_ROUTE), lambda: moe.call(tdg.MOE_DISPATCH),
+                                     lambda: moe.call(tdg.MOE_COMBINE)], args.steps, args.warmup, flush)
+        m_route, m_disp, m_comb = (statistics.mean(x) for x in mparts)
+        bytes_dc = moe.bytes_dispatch + moe.bytes_combine
+        extras["moe_dispatch_combine"] = {
+            "workload": "8 ranks x 4096 tokens, hidden 7168 bf16, 256 experts, top-8 Zipf(1.2)",
+            "route_ms": m_route, "dispatch_ms": m_disp, "combine_ms": m_comb,
+            "dispatch_gbs": moe.bytes_dispatch / m_disp / 1e6, "combine_gbs": moe.bytes_combine / m_comb / 1e6,
+            "gbs": bytes_dc / (m_disp + m_comb) / 1e6,
+            "frac_of_hbm": bytes_dc / (m_disp + m_comb) / 1e6 / pk["hbm"]}
+        st = moe.symm.status()
+        if st["code"] != 0:
+            raise RuntimeError(f"device fault in MoE: {st}")
+        del moe
+        torch.cuda.empty_cache()
+        if rank == 0 and not args.no_cpu:
+            r, s, desc = cpu_oracle_rate()
+            cpu = {"value": r, "unit": "TFLOP/s", "cores": omp_threads(), "kind": "oracle", "sample": desc,
+                   "seconds": s}
+
+    # roofline of the dominant kernel (the GEMM-RS persistent GEMM, one launch per call)
+    dom_ms = rs_ms if rs_ms is not None else ag_ms
+    dom_flop = RS_FLOP if rs_ms is not None else AG_FLOP
+    achieved = dom_flop / dom_ms / 1e9
+    roofline = {"kernel": "rs_gemm_kernel" if rs_ms is not None else "ag_gemm_kernel",
+                "bound": "tensor", "achieved": achieved, "peak": pk["bf16"], "unit": "TFLOP/s",
+                "frac": achieved / pk["bf16"], "traffic": None,
+                "peak_kind": f"bf16 dense burst, {pk['src']}",
+                "frac_of_sustained": achieved / pk["bf16_sus"]}
+    line = {"metric": "AG-GEMM+GEMM-RS TFLOP/s (qwen32b_mlp_tp8)", "value": value, "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "l2": "flushed before every step (256 MB write)",
+                       "mode": args.mode, "producers": args.producers or 16, "sm_count": sms,
+                       "parallelism": f"replicas x{world}, 8 logical ranks each"},
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+            "clocks": clocks, "parts": extras}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -36,7 +36,8 @@ struct AgParams {
     CUtensorMap tmC;   // C: {N, M} box {64, 32}
     DevStatus *status;
     uint32_t epoch;
-    uint64_t timeout_ns;
+    uint64_t timeout_ns;      // bound of a cross-CTA signal wait
+    uint64_t pipe_timeout_ns; // bound of an intra-CTA pipeline wait (longer)
     int k_blocks;
     int64_t M, K, N, Ms;
     int m_tiles, n_tiles;
@@ -327,6 +328,7 @@ extern "C" int tdg_ag_gemm(tdg_symm *h, const tdg_ag_gemm_args *a, void *stream,
     p.status = h->status;
     p.epoch = epoch;
     p.timeout_ns = timeout_or_default(a->timeout_ns);
+    p.pipe_timeout_ns = pipe_timeout(p.timeout_ns);
     p.k_blocks = (int)((K + gm::BK - 1) / gm::BK);
     p.M = M;
     p.K = K;

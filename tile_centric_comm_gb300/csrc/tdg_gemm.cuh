@@ -73,7 +73,8 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p)
 }
 
 // Policy P provides:
-//   struct Params { ... DevStatus *status; uint32_t epoch; uint64_t timeout_ns; int k_blocks; };
+//   struct Params { ... DevStatus *status; uint32_t epoch; uint64_t timeout_ns, pipe_timeout_ns;
+//                   int k_blocks; };
 //   static constexpr int B_MN;                                   // 1: B is K x N
 //   __device__ static int64_t num_items(const Params&);
 //   __device__ static void tile(const Params&, int64_t item, TileInfo&);
@@ -116,7 +117,7 @@ __device__ void gemm_consumer(const typename P::Params &p, uint8_t *smem, int ct
     tc_fence_after();
     const uint32_t tmem_base = ps->tmem_base;
     const int64_t items = P::num_items(p);
-    const uint64_t tmo = p.timeout_ns;
+    const uint64_t tmo = p.pipe_timeout_ns;
 
     if (warp == 0) {
         if (lane == 0) {

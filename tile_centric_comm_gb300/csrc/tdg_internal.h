@@ -81,4 +81,9 @@ inline int cuda_err(cudaError_t e, const char *what)
 
 inline uint64_t timeout_or_default(uint64_t t) { return t ? t : 2000000000ull; }
 
+// Intra-CTA pipeline waits sit downstream of at most one signal wait that runs
+// out (a CTA stops waiting on signals after its first timeout), so their
+// bound is twice the signal bound plus a second.
+inline uint64_t pipe_timeout(uint64_t signal_timeout) { return 2 * signal_timeout + 1000000000ull; }
+
 } // namespace tdg_host

@@ -28,7 +28,8 @@ struct RsParams {
     CUtensorMap tmS; // staging {256, rows per owner, W}, box {64, 32, 1}
     DevStatus *status;
     uint32_t epoch;
-    uint64_t timeout_ns;
+    uint64_t timeout_ns;      // bound of a cross-CTA signal wait
+    uint64_t pipe_timeout_ns; // bound of an intra-CTA pipeline wait (longer)
     int k_blocks;
     int W;
     int64_t M, K, N, Mo;
@@ -285,6 +286,7 @@ extern "C" int tdg_gemm_rs(tdg_symm *h, const tdg_gemm_rs_args *a, void *stream)
     p.status = h->status;
     p.epoch = next_epoch(h);
     p.timeout_ns = timeout_or_default(a->timeout_ns);
+    p.pipe_timeout_ns = pipe_timeout(p.timeout_ns);
     p.k_blocks = (int)((K + gm::BK - 1) / gm::BK);
     p.W = W;
     p.M = M;
