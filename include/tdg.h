@@ -266,6 +266,33 @@ TDG_API size_t tdg_moe_workspace_bytes(int world, int64_t T, int E);
 
 TDG_API int tdg_moe_dispatch_combine(tdg_symm *h, const tdg_moe_args *args, void *stream);
 
+/*
+ * Allocation-free variant of tdg_moe_dispatch_combine.  The pages have no
+ * counterpart: this entry point exists for callers that cannot allocate
+ * device memory at the moment they call -- for example code running inside
+ * a memory-budgeted runtime or a pool that forbids cudaMalloc after start-up,
+ * or a caller with no allocator of its own -- and so cannot hand over the
+ * routing workspace.
+ *
+ * It behaves exactly like tdg_moe_dispatch_combine, except that args->workspace
+ * and args->workspace_bytes are ignored: the routing scratch (two int32 tables
+ * of W * ceil(T/64) * E entries) lives in a fixed device array inside the
+ * library, TDG_MOE_STATIC_WORKSPACE_BYTES (2 MiB) in size, which every GPU that
+ * loads the library keeps until the process exits.  Inputs and outputs are
+ * still the caller's.  Nothing is allocated or freed by this call.
+ *   - Returns TDG_ERR_NOMEM, launching nothing, when the routing phase is
+ *     requested and tdg_moe_workspace_bytes(world, T, E) exceeds 2 MiB
+ *     (that is, when W * ceil(T/64) * E > 262144).
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - All calls on one device share the array and it keeps the last call's
+ *     contents; nothing in it needs to start at zero (every entry a call reads
+ *     is written earlier in the same call).  Calls that overlap on the GPU
+ *     (for example on two streams at once) race on it: serialise them.
+ */
+#define TDG_MOE_STATIC_WORKSPACE_BYTES (2u * 1024u * 1024u)
+TDG_API int tdg_moe_dispatch_combine_noalloc(tdg_symm *h, const tdg_moe_args *args, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -454,3 +454,56 @@ extern "C" int tdg_moe_dispatch_combine(tdg_symm *h, const tdg_moe_args *a, void
     }
     return TDG_OK;
 }
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant: the routing scratch lives in a fixed device array
+// of this file instead of a caller-provided workspace, for callers that cannot
+// allocate device memory when they call.  Host code cannot pass the array's
+// name to a kernel (on the host it is only a stand-in symbol); its device
+// address is looked up once per device with cudaGetSymbolAddress.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+namespace {
+
+static __device__ __align__(256) int32_t g_moe_static_ws[TDG_MOE_STATIC_WORKSPACE_BYTES / sizeof(int32_t)];
+
+std::mutex g_static_ws_mu;
+void *g_static_ws_ptr[64] = {};
+
+} // namespace
+
+extern "C" int tdg_moe_dispatch_combine_noalloc(tdg_symm *h, const tdg_moe_args *a, void *stream)
+{
+    if (!h || !a)
+        return TDG_ERR_INVALID;
+    if ((a->phases & TDG_MOE_ROUTE) &&
+        tdg_moe_workspace_bytes(a->world, a->T, a->E) > (size_t)TDG_MOE_STATIC_WORKSPACE_BYTES) {
+        if (getenv("TDG_LOG"))
+            fprintf(stderr, "[tdg] moe noalloc: routing needs %zu bytes of scratch, the fixed array holds %u\n",
+                    tdg_moe_workspace_bytes(a->world, a->T, a->E), TDG_MOE_STATIC_WORKSPACE_BYTES);
+        return TDG_ERR_NOMEM;
+    }
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_err(e, "moe noalloc device");
+    if (dev < 0 || dev >= 64)
+        return TDG_ERR_UNSUPPORTED;
+    void *ws = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_static_ws_mu);
+        if (!g_static_ws_ptr[dev]) {
+            void *p = nullptr;
+            e = cudaGetSymbolAddress(&p, g_moe_static_ws);
+            if (e != cudaSuccess || !p)
+                return cuda_err(e != cudaSuccess ? e : cudaErrorInvalidSymbol, "moe noalloc symbol");
+            g_static_ws_ptr[dev] = p;
+        }
+        ws = g_static_ws_ptr[dev];
+    }
+    tdg_moe_args b = *a;
+    b.workspace = ws;
+    b.workspace_bytes = TDG_MOE_STATIC_WORKSPACE_BYTES;
+    return tdg_moe_dispatch_combine(h, &b, stream);
+}

@@ -34,8 +34,9 @@ EXPORTS = [
     "tdg_symm_bytes", "tdg_symm_alloc", "tdg_symm_free", "tdg_symm_region", "tdg_symm_at",
     "tdg_symm_flags", "tdg_symm_counters", "tdg_symm_epoch", "tdg_status", "tdg_strerror",
     "tdg_device_info", "tdg_ag_gemm", "tdg_gemm_rs_stage_bytes", "tdg_gemm_rs",
-    "tdg_moe_workspace_bytes", "tdg_moe_dispatch_combine",
+    "tdg_moe_workspace_bytes", "tdg_moe_dispatch_combine", "tdg_moe_dispatch_combine_noalloc",
 ]
+MOE_STATIC_WORKSPACE_BYTES = 2 * 1024 * 1024
 
 _i32, _i64, _u32, _u64 = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32, ctypes.c_uint64
 _sz, _vp = ctypes.c_size_t, ctypes.c_void_p
@@ -116,6 +117,8 @@ def lib():
             L.tdg_moe_workspace_bytes.argtypes = [ctypes.c_int, _i64, ctypes.c_int]
             L.tdg_moe_dispatch_combine.restype = ctypes.c_int
             L.tdg_moe_dispatch_combine.argtypes = [_vp, ctypes.POINTER(MoeArgs), _vp]
+            L.tdg_moe_dispatch_combine_noalloc.restype = ctypes.c_int
+            L.tdg_moe_dispatch_combine_noalloc.argtypes = [_vp, ctypes.POINTER(MoeArgs), _vp]
             _lib = L
     return _lib
 
@@ -254,3 +257,21 @@ def moe_dispatch_combine(symm: Symm, T: int, H: int, E: int, k: int, x_off: int,
                 workspace_bytes=workspace.numel() * workspace.element_size(), phases=phases)
     _check(lib().tdg_moe_dispatch_combine(symm.h, ctypes.byref(a), _stream(stream)),
            "tdg_moe_dispatch_combine")
+
+
+def moe_dispatch_combine_noalloc(symm: Symm, T: int, H: int, E: int, k: int, x_off: int,
+                                 topk_off: int, gate_off: int, out_off: int, recv, counts, base,
+                                 slot, y=None, row_src=None, row_tok=None, row_k=None,
+                                 phases=MOE_ALL, stream=None):
+    """Same as moe_dispatch_combine, for callers that cannot allocate device
+    memory when they call: the routing scratch is the library's fixed 2 MiB
+    device array, so no workspace is passed.  Raises TdgError (TDG_ERR_NOMEM)
+    when world * ceil(T/64) * E exceeds 262144."""
+    def p(t):
+        return t.data_ptr() if t is not None else None
+    a = MoeArgs(world=symm.world, T=T, H=H, E=E, k=k, x_off=x_off, topk_off=topk_off,
+                gate_off=gate_off, out_off=out_off, recv=p(recv), y=p(y), counts=p(counts),
+                base=p(base), slot=p(slot), row_src=p(row_src), row_tok=p(row_tok),
+                row_k=p(row_k), workspace=None, workspace_bytes=0, phases=phases)
+    _check(lib().tdg_moe_dispatch_combine_noalloc(symm.h, ctypes.byref(a), _stream(stream)),
+           "tdg_moe_dispatch_combine_noalloc")
