@@ -41,13 +41,14 @@ def assert_close(got_bits, ref64, tol=1e-2):
 class AGCase:
     """Inputs of one AllGather+GEMM call laid out in a symmetric heap."""
 
-    def __init__(self, inp, b_layout=tdg.B_KN, device="cuda"):
+    def __init__(self, inp, b_layout=tdg.B_KN, device="cuda", ll=False):
         self.inp = inp
         W, Ms, K, N = inp.W, inp.Ms, inp.K, inp.N
         self.M = W * Ms
         self.a_off = 0
         self.g_off = align(Ms * K * 2)
-        region = align(self.g_off + self.M * K * 2 + 1024)
+        self.ll_off = align(self.g_off + self.M * K * 2)     # LL words (M*K*4 bytes)
+        region = align(self.ll_off + (self.M * K * 4 if ll else 0) + 1024)
         nsig = max(1024, self.M)
         self.symm = tdg.Symm(W, region, nsig, device=device)
         for s in range(W):
@@ -61,6 +62,10 @@ class AGCase:
 
     def gathered(self, rank):
         return self.symm.view(rank, self.g_off, (self.M, self.inp.K), torch.bfloat16)
+
+    def ll_words(self, rank):
+        n = self.M * self.inp.K // 2
+        return self.symm.view(rank, self.ll_off, (n,), torch.int64).cpu().numpy().view(np.uint64)
 
     def run(self, rank=0, mode="sm", check_status=True, **kw):
         inp = self.inp

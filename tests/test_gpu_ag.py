@@ -27,13 +27,18 @@ def test_tiny_integer_bit_exact_all_modes_and_ranks():
             _gathered_ok(case, rank)
 
 
+@pytest.mark.parametrize("pair", ["1", "0"])
 @pytest.mark.parametrize("b_layout", [tdg.B_KN, tdg.B_NK])
 @pytest.mark.parametrize("W,Ms,K,N", [
     (4, 256, 320, 520),     # 8 m tiles, 3 n tiles (last one 8 columns), 5 k blocks
     (3, 96, 136, 264),      # Ms not a multiple of 128: gathered read, ragged m tail
     (2, 128, 64, 256),      # exactly one k block, full n tile
+    (2, 384, 128, 136),     # pairs: 3 tiles of 256 rows, the last half empty
 ])
-def test_float_parity_small(W, Ms, K, N, b_layout):
+def test_float_parity_small(W, Ms, K, N, b_layout, pair, monkeypatch):
+    # pair "1": CTA pairs (cta_group::2, 256-row tiles) where the shape allows;
+    # pair "0": one CTA per 128-row tile
+    monkeypatch.setenv("TDG_PAIR", pair)
     inp = synth.ag_inputs(W, Ms, K, N, "normal", seed=W * 7 + K)
     C64, C16 = oracle.ag_gemm(inp.shards, inp.B)
     case = AGCase(inp, b_layout=b_layout)
@@ -43,9 +48,11 @@ def test_float_parity_small(W, Ms, K, N, b_layout):
         _gathered_ok(case, W - 1)
 
 
-def test_integer_exact_larger_and_swizzle_invariance():
+@pytest.mark.parametrize("pair", ["1", "0"])
+def test_integer_exact_larger_and_swizzle_invariance(pair, monkeypatch):
     # integer inputs, |sums| <= 4K: exact in fp32; output identical for every
     # rank, swizzle on/off, signal granularity and producer count
+    monkeypatch.setenv("TDG_PAIR", pair)
     inp = synth.ag_inputs(4, 256, 512, 384, "int2", seed=3)
     _, C16 = oracle.ag_gemm(inp.shards, inp.B)
     case = AGCase(inp)
@@ -67,11 +74,48 @@ def test_timeout_reported_then_next_call_succeeds():
     inp = synth.ag_inputs(2, 128, 64, 256, "int2", seed=1)
     _, C16 = oracle.ag_gemm(inp.shards, inp.B)
     case = AGCase(inp)
-    # rank 0 reads its own shard in place; group 4 (rows 128..159, shard 1) is remote
+    # group 4 = rows 128..159 = the first rows of shard 1, remote for rank 0
     _, st = case.run(rank=0, mode="sm", signal_rows=32, test_skip_notify=1 << 4,
                      timeout_ns=20_000_000, check_status=False)
     assert st["code"] == tdg.TDG_ERR_TIMEOUT and st["where"] == "ag_flag" and st["index"] == 4
     got, st = case.run(rank=0, mode="sm", signal_rows=32)
+    assert st["code"] == 0 and np.array_equal(got, C16)
+
+
+def test_ll_mode_bit_exact_and_words_match_the_codec():
+    # LL path: 8-byte {payload, flag=epoch} words; the GEMM result, the gathered
+    # buffer and every LL word are bit-exact (words against the oracle's codec)
+    inp = synth.make("ag_tiny")
+    _, C16 = oracle.ag_gemm(inp.shards, inp.B)
+    case = AGCase(inp, ll=True)
+    payload = np.concatenate(inp.shards).view(np.uint32).reshape(-1)
+    for rank in range(inp.W):
+        epoch = case.symm.epoch()
+        got, _ = case.run(rank=rank, mode="ll", ll_off=case.ll_off)
+        assert np.array_equal(got, C16)
+        _gathered_ok(case, rank)
+        assert np.array_equal(case.ll_words(rank), oracle.ll_pack(payload, epoch))
+
+
+def test_ll_mode_float_parity():
+    inp = synth.ag_inputs(4, 128, 256, 264, "normal", seed=12)
+    C64, _ = oracle.ag_gemm(inp.shards, inp.B)
+    case = AGCase(inp, ll=True)
+    got, _ = case.run(rank=2, mode="ll", ll_off=case.ll_off, signal_rows=32)
+    assert_close(got, C64)
+    _gathered_ok(case, 2)
+
+
+def test_ll_missing_words_time_out_then_recover():
+    # the senders skip the words of group 1 (host-side injection): the
+    # receiver's bounded spin runs out and reports it; the next call succeeds
+    inp = synth.make("ag_tiny")
+    _, C16 = oracle.ag_gemm(inp.shards, inp.B)
+    case = AGCase(inp, ll=True)
+    _, st = case.run(rank=0, mode="ll", ll_off=case.ll_off, test_skip_notify=1 << 1,
+                     timeout_ns=20_000_000, check_status=False)
+    assert st["code"] == tdg.TDG_ERR_TIMEOUT and st["where"] == "ll" and st["index"] == 1
+    got, st = case.run(rank=0, mode="ll", ll_off=case.ll_off)
     assert st["code"] == 0 and np.array_equal(got, C16)
 
 

@@ -10,10 +10,11 @@ from gpu_util import RSCase, assert_close
 pytestmark = pytest.mark.gpu
 
 
-def test_integer_small_k_bit_exact_both_modes():
+@pytest.mark.parametrize("W,M", [(4, 512), (2, 1024)])   # (2, 1024): CTA pairs
+def test_integer_small_k_bit_exact_both_modes(W, M):
     # integer inputs with small K: every partial |.| <= 2*2*K <= 256 is exact in
     # bf16, and the fp32 sum of W of them is exact too
-    inp = synth.rs_inputs(4, 512, 64, 520, "int2", seed=5)
+    inp = synth.rs_inputs(W, M, 64, 520, "int2", seed=5)
     _, out16 = oracle.gemm_rs(inp.As, inp.Bs)
     case = RSCase(inp)
     for mode in ("sm", "serial", "sm"):
@@ -21,13 +22,16 @@ def test_integer_small_k_bit_exact_both_modes():
         assert np.array_equal(got, out16), mode
 
 
+@pytest.mark.parametrize("pair", ["1", "0"])
 @pytest.mark.parametrize("b_layout", [tdg.B_KN, tdg.B_NK])
 @pytest.mark.parametrize("W,M,K,N", [
     (2, 256, 200, 264),    # ragged k block and n tile
-    (4, 1024, 320, 512),   # 2 m tiles per owner
+    (4, 1024, 320, 512),   # 2 m tiles per owner (one pair tile)
     (8, 1024, 128, 256),
+    (2, 1024, 136, 136),   # pairs with a narrow n tile
 ])
-def test_float_parity_small(W, M, K, N, b_layout):
+def test_float_parity_small(W, M, K, N, b_layout, pair, monkeypatch):
+    monkeypatch.setenv("TDG_PAIR", pair)
     inp = synth.rs_inputs(W, M, K, N, "normal", seed=M + K)
     out64, _ = oracle.gemm_rs(inp.As, inp.Bs)
     case = RSCase(inp, b_layout=b_layout)

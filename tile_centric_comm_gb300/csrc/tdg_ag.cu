@@ -60,6 +60,11 @@ struct AgParams {
     int local_last;
     uint32_t *flags_w;
     uint64_t skip_mask;
+    int pair; // 1: CTA pairs (cta_group::2) with 256-row tiles
+    // LL mode: producer CTAs [0, n_send) send, [n_send, n_prod) receive
+    int ll;
+    int n_send;
+    uint64_t *ll_buf; // M * K / 2 words in region(rank)
 };
 
 template <int BMN> struct AgPolicy {
@@ -68,18 +73,23 @@ template <int BMN> struct AgPolicy {
 
     __device__ static int64_t num_items(const Params &p) { return (int64_t)p.m_tiles * p.n_tiles; }
 
-    __device__ static void tile(const Params &p, int64_t item, TileInfo &t)
+    // tiles are tile_m = 128 (one CTA) or 256 (CTA pair) rows; `half` picks this
+    // CTA's 128-row slice
+    __device__ static void tile(const Params &p, int64_t item, TileInfo &t, int half)
     {
+        const int tm = p.pair ? 2 * gm::BM : gm::BM;
         const int pm0 = (int)(item / p.n_tiles);
         t.pn = (int)(item % p.n_tiles);
         // the pages' swizzle: pid_m = (pid_m + rank * tiles_per_pe) % total
         const int pm = (pm0 + p.swz) % p.m_tiles;
-        t.m0 = pm * gm::BM;
+        t.m0 = pm * tm + half * gm::BM;
         t.n0 = t.pn * gm::BN;
         t.n_valid = (int)min((int64_t)gm::BN, p.N - t.n0);
+        const int q = p.pair ? 32 : 16;
+        t.n_mma = (t.n_valid + q - 1) / q * q;
         if (p.local_inplace && pm >= p.local_lo && pm < p.local_hi) {
             t.a_sel = 1;
-            t.a_row = t.m0 - p.local_lo * gm::BM;
+            t.a_row = t.m0 - p.local_lo * tm;
         } else {
             t.a_sel = 0;
             t.a_row = t.m0;
@@ -90,13 +100,16 @@ template <int BMN> struct AgPolicy {
 
     __device__ static void before_a(const Params &p, const TileInfo &t, bool &gave_up)
     {
-        if (t.a_sel == 1 || !p.wait_flags)
+        if (t.a_sel == 1 || !p.wait_flags || t.m0 >= p.M)
             return;
         const int64_t r0 = t.m0;
         const int64_t r1 = min(p.M, (int64_t)t.m0 + gm::BM) - 1;
-        // wait(ptr, n): every signal group the tile's rows fall into
+        // wait(ptr, n): every signal group this CTA's rows fall into.  In LL
+        // mode a receiver that gives up still releases its group, so the GEMM
+        // waits twice as long and the receiver's report comes first.
+        const uint64_t tmo = p.ll ? 2 * p.timeout_ns : p.timeout_ns;
         for (int64_t g = r0 / p.sig_rows; g <= r1 / p.sig_rows && !gave_up; ++g) {
-            if (!wait_flag(p.flags + g, p.epoch, p.timeout_ns)) {
+            if (!wait_flag(p.flags + g, p.epoch, tmo)) {
                 report_fault(p.status, TDG_ERR_TIMEOUT, TDG_WHERE_AG_FLAG, (uint32_t)g, p.epoch);
                 gave_up = true;
             }
@@ -105,26 +118,39 @@ template <int BMN> struct AgPolicy {
         fence_proxy_async_global();
     }
 
-    __device__ static void load_a(const Params &p, const TileInfo &t, void *dst, uint64_t *bar, int kb)
+    // The TMA form is chosen at compile time: a kernel holds either only
+    // cta_group::1 or only cta_group::2 instructions, never both.
+    template <int PAIR>
+    __device__ static void load(void *dst, const CUtensorMap *m, uint32_t bar, int x, int y)
     {
-        tma_load_2d(dst, t.a_sel ? &p.tmA_l : &p.tmA_g, bar, kb * gm::BK, t.a_row);
+        if constexpr (PAIR)
+            tma_load_2d_pair(dst, m, bar, x, y);
+        else
+            tma_load_2d_addr(dst, m, bar, x, y);
     }
 
-    __device__ static void load_b(const Params &p, const TileInfo &t, void *dst, uint64_t *bar, int kb)
+    template <int PAIR>
+    __device__ static void load_a(const Params &p, const TileInfo &t, void *dst, uint32_t bar, int kb)
+    {
+        load<PAIR>(dst, t.a_sel ? &p.tmA_l : &p.tmA_g, bar, kb * gm::BK, t.a_row);
+    }
+
+    template <int PAIR>
+    __device__ static void load_b(const Params &p, const TileInfo &, void *dst, uint32_t bar, int kb,
+                                  int col0, int cols)
     {
         if (BMN) {
-            const int nch = (t.n_valid + 63) >> 6;
+            const int nch = (cols + 63) >> 6;
             for (int j = 0; j < nch; ++j)
-                tma_load_2d(static_cast<uint8_t *>(dst) + j * 8192, &p.tmB, bar, t.n0 + 64 * j,
-                            kb * gm::BK);
+                load<PAIR>(static_cast<uint8_t *>(dst) + j * 8192, &p.tmB, bar, col0 + 64 * j, kb * gm::BK);
         } else {
-            tma_load_2d(dst, &p.tmB, bar, kb * gm::BK, t.n0);
+            load<PAIR>(dst, &p.tmB, bar, kb * gm::BK, col0);
         }
     }
 
-    __device__ static uint32_t b_bytes(const TileInfo &t)
+    __device__ static uint32_t b_bytes(const Params &p, const TileInfo &, int cols)
     {
-        return BMN ? (uint32_t)(((t.n_valid + 63) >> 6) * 8192) : (uint32_t)gm::B_BYTES;
+        return BMN ? (uint32_t)(((cols + 63) >> 6) * 8192) : (uint32_t)((p.pair ? gm::BN / 2 : gm::BN) * gm::BK * 2);
     }
 
     __device__ static void store_chunk(const Params &p, const TileInfo &t, const void *buf, int ch, int q)
@@ -221,16 +247,85 @@ __device__ void ag_producer(const AgParams &p, uint8_t *smem)
     }
 }
 
-template <int BMN>
+// LL sender (paper summary, 方法: the low-latency protocol stores data and
+// flag together in 8-byte blocks, so no separate signal follows a transfer).
+// Each thread packs two bf16 of a shard (4 bytes) with the call's epoch into
+// one word and writes it into rank `rank`'s LL buffer, at the word's position
+// in the gathered matrix.  Sources in the same order as the bulk producers.
+__device__ void ll_sender(const AgParams &p, int cta, int ncta)
+{
+    const int64_t wps = p.Ms * p.K / 2; // words per shard
+    const int64_t total = wps * p.W;
+    const uint64_t hi = (uint64_t)p.epoch << 32;
+    for (int64_t w = (int64_t)cta * blockDim.x + threadIdx.x; w < total; w += (int64_t)ncta * blockDim.x) {
+        const int seq = (int)(w / wps);
+        const int64_t off = w % wps;
+        const int shard = (p.rank + 1 + seq) % p.W;
+        const int64_t gw = (int64_t)shard * wps + off;
+        const int64_t g = (gw * 2 / p.K) / p.sig_rows;
+        if ((p.skip_mask >> (g & 63)) & 1ull)
+            continue;
+        const uint32_t payload = *reinterpret_cast<const uint32_t *>(
+            p.regions + (uint64_t)shard * p.region_bytes + p.a_off + (uint64_t)off * 4);
+        st_relaxed_gpu_u64(p.ll_buf + gw, hi | payload);
+    }
+}
+
+// LL receiver: spin (bounded) on every word of a signal group until its flag
+// is this call's epoch, unpack the payload into the gathered buffer, then hand
+// the group to the GEMM with one release of the group's flag.
+__device__ void ll_receiver(const AgParams &p, int cta, int ncta)
+{
+    const int64_t wpg = p.sig_rows * p.K / 2; // words per group
+    const int64_t n_groups = p.M / p.sig_rows;
+    uint32_t *g32 = reinterpret_cast<uint32_t *>(p.gathered);
+    bool gave_up = false;
+    for (int64_t g = cta; g < n_groups; g += ncta) {
+        for (int64_t i = threadIdx.x; i < wpg; i += blockDim.x) {
+            const int64_t w = g * wpg + i;
+            uint64_t v = ld_relaxed_gpu_u64(p.ll_buf + w);
+            if ((uint32_t)(v >> 32) != p.epoch && !gave_up) {
+                const uint64_t t0 = globaltimer();
+                while ((uint32_t)(v >> 32) != p.epoch) {
+                    __nanosleep(64);
+                    v = ld_relaxed_gpu_u64(p.ll_buf + w);
+                    if (globaltimer() - t0 > p.timeout_ns) {
+                        report_fault(p.status, TDG_ERR_TIMEOUT, TDG_WHERE_LL, (uint32_t)g, p.epoch);
+                        gave_up = true;
+                        break;
+                    }
+                }
+            }
+            g32[w] = (uint32_t)v;
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            __threadfence();
+            st_release_gpu(p.flags_w + g, p.epoch);
+        }
+    }
+}
+
+template <int BMN, int PAIR>
 __global__ void __launch_bounds__(gm::NUM_THREADS, 1) ag_gemm_kernel(const __grid_constant__ AgParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
     if ((int)blockIdx.x < p.n_prod) {
-        ag_producer(p, smem);
+        // producer CTAs never take part in a pair
+        if (!p.ll)
+            ag_producer(p, smem);
+        else if ((int)blockIdx.x < p.n_send)
+            ll_sender(p, blockIdx.x, p.n_send);
+        else
+            ll_receiver(p, blockIdx.x - p.n_send, p.n_prod - p.n_send);
         return;
     }
-    gemm_consumer<AgPolicy<BMN>>(p, smem, (int)blockIdx.x - p.n_prod, (int)gridDim.x - p.n_prod);
+    const int c = (int)blockIdx.x - p.n_prod, nc = (int)gridDim.x - p.n_prod;
+    if (PAIR)
+        gemm_consumer<AgPolicy<BMN>, 1>(p, smem, c >> 1, nc >> 1);
+    else
+        gemm_consumer<AgPolicy<BMN>, 0>(p, smem, c, nc);
 }
 
 } // namespace tdg
@@ -240,28 +335,62 @@ using namespace tdg_host;
 
 namespace {
 
-const void *ag_kernel_fn(int b_layout)
+const void *ag_kernel_fn(int b_layout, int pair)
 {
-    return b_layout == TDG_B_KN ? reinterpret_cast<const void *>(&ag_gemm_kernel<1>)
-                                : reinterpret_cast<const void *>(&ag_gemm_kernel<0>);
+    if (b_layout == TDG_B_KN)
+        return pair ? reinterpret_cast<const void *>(&ag_gemm_kernel<1, 1>)
+                    : reinterpret_cast<const void *>(&ag_gemm_kernel<1, 0>);
+    return pair ? reinterpret_cast<const void *>(&ag_gemm_kernel<0, 1>)
+                : reinterpret_cast<const void *>(&ag_gemm_kernel<0, 0>);
 }
 
-int launch_ag(const AgParams &p, int b_layout, int grid, bool coop, cudaStream_t s)
+int prepare(const void *fn, int dev)
 {
-    const void *fn = ag_kernel_fn(b_layout);
-    static bool smem_set[2][64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    bool &done = smem_set[b_layout & 1][dev & 63];
-    if (!done) {
-        cudaError_t e = set_smem(fn, gm::SMEM_BYTES);
-        if (e != cudaSuccess)
-            return cuda_err(e, "ag set smem");
-        done = true;
+    static const void *done[8][64] = {};
+    for (int i = 0; i < 8; ++i) {
+        if (done[i][dev & 63] == fn)
+            return TDG_OK;
+        if (!done[i][dev & 63]) {
+            cudaError_t e = set_smem(fn, gm::SMEM_BYTES);
+            if (e != cudaSuccess)
+                return cuda_err(e, "ag set smem");
+            done[i][dev & 63] = fn;
+            return TDG_OK;
+        }
     }
+    return cuda_err(set_smem(fn, gm::SMEM_BYTES), "ag set smem");
+}
+
+// grid for a launch with n_prod producer CTAs plus consumers on every other SM
+int ag_grid(const AgParams &p, int b_layout, int sms, int dev)
+{
+    if (!p.pair)
+        return sms;
+    if (prepare(ag_kernel_fn(b_layout, 1), dev) != TDG_OK)
+        return 0;
+    const int mp = max_pairs(ag_kernel_fn(b_layout, 1), gm::NUM_THREADS, gm::SMEM_BYTES);
+    const int pairs = mp > 0 ? (mp < sms / 2 ? mp : sms / 2) : 0;
+    return 2 * pairs;
+}
+
+int launch_ag(const AgParams &p, int b_layout, int grid, bool coop, cudaStream_t s, int dev)
+{
+    const void *fn = ag_kernel_fn(b_layout, p.pair);
+    int rc = prepare(fn, dev);
+    if (rc != TDG_OK)
+        return rc;
+    if (grid < 1 || grid < p.n_prod) // a copy-only launch has no consumers
+        return TDG_ERR_UNSUPPORTED;
     void *args[] = {const_cast<AgParams *>(&p)};
-    return cuda_err(launch(fn, dim3(grid), dim3(gm::NUM_THREADS), gm::SMEM_BYTES, s, args, coop),
-                    "ag launch");
+    cudaError_t e = launch(fn, dim3(grid), dim3(gm::NUM_THREADS), gm::SMEM_BYTES, s, args, coop,
+                           p.pair ? 2 : 1);
+    if (e != cudaSuccess && coop && p.pair) {
+        // co-residency then rests on the grid being no larger than the number
+        // of clusters that fit at once (the bounded waits cover the rest)
+        (void)cudaGetLastError();
+        e = launch(fn, dim3(grid), dim3(gm::NUM_THREADS), gm::SMEM_BYTES, s, args, false, 2);
+    }
+    return cuda_err(e, "ag launch");
 }
 
 } // namespace
@@ -294,11 +423,21 @@ extern "C" int tdg_ag_gemm(tdg_symm *h, const tdg_ag_gemm_args *a, void *stream,
         return TDG_ERR_INVALID; // the gathered buffer overlaps the shard
     if (K == 0)
         return cuda_err(cudaMemsetAsync(a->C, 0, (size_t)M * N * 2, s), "ag K==0");
-    if (a->mode == TDG_MODE_LL)
-        return TDG_ERR_UNSUPPORTED;
+    const bool ll = a->mode == TDG_MODE_LL;
+    const uint64_t ll_bytes = (uint64_t)M * K * 4;
+    if (ll) {
+        if (!aligned16(a->ll_off) || a->ll_off + ll_bytes > h->region_bytes)
+            return a->ll_off + ll_bytes > h->region_bytes ? TDG_ERR_NOMEM : TDG_ERR_INVALID;
+        if ((a->ll_off < a->a_off + shard_bytes && a->a_off < a->ll_off + ll_bytes) ||
+            (a->ll_off < a->g_off + gath_bytes && a->g_off < a->ll_off + ll_bytes))
+            return TDG_ERR_INVALID; // the LL buffer overlaps the shard or the gathered buffer
+    }
 
     const int BM = gm::BM;
-    const bool inplace = (Ms % BM) == 0;
+    // CTA pairs (256-row tiles) once there is more than one 128-row tile
+    const int pair = (pairs_enabled() && M > BM && !ll) ? 1 : 0;
+    const int TM = pair ? 2 * BM : BM;
+    const bool inplace = (Ms % TM) == 0;
     int64_t sig_rows = a->signal_rows;
     if (sig_rows <= 0)
         sig_rows = (a->mode == TDG_MODE_CE) ? Ms : (inplace ? (Ms % 32 == 0 ? 32 : Ms) : Ms);
@@ -319,7 +458,7 @@ extern "C" int tdg_ag_gemm(tdg_symm *h, const tdg_ag_gemm_args *a, void *stream,
     if (a->b_layout == TDG_B_KN)
         ok = ok && map_bf16_2d(&p.tmB, a->B, N, K, N * 2, 64, 64);
     else
-        ok = ok && map_bf16_2d(&p.tmB, a->B, K, N, K * 2, 64, 256);
+        ok = ok && map_bf16_2d(&p.tmB, a->B, K, N, K * 2, 64, pair ? 128 : 256);
     ok = ok && map_bf16_2d(&p.tmC, a->C, N, M, N * 2, 64, 32);
     if (!ok)
         return TDG_ERR_CUDA;
@@ -334,12 +473,13 @@ extern "C" int tdg_ag_gemm(tdg_symm *h, const tdg_ag_gemm_args *a, void *stream,
     p.K = K;
     p.N = N;
     p.Ms = Ms;
-    p.m_tiles = (int)((M + BM - 1) / BM);
+    p.pair = pair;
+    p.m_tiles = (int)((M + TM - 1) / TM);
     p.n_tiles = (int)((N + gm::BN - 1) / gm::BN);
-    p.swz = a->swizzle ? (int)(((int64_t)rank * Ms / BM) % p.m_tiles) : 0;
+    p.swz = a->swizzle ? (int)(((int64_t)rank * Ms / TM) % p.m_tiles) : 0;
     p.local_inplace = inplace ? 1 : 0;
-    p.local_lo = inplace ? (int)(rank * Ms / BM) : 0;
-    p.local_hi = inplace ? (int)((rank + 1) * Ms / BM) : 0;
+    p.local_lo = inplace ? (int)(rank * Ms / TM) : 0;
+    p.local_hi = inplace ? (int)((rank + 1) * Ms / TM) : 0;
     p.flags = flags;
     p.sig_rows = sig_rows;
     p.regions = h->base;
@@ -353,9 +493,30 @@ extern "C" int tdg_ag_gemm(tdg_symm *h, const tdg_ag_gemm_args *a, void *stream,
     p.skip_mask = a->test_skip_notify;
 
     const int sms = h->sm_count;
+    const int dev = h->device;
+    const int ggrid = ag_grid(p, a->b_layout, sms, dev); // GEMM-only grid
+    if (ggrid <= 0)
+        return TDG_ERR_UNSUPPORTED;
+    if (ll) {
+        // sender and receiver CTAs beside the GEMM, all in one cooperative launch
+        const int n_send = a->producers > 0 ? a->producers : 8;
+        const int64_t groups = M / sig_rows;
+        const int n_recv = (int)(groups < 8 ? groups : 8);
+        if (n_send + n_recv >= ggrid)
+            return TDG_ERR_INVALID;
+        p.ll = 1;
+        p.ll_buf = reinterpret_cast<uint64_t *>(region_r + a->ll_off);
+        p.n_send = n_send;
+        p.n_prod = n_send + n_recv;
+        p.wait_flags = 1;
+        p.n_units = 0;
+        return launch_ag(p, a->b_layout, ggrid, true, s, dev);
+    }
     if (a->mode == TDG_MODE_SM) {
         int nprod = a->producers > 0 ? a->producers : 16;
-        if (nprod >= sms)
+        if (pair)
+            nprod = (nprod + 1) & ~1; // producer CTAs fill whole clusters
+        if (nprod >= ggrid)
             return TDG_ERR_INVALID;
         p.n_prod = nprod;
         p.wait_flags = 1;
@@ -363,7 +524,7 @@ extern "C" int tdg_ag_gemm(tdg_symm *h, const tdg_ag_gemm_args *a, void *stream,
         p.unit_rows = sig_rows;
         p.units_per_shard = Ms / sig_rows;
         p.n_units = (int64_t)W * p.units_per_shard;
-        return launch_ag(p, a->b_layout, sms, true, s);
+        return launch_ag(p, a->b_layout, ggrid, true, s, dev);
     }
     if (a->mode == TDG_MODE_SERIAL) {
         // copy phase: every SM copies, fine-grained units, no signals
@@ -377,7 +538,8 @@ extern "C" int tdg_ag_gemm(tdg_symm *h, const tdg_ag_gemm_args *a, void *stream,
         c.units_per_shard = Ms / c.unit_rows;
         c.n_units = (int64_t)W * c.units_per_shard;
         c.local_last = 0;
-        int rc = launch_ag(c, a->b_layout, sms, false, s);
+        c.pair = 0;
+        int rc = launch_ag(c, a->b_layout, sms, false, s, dev);
         if (rc != TDG_OK)
             return rc;
         // GEMM phase: stream-ordered after the copy, no waits
@@ -385,7 +547,7 @@ extern "C" int tdg_ag_gemm(tdg_symm *h, const tdg_ag_gemm_args *a, void *stream,
         g.n_prod = 0;
         g.wait_flags = 0;
         g.n_units = 0;
-        return launch_ag(g, a->b_layout, sms, false, s);
+        return launch_ag(g, a->b_layout, ggrid, false, s, dev);
     }
     // CE mode
     cudaStream_t side = static_cast<cudaStream_t>(side_stream);
@@ -427,7 +589,7 @@ extern "C" int tdg_ag_gemm(tdg_symm *h, const tdg_ag_gemm_args *a, void *stream,
         g.n_prod = 0;
         g.wait_flags = 1;
         g.n_units = 0;
-        rc = launch_ag(g, a->b_layout, sms, false, s);
+        rc = launch_ag(g, a->b_layout, ggrid, false, s, dev);
     }
     // the call completes on the main stream only when the side stream has too
     e = cudaEventRecord(ev1, side);

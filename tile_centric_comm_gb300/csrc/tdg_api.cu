@@ -98,19 +98,47 @@ cudaError_t set_smem(const void *fn, int bytes)
 }
 
 cudaError_t launch(const void *fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s,
-                   void **args, bool cooperative)
+                   void **args, bool cooperative, int cluster)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    attr[n].id = cudaLaunchAttributeCooperative;
+    attr[n].val.cooperative = cooperative ? 1 : 0;
+    ++n;
+    if (cluster > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = (unsigned)cluster;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+int max_pairs(const void *fn, int block, int smem)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = cooperative ? 1 : 0;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelExC(&cfg, fn, args);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess)
+        return 0;
+    return n;
 }
 
 int occupancy_ok(const void *fn, int block, int smem, int grid, int sm_count)

@@ -4,18 +4,29 @@
 // waits for each tile and computes on it at once; the GEMM producer signals
 // each finished output tile).
 //
-// One CTA per SM, 6 warps:
+// Each CTA runs 6 warps:
 //   warp 0      TMA loader: per tile it first runs the policy's signal wait
 //               (the wait / consume_token pair of the pages), then streams
-//               BK-wide slices of A and B into a STAGES-deep shared-memory ring.
-//   warp 1      MMA issuer: one thread issues tcgen05.mma (M=128, N<=256,
-//               K=16) into one of two TMEM accumulators (2 x 256 fp32 columns)
-//               and frees ring slots with tcgen05.commit.
+//               BK-wide slices of A and B into a shared-memory ring.
+//   warp 1      MMA issuer: one thread issues tcgen05.mma (K=16 per
+//               instruction) into one of two TMEM accumulators (2 x 256 fp32
+//               columns) and frees ring slots with tcgen05.commit.
 //   warps 2..5  epilogue: tcgen05.ld -> bf16 (round to nearest even) ->
 //               128B-swizzled staging -> TMA store; then the policy's
 //               after-tile hook (the GEMM+RS signal and reduction).
-// Tiles are BM x BN = 128 x 256; a tile at the right edge of N issues a
-// narrower MMA (N rounded up to 16) and stores only its valid columns.
+//
+// Two shapes of the same pipeline (template parameter PAIR):
+//   PAIR = 0  one CTA per SM owns a 128 x 256 tile; 4 stages of 48 KB.
+//   PAIR = 1  a cluster of two CTAs (an SM pair) owns a 256 x 256 tile:
+//             each CTA loads its 128 rows of A and half of the tile's columns
+//             of B; the leader CTA issues tcgen05.mma.cta_group::2, which
+//             reads both CTAs' shared memory and writes each CTA's TMEM
+//             (its own 128 rows).  Both CTAs' loads complete on the leader's
+//             barrier; the leader's commits arrive on both CTAs' barriers.
+//             Stages are 32 KB, so 6 are in flight, and each SM moves a third
+//             less operand data per FLOP than with PAIR = 0.
+// A tile at the right edge of N issues a narrower MMA and stores only its
+// valid columns; rows past M come from TMA zero fill and are not stored.
 // Operands: A is K-major (rows of K); B is either MN-major (K x N row-major,
 // the transpose bit of the instruction descriptor) or K-major (N x K).
 #pragma once
@@ -25,47 +36,55 @@
 
 namespace tdg {
 namespace gm {
-constexpr int BM = 128;
-constexpr int BN = 256;
+constexpr int BM = 128; // rows per CTA
+constexpr int BN = 256; // columns per tile
 constexpr int BK = 64;
-constexpr int STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2;            // 16 KB
-constexpr int B_BYTES = BN * BK * 2;            // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 48 KB
+constexpr int A_BYTES = BM * BK * 2; // 16 KB
 constexpr int NUM_THREADS = 192;
 constexpr int EPI_WARP0 = 2;
 constexpr int EPI_WARPS = 4;
-constexpr int EPI_BUF = 32 * 128;               // 32 rows x 64 bf16 (128 B)
-constexpr int OFF_EPI = STAGES * STAGE_BYTES;   // 196608
+constexpr int EPI_BUF = 32 * 128;     // 32 rows x 64 bf16 (128 B)
+constexpr int RING_BYTES = 196608;    // 4 x 48 KB or 6 x 32 KB
+constexpr int OFF_EPI = RING_BYTES;
 constexpr int OFF_BAR = OFF_EPI + EPI_WARPS * 2 * EPI_BUF; // 229376
 constexpr int BAR_BYTES = 256;
 constexpr int SMEM_BYTES = OFF_BAR + BAR_BYTES + 1024;     // + alignment slack
 constexpr uint32_t TMEM_COLS = 512;
+
+template <int PAIR> struct Shape {
+    static constexpr int B_BYTES = (PAIR ? BN / 2 : BN) * BK * 2;  // B columns held per CTA
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGES = RING_BYTES / STAGE_BYTES;        // 4 or 6
+    static constexpr int TILE_M = PAIR ? 2 * BM : BM;              // rows per tile
+};
+static_assert(Shape<0>::STAGES == 4 && Shape<1>::STAGES == 6, "ring layout");
 } // namespace gm
 
 struct TileInfo {
-    int m0;      // first output row of the tile
-    int n0;      // first output column
+    int m0;      // first output row handled by THIS CTA (tile row + 128 * half)
+    int n0;      // first output column of the tile
     int n_valid; // columns of this tile inside N (1..BN)
-    int a_row;   // row coordinate of the tile in the selected A tensor map
+    int n_mma;   // MMA N: n_valid rounded up (16 for one CTA, 32 for a pair)
+    int a_row;   // row coordinate of this CTA's A slice in the selected map
     int a_sel;   // policy-defined: which A map / which rank
     int owner;   // policy-defined (RS: owner rank)
-    int m_loc;   // policy-defined (RS: m tile inside the owner)
+    int m_loc;   // policy-defined (RS: 128-row tile inside the owner)
     int pn;      // n tile index
 };
 
 struct PipeSmem {
-    uint64_t full[gm::STAGES];
-    uint64_t empty[gm::STAGES];
+    uint64_t full[6];
+    uint64_t empty[6];
     uint64_t tfull[2];
     uint64_t tempty[2];
     uint64_t drain;     // used only after an abort, to drain issued MMAs
     uint32_t tmem_base;
     volatile int abort;
-    int is_last;        // RS: broadcast of the "last arriver" decision
-    uint32_t issued;    // ring fills issued by the loader
-    uint32_t consumed;  // ring fills consumed by the MMA issuer
+    int is_last;
+    uint32_t issued;    // ring fills issued by this CTA's loader
+    uint32_t consumed;  // ring fills consumed by the leader's MMA issuer
 };
+static_assert(sizeof(PipeSmem) <= gm::BAR_BYTES, "barrier block");
 
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p)
 {
@@ -77,29 +96,37 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p)
 //                   int k_blocks; };
 //   static constexpr int B_MN;                                   // 1: B is K x N
 //   __device__ static int64_t num_items(const Params&);
-//   __device__ static void tile(const Params&, int64_t item, TileInfo&);
-//   __device__ static void before_a(const Params&, const TileInfo&, bool &gave_up);  // lane 0 of warp 0
-//   __device__ static void load_a(const Params&, const TileInfo&, void *dst, uint64_t *bar, int kb);
-//   __device__ static void load_b(const Params&, const TileInfo&, void *dst, uint64_t *bar, int kb);
-//   __device__ static uint32_t b_bytes(const TileInfo&);
+//   __device__ static void tile(const Params&, int64_t item, TileInfo&, int half);
+//   __device__ static void before_a(const Params&, const TileInfo&, bool &gave_up);  // loader thread
+//   template <int PAIR> __device__ static void load_a(const Params&, const TileInfo&, void *dst,
+//                                                     uint32_t bar, int kb);
+//   template <int PAIR> __device__ static void load_b(const Params&, const TileInfo&, void *dst,
+//                                                     uint32_t bar, int kb, int col0, int cols);
+//   __device__ static uint32_t b_bytes(const Params&, const TileInfo&, int cols);
 //   __device__ static void store_chunk(const Params&, const TileInfo&, const void *buf, int ch, int q);
 //   __device__ static void after_tile(const Params&, const TileInfo&, int q, int lane);  // per epilogue warp
-template <class P>
-__device__ void gemm_consumer(const typename P::Params &p, uint8_t *smem, int cta, int ncta)
+// The load hooks receive the mbarrier as a shared::cluster address (the
+// leader's barrier in pair mode) and issue pair TMA when PAIR is set.  All
+// tcgen05 and TMA instructions of one kernel use a single cta_group.
+template <class P, int PAIR>
+__device__ void gemm_consumer(const typename P::Params &p, uint8_t *smem, int unit, int nunits)
 {
     using namespace gm;
+    using S = Shape<PAIR>;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const int half = PAIR ? (int)cluster_ctarank() : 0;
+    const bool leader = half == 0;
     PipeSmem *ps = reinterpret_cast<PipeSmem *>(smem + OFF_BAR);
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < STAGES; ++i) {
+        for (int i = 0; i < S::STAGES; ++i) {
             mbar_init(&ps->full[i], 1);
             mbar_init(&ps->empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&ps->tfull[i], 1);
-            mbar_init(&ps->tempty[i], EPI_WARPS);
+            mbar_init(&ps->tempty[i], EPI_WARPS * (PAIR ? 2 : 1));
         }
         mbar_init(&ps->drain, 1);
         ps->issued = 0;
@@ -109,38 +136,53 @@ __device__ void gemm_consumer(const typename P::Params &p, uint8_t *smem, int ct
         fence_mbar_init();
     }
     if (warp == 1) {
-        tmem_alloc(&ps->tmem_base, TMEM_COLS);
-        tmem_relinquish();
+        if (PAIR) {
+            tmem_alloc_pair(&ps->tmem_base, TMEM_COLS);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(&ps->tmem_base, TMEM_COLS);
+            tmem_relinquish();
+        }
         tc_fence_before();
     }
     __syncthreads();
+    if (PAIR)
+        cluster_sync(); // the peer's barriers are initialised before any remote use
     tc_fence_after();
     const uint32_t tmem_base = ps->tmem_base;
     const int64_t items = P::num_items(p);
     const uint64_t tmo = p.pipe_timeout_ns;
+    // the barrier a load completes on / an epilogue releases: the leader's
+    const uint32_t full0 = PAIR ? mapa_shared(smem_u32(&ps->full[0]), 0) : smem_u32(&ps->full[0]);
+    const uint32_t tempty0 = PAIR ? mapa_shared(smem_u32(&ps->tempty[0]), 0) : smem_u32(&ps->tempty[0]);
 
     if (warp == 0) {
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
             bool gave_up = false;
-            for (int64_t it = cta; it < items && !ps->abort; it += ncta) {
+            for (int64_t it = unit; it < items && !ps->abort; it += nunits) {
                 TileInfo ti;
-                P::tile(p, it, ti);
+                P::tile(p, it, ti, half);
                 P::before_a(p, ti, gave_up);
-                const uint32_t bytes = A_BYTES + P::b_bytes(ti);
+                const int cols = PAIR ? ti.n_mma / 2 : ti.n_mma;
+                const int col0 = ti.n0 + (PAIR ? half * cols : 0);
+                const uint32_t my_bytes = A_BYTES + P::b_bytes(p, ti, cols);
                 for (int kb = 0; kb < p.k_blocks; ++kb) {
                     if (!mbar_wait(&ps->empty[stage], phase ^ 1u, tmo)) {
                         report_fault(p.status, TDG_ERR_TIMEOUT, TDG_WHERE_PIPE, 0, p.epoch);
                         ps->abort = 1;
                         break;
                     }
-                    uint8_t *sa = smem + stage * STAGE_BYTES;
-                    mbar_arrive_expect_tx(&ps->full[stage], bytes);
-                    P::load_a(p, ti, sa, &ps->full[stage], kb);
-                    P::load_b(p, ti, sa + A_BYTES, &ps->full[stage], kb);
+                    uint8_t *sa = smem + stage * S::STAGE_BYTES;
+                    // the leader arms its barrier for both CTAs' bytes
+                    if (leader)
+                        mbar_arrive_expect_tx(&ps->full[stage], PAIR ? 2 * my_bytes : my_bytes);
+                    const uint32_t bar = full0 + stage * 8;
+                    P::template load_a<PAIR>(p, ti, sa, bar, kb);
+                    P::template load_b<PAIR>(p, ti, sa + A_BYTES, bar, kb, col0, cols);
                     ps->issued += 1;
-                    if (++stage == STAGES) {
+                    if (++stage == S::STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
@@ -149,17 +191,16 @@ __device__ void gemm_consumer(const typename P::Params &p, uint8_t *smem, int ct
         }
         __syncwarp();
     } else if (warp == 1) {
-        if (lane == 0) {
+        if (lane == 0 && leader) {
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
             const uint32_t sbase = smem_u32(smem);
-            for (int64_t it = cta; it < items && !ps->abort; it += ncta) {
+            for (int64_t it = unit; it < items && !ps->abort; it += nunits) {
                 TileInfo ti;
-                P::tile(p, it, ti);
-                const int n_mma = (ti.n_valid + 15) & ~15;
-                const uint32_t idesc = idesc_bf16(BM, n_mma, P::B_MN);
+                P::tile(p, it, ti, half);
+                const uint32_t idesc = idesc_bf16(S::TILE_M, ti.n_mma, P::B_MN);
                 if (!mbar_wait(&ps->tempty[acc], acc_phase ^ 1u, tmo)) {
                     report_fault(p.status, TDG_ERR_TIMEOUT, TDG_WHERE_PIPE, 1, p.epoch);
                     ps->abort = 1;
@@ -176,7 +217,7 @@ __device__ void gemm_consumer(const typename P::Params &p, uint8_t *smem, int ct
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_addr = sbase + stage * STAGE_BYTES;
+                    const uint32_t a_addr = sbase + stage * S::STAGE_BYTES;
                     const uint32_t b_addr = a_addr + A_BYTES;
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k) {
@@ -186,18 +227,27 @@ __device__ void gemm_consumer(const typename P::Params &p, uint8_t *smem, int ct
                         // K-major B: same form as A.
                         const uint64_t bd = P::B_MN ? sdesc_sw128(b_addr + k * 2048, 8192, 1024)
                                                     : sdesc_sw128(b_addr + k * 32, 16, 1024);
-                        umma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+                        if (PAIR)
+                            umma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+                        else
+                            umma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
                     }
-                    umma_commit(&ps->empty[stage]);
+                    if (PAIR)
+                        umma_commit_pair(&ps->empty[stage]);
+                    else
+                        umma_commit(&ps->empty[stage]);
                     ps->consumed += 1;
-                    if (++stage == STAGES) {
+                    if (++stage == S::STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok)
                     break;
-                umma_commit(&ps->tfull[acc]);
+                if (PAIR)
+                    umma_commit_pair(&ps->tfull[acc]);
+                else
+                    umma_commit(&ps->tfull[acc]);
                 if (++acc == 2) {
                     acc = 0;
                     acc_phase ^= 1u;
@@ -205,7 +255,10 @@ __device__ void gemm_consumer(const typename P::Params &p, uint8_t *smem, int ct
             }
             if (ps->abort) {
                 // let every MMA this thread issued finish before TMEM is freed
-                umma_commit(&ps->drain);
+                if (PAIR)
+                    umma_commit_pair(&ps->drain);
+                else
+                    umma_commit(&ps->drain);
                 (void)mbar_wait(&ps->drain, 0, tmo);
             }
         }
@@ -217,9 +270,9 @@ __device__ void gemm_consumer(const typename P::Params &p, uint8_t *smem, int ct
         int acc = 0;
         uint32_t acc_phase = 0;
         int buf = 0;
-        for (int64_t it = cta; it < items; it += ncta) {
+        for (int64_t it = unit; it < items; it += nunits) {
             TileInfo ti;
-            P::tile(p, it, ti);
+            P::tile(p, it, ti, half);
             bool ok = mbar_wait(&ps->tfull[acc], acc_phase, tmo);
             if (!ok || ps->abort) {
                 if (lane == 0 && !ok)
@@ -242,12 +295,11 @@ __device__ void gemm_consumer(const typename P::Params &p, uint8_t *smem, int ct
                 uint8_t *row = bufs + buf * EPI_BUF + lane * 128;
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    uint32_t w0, w1, w2, w3;
                     const uint32_t *src = (j < 4) ? &r0[j * 8] : &r1[(j - 4) * 8];
-                    w0 = pack_bf16x2(__uint_as_float(src[0]), __uint_as_float(src[1]));
-                    w1 = pack_bf16x2(__uint_as_float(src[2]), __uint_as_float(src[3]));
-                    w2 = pack_bf16x2(__uint_as_float(src[4]), __uint_as_float(src[5]));
-                    w3 = pack_bf16x2(__uint_as_float(src[6]), __uint_as_float(src[7]));
+                    const uint32_t w0 = pack_bf16x2(__uint_as_float(src[0]), __uint_as_float(src[1]));
+                    const uint32_t w1 = pack_bf16x2(__uint_as_float(src[2]), __uint_as_float(src[3]));
+                    const uint32_t w2 = pack_bf16x2(__uint_as_float(src[4]), __uint_as_float(src[5]));
+                    const uint32_t w3 = pack_bf16x2(__uint_as_float(src[6]), __uint_as_float(src[7]));
                     *reinterpret_cast<uint4 *>(row + ((j ^ (lane & 7)) << 4)) = make_uint4(w0, w1, w2, w3);
                 }
                 fence_proxy_async_smem();
@@ -260,8 +312,12 @@ __device__ void gemm_consumer(const typename P::Params &p, uint8_t *smem, int ct
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&ps->tempty[acc]);
+            if (lane == 0) {
+                if (PAIR)
+                    mbar_arrive_remote(tempty0 + acc * 8);
+                else
+                    mbar_arrive(&ps->tempty[acc]);
+            }
             if (++acc == 2) {
                 acc = 0;
                 acc_phase ^= 1u;
@@ -273,15 +329,26 @@ __device__ void gemm_consumer(const typename P::Params &p, uint8_t *smem, int ct
     }
     __syncthreads();
     if (ps->abort && threadIdx.x == 0) {
-        // wait (bounded) for ring fills that were issued but never consumed,
-        // so no TMA write lands in shared memory after the CTA has exited
-        for (uint32_t f = ps->consumed; f < ps->issued; ++f)
-            (void)mbar_wait(&ps->full[f % STAGES], (f / STAGES) & 1u, tmo);
+        // wait (bounded) until no TMA write of this CTA is still in flight.
+        if (!PAIR || leader) {
+            for (uint32_t f = ps->consumed; f < ps->issued; ++f)
+                (void)mbar_wait(&ps->full[f % S::STAGES], (f / S::STAGES) & 1u, tmo);
+        } else {
+            // a peer's fill is known done once the leader has freed its slot
+            for (uint32_t f = ps->issued > (uint32_t)S::STAGES ? ps->issued - S::STAGES : 0u;
+                 f < ps->issued; ++f)
+                (void)mbar_wait(&ps->empty[f % S::STAGES], (f / S::STAGES) & 1u, tmo);
+        }
     }
     __syncthreads();
+    if (PAIR)
+        cluster_sync(); // neither CTA leaves while the other may still touch it
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, TMEM_COLS);
+        if (PAIR)
+            tmem_dealloc_pair(tmem_base, TMEM_COLS);
+        else
+            tmem_dealloc(tmem_base, TMEM_COLS);
     }
 }
 

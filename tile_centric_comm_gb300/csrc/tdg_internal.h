@@ -66,7 +66,17 @@ cudaError_t set_smem(const void *fn, int bytes);
 // Launch with the cooperative attribute (all CTAs co-resident, which the
 // cross-CTA signal waits rely on).
 cudaError_t launch(const void *fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s,
-                   void **args, bool cooperative);
+                   void **args, bool cooperative, int cluster = 1);
+
+// Number of 2-CTA clusters of `fn` that can be resident at once (0 on error).
+int max_pairs(const void *fn, int block, int smem);
+
+// CTA pairs (cta_group::2) unless TDG_PAIR=0 is set in the environment.
+inline bool pairs_enabled()
+{
+    const char *e = getenv("TDG_PAIR");
+    return !(e && e[0] == '0');
+}
 
 int occupancy_ok(const void *fn, int block, int smem, int grid, int sm_count);
 

@@ -33,7 +33,9 @@ struct RsParams {
     int k_blocks;
     int W;
     int64_t M, K, N, Mo;
-    int mt;      // m tiles per owner (Mo / 128)
+    int mt;      // 128-row tiles per owner (Mo / 128): the staging layout
+    int mtp;     // scheduled tiles per owner (Mo / 128, or Mo / 256 with pairs)
+    int pair;    // 1: CTA pairs (cta_group::2) with 256-row tiles
     int n_tiles;
     int order;   // 0: owner, rank, m, n (rank outside m, n); 1: rank fastest
     int fused_reduce;
@@ -113,12 +115,12 @@ template <int BMN> struct RsPolicy {
 
     __device__ static int64_t num_items(const Params &p)
     {
-        return (int64_t)p.W * p.W * p.mt * p.n_tiles;
+        return (int64_t)p.W * p.W * p.mtp * p.n_tiles;
     }
 
-    __device__ static void tile(const Params &p, int64_t item, TileInfo &t)
+    __device__ static void tile(const Params &p, int64_t item, TileInfo &t, int half)
     {
-        const int64_t per_rank = (int64_t)p.mt * p.n_tiles;
+        const int64_t per_rank = (int64_t)p.mtp * p.n_tiles;
         int o, r;
         int64_t rem;
         if (p.order == 1) {
@@ -135,36 +137,52 @@ template <int BMN> struct RsPolicy {
         }
         t.owner = o;
         t.a_sel = r;
-        t.m_loc = (int)(rem / p.n_tiles);
+        t.m_loc = (int)(rem / p.n_tiles) * (p.pair ? 2 : 1) + half; // 128-row tile in the owner
         t.pn = (int)(rem % p.n_tiles);
         t.m0 = (o * p.mt + t.m_loc) * gm::BM;
         t.a_row = t.m0;
         t.n0 = t.pn * gm::BN;
         t.n_valid = (int)min((int64_t)gm::BN, p.N - t.n0);
+        const int q = p.pair ? 32 : 16;
+        t.n_mma = (t.n_valid + q - 1) / q * q;
     }
 
     __device__ static void before_a(const Params &, const TileInfo &, bool &) {}
 
-    __device__ static void load_a(const Params &p, const TileInfo &t, void *dst, uint64_t *bar, int kb)
+    // The TMA form is chosen at compile time: a kernel holds either only
+    // cta_group::1 or only cta_group::2 instructions, never both.
+    template <int PAIR>
+    __device__ static void load(void *dst, const CUtensorMap *m, uint32_t bar, int x, int y, int z)
     {
-        tma_load_3d(dst, &p.tmA, bar, kb * gm::BK, t.a_row, t.a_sel);
+        if constexpr (PAIR)
+            tma_load_3d_pair(dst, m, bar, x, y, z);
+        else
+            tma_load_3d_addr(dst, m, bar, x, y, z);
     }
 
-    __device__ static void load_b(const Params &p, const TileInfo &t, void *dst, uint64_t *bar, int kb)
+    template <int PAIR>
+    __device__ static void load_a(const Params &p, const TileInfo &t, void *dst, uint32_t bar, int kb)
+    {
+        load<PAIR>(dst, &p.tmA, bar, kb * gm::BK, t.a_row, t.a_sel);
+    }
+
+    template <int PAIR>
+    __device__ static void load_b(const Params &p, const TileInfo &t, void *dst, uint32_t bar, int kb,
+                                  int col0, int cols)
     {
         if (BMN) {
-            const int nch = (t.n_valid + 63) >> 6;
+            const int nch = (cols + 63) >> 6;
             for (int j = 0; j < nch; ++j)
-                tma_load_3d(static_cast<uint8_t *>(dst) + j * 8192, &p.tmB, bar, t.n0 + 64 * j,
-                            kb * gm::BK, t.a_sel);
+                load<PAIR>(static_cast<uint8_t *>(dst) + j * 8192, &p.tmB, bar, col0 + 64 * j, kb * gm::BK,
+                           t.a_sel);
         } else {
-            tma_load_3d(dst, &p.tmB, bar, kb * gm::BK, t.n0, t.a_sel);
+            load<PAIR>(dst, &p.tmB, bar, kb * gm::BK, col0, t.a_sel);
         }
     }
 
-    __device__ static uint32_t b_bytes(const TileInfo &t)
+    __device__ static uint32_t b_bytes(const Params &p, const TileInfo &, int cols)
     {
-        return BMN ? (uint32_t)(((t.n_valid + 63) >> 6) * 8192) : (uint32_t)gm::B_BYTES;
+        return BMN ? (uint32_t)(((cols + 63) >> 6) * 8192) : (uint32_t)((p.pair ? gm::BN / 2 : gm::BN) * gm::BK * 2);
     }
 
     // push: the partial tile goes to the owner's staging area
@@ -197,12 +215,15 @@ template <int BMN> struct RsPolicy {
     }
 };
 
-template <int BMN>
+template <int BMN, int PAIR>
 __global__ void __launch_bounds__(gm::NUM_THREADS, 1) rs_gemm_kernel(const __grid_constant__ RsParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
-    gemm_consumer<RsPolicy<BMN>>(p, smem, (int)blockIdx.x, (int)gridDim.x);
+    if (PAIR)
+        gemm_consumer<RsPolicy<BMN>, 1>(p, smem, (int)blockIdx.x >> 1, (int)gridDim.x >> 1);
+    else
+        gemm_consumer<RsPolicy<BMN>, 0>(p, smem, (int)blockIdx.x, (int)gridDim.x);
 }
 
 // SERIAL reduction: one 4-warp CTA per output tile.
@@ -272,13 +293,14 @@ extern "C" int tdg_gemm_rs(tdg_symm *h, const tdg_gemm_rs_args *a, void *stream)
         return TDG_OK;
     }
 
+    const int pair = (pairs_enabled() && Mo % (2 * gm::BM) == 0) ? 1 : 0;
     RsParams p;
     memset(&p, 0, sizeof p);
     bool ok = map_bf16_3d(&p.tmA, h->base + a->a_off, K, M, W, K * 2, R, 64, gm::BM, 1);
     if (a->b_layout == TDG_B_KN)
         ok = ok && map_bf16_3d(&p.tmB, h->base + a->b_off, N, K, W, N * 2, R, 64, 64, 1);
     else
-        ok = ok && map_bf16_3d(&p.tmB, h->base + a->b_off, K, N, W, K * 2, R, 64, 256, 1);
+        ok = ok && map_bf16_3d(&p.tmB, h->base + a->b_off, K, N, W, K * 2, R, 64, pair ? 128 : 256, 1);
     const uint64_t rows_per_owner = (uint64_t)W * mt * n_tiles * gm::BM;
     ok = ok && map_bf16_3d(&p.tmS, h->base + a->stage_off, gm::BN, rows_per_owner, W, gm::BN * 2, R, 64, 32, 1);
     if (!ok)
@@ -294,6 +316,8 @@ extern "C" int tdg_gemm_rs(tdg_symm *h, const tdg_gemm_rs_args *a, void *stream)
     p.N = N;
     p.Mo = Mo;
     p.mt = mt;
+    p.pair = pair;
+    p.mtp = pair ? mt / 2 : mt;
     p.n_tiles = n_tiles;
     p.order = getenv("TDG_RS_ORDER") ? atoi(getenv("TDG_RS_ORDER")) : 0;
     p.fused_reduce = a->mode == TDG_MODE_SM ? 1 : 0;
@@ -304,18 +328,32 @@ extern "C" int tdg_gemm_rs(tdg_symm *h, const tdg_gemm_rs_args *a, void *stream)
     p.counters = h->counters;
     p.nsig = h->nsig;
 
-    const void *fn = a->b_layout == TDG_B_KN ? reinterpret_cast<const void *>(&rs_gemm_kernel<1>)
-                                             : reinterpret_cast<const void *>(&rs_gemm_kernel<0>);
-    static bool smem_set[2][64] = {};
-    bool &done = smem_set[a->b_layout & 1][h->device & 63];
+    const void *fn;
+    if (a->b_layout == TDG_B_KN)
+        fn = pair ? reinterpret_cast<const void *>(&rs_gemm_kernel<1, 1>)
+                  : reinterpret_cast<const void *>(&rs_gemm_kernel<1, 0>);
+    else
+        fn = pair ? reinterpret_cast<const void *>(&rs_gemm_kernel<0, 1>)
+                  : reinterpret_cast<const void *>(&rs_gemm_kernel<0, 0>);
+    static bool smem_set[2][2][64] = {};
+    bool &done = smem_set[a->b_layout & 1][pair][h->device & 63];
     if (!done) {
         cudaError_t e = set_smem(fn, gm::SMEM_BYTES);
         if (e != cudaSuccess)
             return cuda_err(e, "rs set smem");
         done = true;
     }
+    int grid = h->sm_count;
+    if (pair) {
+        const int mp = max_pairs(fn, gm::NUM_THREADS, gm::SMEM_BYTES);
+        const int pairs = mp < h->sm_count / 2 ? mp : h->sm_count / 2;
+        if (pairs <= 0)
+            return TDG_ERR_UNSUPPORTED;
+        grid = 2 * pairs;
+    }
     void *args[] = {&p};
-    int rc = cuda_err(launch(fn, dim3(h->sm_count), dim3(gm::NUM_THREADS), gm::SMEM_BYTES, s, args, false),
+    int rc = cuda_err(launch(fn, dim3(grid), dim3(gm::NUM_THREADS), gm::SMEM_BYTES, s, args, false,
+                             pair ? 2 : 1),
                       "rs gemm launch");
     if (rc != TDG_OK || a->mode == TDG_MODE_SM)
         return rc;
