@@ -41,17 +41,36 @@ WORKLOAD = ("qwen32b_mlp_tp8: AG-GEMM up-proj (W=8, A_r 1024x5120, B 5120x3200) 
             "GEMM-RS down-proj (W=8, A_r 8192x3200, B_r 3200x5120), bf16 in, fp32 accumulate, bf16 out")
 
 
+# DRAM traffic of one rs_gemm_kernel launch at this workload, dram__bytes_read.sum +
+# dram__bytes_write.sum from one ncu capture (2.632 GB read + 0.743 GB written).  It is
+# reported only while the kernel's sources still hash to the value the capture was taken with.
+RS_TRAFFIC = {"sources": "4a3dd7b362a71a12", "bytes": 2_631_706_000 + 742_750_208}
+RS_SOURCES = ["tdg_gemm.cuh", "tdg_rs.cu", "tdg_ptx.cuh"]
+
+
+def rs_sources_hash():
+    import hashlib
+    h = hashlib.sha256()
+    for f in RS_SOURCES:
+        with open(os.path.join(ROOT, "tile_centric_comm_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="tdg", choices=["tdg", "reference"])
-    ap.add_argument("--mode", default="sm", choices=["sm", "ce"])
+    ap.add_argument("--mode", default="ce", choices=["sm", "ce"],
+                    help="AG-GEMM overlap: ce = copy engine + flags (default), sm = producer CTAs")
     ap.add_argument("--producers", type=int, default=0)
     ap.add_argument("--no-extras", action="store_true", help="skip serial/e2e/MoE/CPU legs")
     ap.add_argument("--no-cpu", action="store_true")
-    ap.add_argument("--only", default="", help="debug: 'ag' or 'rs' alone")
+    ap.add_argument("--only", default="", help="measure 'ag' or 'rs' alone (not the bench line)")
+    ap.add_argument("--ag-shape", default="", help="W,Ms,K,N for --only ag, e.g. 8,2048,8192,7168 "
+                    "(the Llama-3-70B gate+up shape)")
     return ap.parse_args()
 
 
@@ -88,8 +107,16 @@ class Clocks:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
+            # the timed region starts only once the sampler is producing lines
+            t0 = time.time()
+            while time.time() - t0 < 10:
+                self.f.flush()
+                if os.path.getsize(self.path) > 0:
+                    break
+                time.sleep(0.05)
+            self.start_line = sum(1 for _ in open(self.path))
         except Exception:
             self.proc = None
         return self
@@ -107,7 +134,9 @@ class Clocks:
         if self.proc is None or not os.path.exists(self.path):
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         rows = []
-        for line in open(self.path):
+        for i, line in enumerate(open(self.path)):
+            if i < getattr(self, "start_line", 0):
+                continue
             parts = [x.strip() for x in line.split(",")]
             if len(parts) >= 9:
                 rows.append(parts)
@@ -220,25 +249,27 @@ class MLP:
 
 
 def timed_steps(torch, fns, steps, warmup, flush):
-    """Run `fns` (list of callables, one part each) per step; flush L2 before
-    every step; return per-part lists of device times (ms) for the timed steps."""
+    """Run `fns` (one callable per part) once per step, flushing L2 before every
+    step (outside the events); return per-part lists of device times (ms) of the
+    timed steps.  The GPU runs the steps back to back; the host waits once."""
     n = len(fns)
     stream = torch.cuda.current_stream()
-    res = [[] for _ in range(n)]
-    for it in range(warmup + steps):
+    for _ in range(warmup):
         flush.zero_()
-        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
-        evs[0].record(stream)
+        for f in fns:
+            f()
+    torch.cuda.synchronize()
+    evs = []
+    for _ in range(steps):
+        flush.zero_()
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+        e[0].record(stream)
         for i, f in enumerate(fns):
             f()
-            evs[i + 1].record(stream)
-        if it >= warmup:
-            res_it = evs
-            torch.cuda.synchronize()
-            for i in range(n):
-                res[i].append(res_it[i].elapsed_time(res_it[i + 1]))
+            e[i + 1].record(stream)
+        evs.append(e)
     torch.cuda.synchronize()
-    return res
+    return [[e[i].elapsed_time(e[i + 1]) for e in evs] for i in range(n)]
 
 
 def cpu_oracle_rate(sample_rows_ag=256, sample_rows_rs=64):
@@ -332,6 +363,11 @@ def run_reference(args, rank):
 def main():
     args = parse()
     rank, world, local = dist_env()
+    if args.ag_shape:
+        if args.only != "ag":
+            raise SystemExit("--ag-shape needs --only ag")
+        W, Ms, K, N = (int(x) for x in args.ag_shape.split(","))
+        AG.update(W=W, Ms=Ms, K=K, N=N)
     if args.impl == "reference":
         run_reference(args, rank)
         return
@@ -376,7 +412,8 @@ def main():
         pg.all_reduce(t, op=pg.ReduceOp.MAX)
         total_ms = float(t.item())
     ms_per_step = total_ms / args.steps
-    flop = (AG_FLOP if args.only != "rs" else 0) + (RS_FLOP if args.only != "ag" else 0)
+    ag_flop = 2 * AG["W"] * AG["Ms"] * AG["K"] * AG["N"]
+    flop = (ag_flop if args.only != "rs" else 0) + (RS_FLOP if args.only != "ag" else 0)
     value = world * flop * args.steps / (total_ms * 1e-3) / 1e12
     launches = 2 * args.steps if not args.only else args.steps
     ag_ms = statistics.mean(parts[0]) if args.only != "rs" else None
@@ -397,11 +434,13 @@ def main():
                              "overlap_gain_vs_serial": s_rs / rs_ms,
                              "frac_of_bf16_peak": RS_FLOP / rs_ms / 1e9 / pk["bf16"]}
         extras["overlap_gain_vs_serial"] = (s_ag + s_rs) / (ag_ms + rs_ms)
-        if args.mode == "sm":
-            cparts = timed_steps(torch, [lambda: mlp.ag_call("ce")], args.steps, args.warmup, flush)
-            c_ag = statistics.mean(cparts[0])
-            extras["ag_gemm"]["ce_mode_ms"] = c_ag
-            extras["ag_gemm"]["ce_mode_tflops"] = AG_FLOP / c_ag / 1e9
+        other = "sm" if args.mode == "ce" else "ce"
+        cparts = timed_steps(torch, [lambda: mlp.ag_call(other)], args.steps, args.warmup, flush)
+        c_ag = statistics.mean(cparts[0])
+        extras["ag_gemm"]["mode"] = args.mode
+        extras["ag_gemm"][f"{other}_mode_ms"] = c_ag
+        extras["ag_gemm"][f"{other}_mode_tflops"] = AG_FLOP / c_ag / 1e9
+        extras["ag_gemm"][f"{other}_mode_overlap_gain_vs_serial"] = s_ag / c_ag
         mlp.check_status()
         # end to end through the public API with host buffers
         def e2e_step():
@@ -443,11 +482,15 @@ def main():
 
     # roofline of the dominant kernel (the GEMM-RS persistent GEMM, one launch per call)
     dom_ms = rs_ms if rs_ms is not None else ag_ms
-    dom_flop = RS_FLOP if rs_ms is not None else AG_FLOP
+    dom_flop = RS_FLOP if rs_ms is not None else ag_flop
     achieved = dom_flop / dom_ms / 1e9
     roofline = {"kernel": "rs_gemm_kernel" if rs_ms is not None else "ag_gemm_kernel",
                 "bound": "tensor", "achieved": achieved, "peak": pk["bf16"], "unit": "TFLOP/s",
-                "frac": achieved / pk["bf16"], "traffic": None,
+                "frac": achieved / pk["bf16"],
+                "traffic": (RS_TRAFFIC["bytes"] if rs_ms is not None and rs_sources_hash() == RS_TRAFFIC["sources"]
+                            else None),
+                "traffic_unit": "bytes per launch",
+                "algorithmic_bytes": 1_352_000_000 + 755_000_000 if rs_ms is not None else None,
                 "peak_kind": f"bf16 dense burst, {pk['src']}",
                 "frac_of_sustained": achieved / pk["bf16_sus"]}
     line = {"metric": "AG-GEMM+GEMM-RS TFLOP/s (qwen32b_mlp_tp8)", "value": value, "unit": "TFLOP/s",
@@ -455,7 +498,8 @@ def main():
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
             "config": {"workload": WORKLOAD, "l2": "flushed before every step (256 MB write)",
-                       "mode": args.mode, "producers": args.producers or 16, "sm_count": sms,
+                       "ag_mode": args.mode, "rs_mode": "sm (push + last-arriver reduction)",
+                       "producers": (args.producers or 16) if args.mode == "sm" else None, "sm_count": sms,
                        "parallelism": f"replicas x{world}, 8 logical ranks each"},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
             "clocks": clocks, "parts": extras}

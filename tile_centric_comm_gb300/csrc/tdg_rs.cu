@@ -4,9 +4,10 @@
 // by signals).
 //
 // One persistent tcgen05 GEMM runs every rank's partial product.  Work items
-// are (owner o, rank r, m tile inside o, n tile); by default all ranks'
-// items of one owner block run back to back, so every output tile gathers
-// its W partials close together in time.  The epilogue pushes each bf16
+// are (owner block, rank r, owner o in the block, m tile inside o, n tile):
+// all ranks' items of one block of two owners run back to back, so every
+// output tile gathers its W partials close together in time while each B_r
+// is streamed once per block.  The epilogue pushes each bf16
 // partial tile (tile-contiguous, 128 x 256) into owner o's staging area
 // (region o) with TMA, waits for the write to complete, fences the async
 // proxy, and increments the owner's per-(tile, row-quarter) arrival counter
@@ -37,7 +38,8 @@ struct RsParams {
     int mtp;     // scheduled tiles per owner (Mo / 128, or Mo / 256 with pairs)
     int pair;    // 1: CTA pairs (cta_group::2) with 256-row tiles
     int n_tiles;
-    int order;   // 0: owner, rank, m, n (rank outside m, n); 1: rank fastest
+    int order;   // 0: owner blocks of `ob` owners, then rank, owner, m, n; 1: rank fastest
+    int ob;      // owners per block in order 0 (1 = owner by owner, W = rank-major)
     int fused_reduce;
     uint8_t *regions;
     uint64_t region_bytes;
@@ -129,10 +131,15 @@ template <int BMN> struct RsPolicy {
             o = (int)(rest / per_rank);
             rem = rest % per_rank;
         } else {
-            const int64_t per_owner = (int64_t)p.W * per_rank;
-            o = (int)(item / per_owner);
-            const int64_t x = item % per_owner;
-            r = (int)(x / per_rank);
+            // blocks of ob owners; inside a block every rank's tiles run back
+            // to back, so B_r is streamed once per block and every output tile
+            // of the block gathers its W partials within the block
+            const int64_t per_block = (int64_t)p.W * p.ob * per_rank;
+            const int blk = (int)(item / per_block);
+            int64_t x = item % per_block;
+            r = (int)(x / (p.ob * per_rank));
+            x %= p.ob * per_rank;
+            o = blk * p.ob + (int)(x / per_rank);
             rem = x % per_rank;
         }
         t.owner = o;
@@ -320,6 +327,11 @@ extern "C" int tdg_gemm_rs(tdg_symm *h, const tdg_gemm_rs_args *a, void *stream)
     p.mtp = pair ? mt / 2 : mt;
     p.n_tiles = n_tiles;
     p.order = getenv("TDG_RS_ORDER") ? atoi(getenv("TDG_RS_ORDER")) : 0;
+    // two owners per block measured best at the Qwen-32B down-projection shape
+    // (B_r streamed W/2 times instead of W; partials of a block stay L2-warm)
+    p.ob = getenv("TDG_RS_OB") ? atoi(getenv("TDG_RS_OB")) : 2;
+    if (p.ob < 1 || W % p.ob)
+        p.ob = W % 2 == 0 ? 2 : 1;
     p.fused_reduce = a->mode == TDG_MODE_SM ? 1 : 0;
     p.regions = h->base;
     p.region_bytes = R;
