@@ -222,24 +222,58 @@ class MLP:
         self.tdg.gemm_rs(self.rs, RS["M"], RS["K"], RS["N"], self.rs_a_off, self.rs_b_off,
                          self.rs_s_off, self.rs_o_off, mode=mode)
 
-    def upload(self):
-        """host -> device copies of one step's inputs (pinned, async)."""
+    def upload_ag(self):
+        """host -> device copies of the AG-GEMM inputs (pinned, async)."""
         t = self.torch
         Ms, K = AG["Ms"], AG["K"]
         for s in range(AG["W"]):
             self.ag.view(s, 0, (Ms, K), t.bfloat16).copy_(self.ag_host[s], non_blocking=True)
         self.ag_B.copy_(self.ag_B_host, non_blocking=True)
+
+    def upload_rs(self):
+        t = self.torch
         M, K, N = RS["M"], RS["K"], RS["N"]
         for r in range(RS["W"]):
             self.rs.view(r, self.rs_a_off, (M, K), t.bfloat16).copy_(self.rs_A_host[r], non_blocking=True)
             self.rs.view(r, self.rs_b_off, (K, N), t.bfloat16).copy_(self.rs_B_host[r], non_blocking=True)
 
-    def download(self):
+    def download_ag(self):
         self.C_host.copy_(self.ag_C, non_blocking=True)
+
+    def download_rs(self):
         Mo, N = RS["M"] // RS["W"], RS["N"]
         for o in range(RS["W"]):
             self.out_host[o].copy_(self.rs.view(o, self.rs_o_off, (Mo, N), self.torch.bfloat16),
                                    non_blocking=True)
+
+    def e2e_step(self):
+        """One step through the public API with host buffers: uploads on a copy
+        stream overlap the compute of the previous operation, and the AG output
+        downloads while the GEMM-RS runs."""
+        t = self.torch
+        ms = t.cuda.current_stream()
+        if not hasattr(self, "_copy_stream"):
+            self._copy_stream = t.cuda.Stream()
+        cs = self._copy_stream
+        start = t.cuda.Event()
+        start.record(ms)
+        cs.wait_event(start)               # nothing of this step starts before it
+        ag_in, rs_in, ag_done = t.cuda.Event(), t.cuda.Event(), t.cuda.Event()
+        with t.cuda.stream(cs):
+            self.upload_ag()
+            ag_in.record(cs)
+            self.upload_rs()
+            rs_in.record(cs)
+        ms.wait_event(ag_in)
+        self.ag_call()
+        ag_done.record(ms)
+        ms.wait_event(rs_in)
+        self.rs_call("sm")
+        with t.cuda.stream(cs):
+            cs.wait_event(ag_done)
+            self.download_ag()
+        self.download_rs()
+        ms.wait_stream(cs)
 
     def check_status(self):
         for s in (self.ag, self.rs):
@@ -443,18 +477,26 @@ def main():
         extras["ag_gemm"][f"{other}_mode_overlap_gain_vs_serial"] = s_ag / c_ag
         mlp.check_status()
         # end to end through the public API with host buffers
-        def e2e_step():
-            mlp.upload()
-            mlp.ag_call()
-            mlp.rs_call("sm")
-            mlp.download()
-        eparts = timed_steps(torch, [e2e_step], args.steps, args.warmup, flush)
+        eparts = timed_steps(torch, [mlp.e2e_step], args.steps, args.warmup, flush)
         e_ms = statistics.mean(eparts[0])
         e2e = {"value": STEP_FLOP / e_ms / 1e9, "unit": "TFLOP/s",
                "h2d_bytes_per_step": mlp.h2d_bytes, "d2h_bytes_per_step": mlp.d2h_bytes,
                "ms_per_step": e_ms}
         mlp.check_status()
-        del mlp
+        # context: the library GEMM (cuBLAS through torch.matmul) on the same
+        # shapes, with no communication at all (not part of the path)
+        a_cat = mlp.ag.view(0, mlp.ag_g_off, (AG["W"] * AG["Ms"], AG["K"]), torch.bfloat16)
+        b_rs = [mlp.rs.view(r, mlp.rs_b_off, (RS["K"], RS["N"]), torch.bfloat16) for r in range(RS["W"])]
+        a_rs = [mlp.rs.view(r, mlp.rs_a_off, (RS["M"], RS["K"]), torch.bfloat16) for r in range(RS["W"])]
+        c_rs = torch.empty((RS["M"], RS["N"]), dtype=torch.bfloat16, device="cuda")
+        lparts = timed_steps(torch, [lambda: torch.matmul(a_cat, mlp.ag_B, out=mlp.ag_C),
+                                     lambda: [torch.matmul(a_rs[r], b_rs[r], out=c_rs) for r in range(RS["W"])]],
+                             args.steps, args.warmup, flush)
+        l_ag, l_rs = statistics.mean(lparts[0]), statistics.mean(lparts[1])
+        extras["library_gemm_context"] = {
+            "what": "torch.matmul (cuBLAS) on the same GEMM shapes, no AllGather / ReduceScatter",
+            "ag_shape_tflops": AG_FLOP / l_ag / 1e9, "rs_shapes_tflops": RS_FLOP / l_rs / 1e9}
+        del mlp, a_cat, b_rs, a_rs, c_rs
         torch.cuda.empty_cache()
         # MoE dispatch + combine
         moe = MoEBench(torch, tdg, synth)
