@@ -73,6 +73,7 @@ def _L():
             lib.orc_ll_unpack.restype = ctypes.c_int64
             lib.orc_ll_unpack.argtypes = [vp, i64, ctypes.c_uint32, vp]
             lib.orc_swizzle_order.argtypes = [i32, i64, i64, i64, vp, vp]
+            lib.orc_allreduce.argtypes = [i32, i64, vp, vp]
             _lib = lib
     return _lib
 
@@ -243,3 +244,14 @@ def swizzle_order(rank: int, tiles_per_pe: int, total_m: int, n_tiles: int):
     pn = np.empty(total_m * n_tiles, np.int64)
     _L().orc_swizzle_order(rank, tiles_per_pe, total_m, n_tiles, _p(pm), _p(pn))
     return pm, pn
+
+
+# ------------------------------------------------------------- AllReduce ----
+def allreduce(xs):
+    """Element-wise sum (float64) of W float32 buffers of equal length."""
+    xs = [np.ascontiguousarray(x, np.float32).reshape(-1) for x in xs]
+    n = xs[0].size
+    assert all(x.size == n for x in xs)
+    out = np.empty(n, np.float64)
+    _L().orc_allreduce(len(xs), n, _ptr_array(xs), _p(out))
+    return out

@@ -389,3 +389,27 @@ ORC_EXPORT void orc_swizzle_order(int rank, int64_t tiles_per_pe,
         pid_n_out[id] = pid_n;
     }
 }
+
+/* ------------------------------------------------------------------------ */
+/* AllReduce                                                                 */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * "Triton-distributed 语义", 示例：带重叠的环形 AllReduce: after the ring's
+ * reduce-scatter and all-gather phases every rank holds the element-wise sum
+ * of all ranks' buffers.  The oracle is that sum:
+ *
+ *   out[i] = sum_{r=0}^{W-1} x_r[i]      (double precision, rank order)
+ *
+ * x[r] points to rank r's buffer of n float32 values; out has n doubles.
+ */
+ORC_EXPORT void orc_allreduce(int W, int64_t n, const float *const *x, double *out)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i) {
+        double s = 0.0;
+        for (int r = 0; r < W; ++r)
+            s += (double)x[r][i];
+        out[i] = s;
+    }
+}

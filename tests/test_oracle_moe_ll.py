@@ -173,3 +173,26 @@ def test_swizzle_is_permutation_starting_local(W, tpp, n):
         # each rank starts on its own (local) rows
         first = pm[: tpp * n]
         assert set(first.tolist()) == set(range(rank * tpp, (rank + 1) * tpp))
+
+
+# ------------------------------------------------------------ AllReduce ----
+def test_allreduce_closed_form_and_brute_force():
+    # closed form: x_r = r * 1 + i  ->  sum = W(W-1)/2 + W*i
+    W, n = 5, 37
+    xs = [np.arange(n, dtype=np.float32) + r for r in range(W)]
+    out = oracle.allreduce(xs)
+    assert np.array_equal(out, W * np.arange(n) + W * (W - 1) / 2)
+    # brute force in pure Python on random floats
+    g = np.random.default_rng(3)
+    xs = [g.standard_normal(11).astype(np.float32) for _ in range(4)]
+    want = [sum(float(x[i]) for x in xs) for i in range(11)]
+    assert np.array_equal(oracle.allreduce(xs), np.array(want))
+
+
+def test_allreduce_rank_permutation_invariance_and_single_rank():
+    g = np.random.default_rng(4)
+    xs = [g.integers(-1000, 1000, 64).astype(np.float32) for _ in range(6)]
+    a = oracle.allreduce(xs)
+    b = oracle.allreduce(xs[::-1])
+    assert np.array_equal(a, b)          # integers: exact in any order
+    assert np.array_equal(oracle.allreduce(xs[:1]), xs[0].astype(np.float64))
