@@ -517,6 +517,24 @@ def main():
             raise RuntimeError(f"device fault in MoE: {st}")
         del moe
         torch.cuda.empty_cache()
+        # ring AllReduce over the 8 logical ranks, 32 Mi float32 per rank
+        W, cnt = 8, 32 * 1024 * 1024
+        rsym = tdg.Symm(W, _align(cnt * 4 + tdg.allreduce_recv_bytes(W, cnt) + 2048), 65536)
+        for r in range(W):
+            rsym.view(r, 0, (cnt,), torch.float32).normal_()
+        recv_off = _align(cnt * 4)
+        aparts = timed_steps(torch, [lambda: tdg.allreduce(rsym, cnt, 0, recv_off)], args.steps, args.warmup, flush)
+        a_ms = statistics.mean(aparts[0])
+        st = rsym.status()
+        if st["code"] != 0:
+            raise RuntimeError(f"device fault in the ring AllReduce: {st}")
+        hbm = (5 * W - 4) * cnt * 4   # bytes the ring reads and writes in HBM
+        extras["ring_allreduce"] = {
+            "workload": "8 logical ranks x 32 Mi float32, ring reduce-scatter + all-gather, 64 Ki-element tiles",
+            "ms": a_ms, "hbm_bytes": hbm, "gbs": hbm / a_ms / 1e6, "frac_of_hbm": hbm / a_ms / 1e6 / pk["hbm"],
+            "busbw_gbs": 2 * (W - 1) / W * cnt * 4 / a_ms / 1e6}
+        del rsym
+        torch.cuda.empty_cache()
         if rank == 0 and not args.no_cpu:
             r, s, desc = cpu_oracle_rate()
             cpu = {"value": r, "unit": "TFLOP/s", "cores": omp_threads(), "kind": "oracle", "sample": desc,

@@ -123,6 +123,7 @@ typedef struct {
 #define TDG_WHERE_PIPE 2       /* an intra-CTA pipeline barrier ran out of time */
 #define TDG_WHERE_LL 3         /* LL receiver waiting on a data+flag word     */
 #define TDG_WHERE_MOE_EXPERT 4 /* an expert id outside [0, E)                 */
+#define TDG_WHERE_RING 5       /* ring AllReduce waiting on a tile of a step   */
 
 /*
  * Copy the status block to *out (may be NULL) after synchronising `stream`,
@@ -214,6 +215,39 @@ typedef struct {
 TDG_API size_t tdg_gemm_rs_stage_bytes(int world, int64_t M, int64_t N);
 
 TDG_API int tdg_gemm_rs(tdg_symm *h, const tdg_gemm_rs_args *args, void *stream);
+
+/* ---- ring AllReduce --------------------------------------------------------- */
+/*
+ * Tile-centric ring AllReduce over the W logical ranks ("Triton-distributed
+ * 语义", 示例：带重叠的环形 AllReduce): a reduce-scatter ring (W-1 steps) followed
+ * by an all-gather ring (W-1 steps); every tile of every step carries its own
+ * signal, so a tile is reduced or forwarded as soon as it arrives.
+ *
+ * x_r (count float32) at region(r) + x_off is reduced in place: afterwards
+ * every rank holds sum_r x_r.  Each buffer is split into W chunks of count/W;
+ * at reduce-scatter step s rank r sends chunk (r - s) mod W to rank r+1, which
+ * adds its own copy (local + incoming, float32) -- the textbook ring, since
+ * the tile indices printed in the pages' example are inconsistent -- and at
+ * all-gather step s rank r forwards chunk (r + 1 - s) mod W.
+ * recv_r at region(r) + recv_off holds W-1 chunk-sized float32 slots
+ * (tdg_allreduce_recv_bytes).  Signals: rank r's flag words
+ * [0, (2W-2) * tiles_per_chunk).
+ * Requirements: count % (4 * world) == 0, tile_elems % 4 == 0 (0 = default),
+ * offsets 16-byte aligned, (2W-2) * ceil(count/W / tile_elems) <=
+ * signals_per_rank.  count == 0 or world == 1 is a no-op.
+ */
+typedef struct {
+    int world;
+    int64_t count;       /* float32 elements per rank                          */
+    size_t x_off;        /* data, reduced in place                             */
+    size_t recv_off;     /* W-1 receive slots of count/W float32               */
+    int64_t tile_elems;  /* elements per signalled tile (0 = 65536)            */
+    int ctas_per_rank;   /* 0 = default                                        */
+    uint64_t timeout_ns; /* bound of every device wait; 0 = 2 s                */
+} tdg_allreduce_args;
+
+TDG_API size_t tdg_allreduce_recv_bytes(int world, int64_t count);
+TDG_API int tdg_allreduce(tdg_symm *h, const tdg_allreduce_args *args, void *stream);
 
 /* ---- MoE dispatch / combine ------------------------------------------------ */
 /*

@@ -87,6 +87,9 @@ def test_host_size_helpers(L):
     # MoE workspace: two int32 tables of W x ceil(T/64) x E
     assert L.tdg_moe_workspace_bytes(8, 4096, 256) == 2 * 8 * 64 * 256 * 4
     assert L.tdg_moe_workspace_bytes(2, 65, 4) == 2 * 2 * 2 * 4 * 4
+    # ring AllReduce: W-1 receive slots of count/W float32
+    assert L.tdg_allreduce_recv_bytes(8, 1 << 20) == 7 * (1 << 17) * 4
+    assert L.tdg_allreduce_recv_bytes(1, 1024) == 0
 
 
 def test_strerror_and_invalid_handles(L):
@@ -99,6 +102,7 @@ def test_strerror_and_invalid_handles(L):
     assert L.tdg_ag_gemm(None, None, None, None) == tdg.TDG_ERR_INVALID
     assert L.tdg_gemm_rs(None, None, None) == tdg.TDG_ERR_INVALID
     assert L.tdg_moe_dispatch_combine(None, None, None) == tdg.TDG_ERR_INVALID
+    assert L.tdg_allreduce(None, None, None) == tdg.TDG_ERR_INVALID
     h = ctypes.c_void_p()
     # misaligned base / bad world are rejected before any CUDA call
     assert L.tdg_symm_alloc(ctypes.c_void_p(1024 + 16), 1 << 20, 2, 4096, 16,

@@ -27,7 +27,7 @@ MODE_SM, MODE_CE, MODE_LL, MODE_SERIAL = 0, 1, 2, 3
 MODES = {"sm": MODE_SM, "ce": MODE_CE, "ll": MODE_LL, "serial": MODE_SERIAL}
 B_KN, B_NK = 0, 1
 MOE_ROUTE, MOE_DISPATCH, MOE_COMBINE, MOE_ALL = 1, 2, 4, 7
-WHERE = {1: "ag_flag", 2: "pipe", 3: "ll", 4: "moe_expert"}
+WHERE = {1: "ag_flag", 2: "pipe", 3: "ll", 4: "moe_expert", 5: "ring"}
 
 # every symbol include/tdg.h declares
 EXPORTS = [
@@ -35,6 +35,7 @@ EXPORTS = [
     "tdg_symm_flags", "tdg_symm_counters", "tdg_symm_epoch", "tdg_status", "tdg_strerror",
     "tdg_device_info", "tdg_ag_gemm", "tdg_gemm_rs_stage_bytes", "tdg_gemm_rs",
     "tdg_moe_workspace_bytes", "tdg_moe_dispatch_combine", "tdg_moe_dispatch_combine_noalloc",
+    "tdg_allreduce_recv_bytes", "tdg_allreduce",
 ]
 MOE_STATIC_WORKSPACE_BYTES = 2 * 1024 * 1024
 
@@ -66,6 +67,11 @@ class MoeArgs(ctypes.Structure):
                 ("out_off", _sz), ("recv", _vp), ("y", _vp), ("counts", _vp), ("base", _vp),
                 ("slot", _vp), ("row_src", _vp), ("row_tok", _vp), ("row_k", _vp),
                 ("workspace", _vp), ("workspace_bytes", _sz), ("phases", ctypes.c_int)]
+
+
+class AllReduceArgs(ctypes.Structure):
+    _fields_ = [("world", ctypes.c_int), ("count", _i64), ("x_off", _sz), ("recv_off", _sz),
+                ("tile_elems", _i64), ("ctas_per_rank", ctypes.c_int), ("timeout_ns", _u64)]
 
 
 class TdgError(RuntimeError):
@@ -117,6 +123,10 @@ def lib():
             L.tdg_moe_workspace_bytes.argtypes = [ctypes.c_int, _i64, ctypes.c_int]
             L.tdg_moe_dispatch_combine.restype = ctypes.c_int
             L.tdg_moe_dispatch_combine.argtypes = [_vp, ctypes.POINTER(MoeArgs), _vp]
+            L.tdg_allreduce_recv_bytes.restype = _sz
+            L.tdg_allreduce_recv_bytes.argtypes = [ctypes.c_int, _i64]
+            L.tdg_allreduce.restype = ctypes.c_int
+            L.tdg_allreduce.argtypes = [_vp, ctypes.POINTER(AllReduceArgs), _vp]
             L.tdg_moe_dispatch_combine_noalloc.restype = ctypes.c_int
             L.tdg_moe_dispatch_combine_noalloc.argtypes = [_vp, ctypes.POINTER(MoeArgs), _vp]
             _lib = L
@@ -238,6 +248,17 @@ def gemm_rs(symm: Symm, M: int, K: int, N: int, a_off: int, b_off: int, stage_of
                    stage_off=stage_off, out_off=out_off, b_layout=b_layout,
                    mode=MODES[mode], timeout_ns=timeout_ns)
     _check(lib().tdg_gemm_rs(symm.h, ctypes.byref(a), _stream(stream)), "tdg_gemm_rs")
+
+
+def allreduce_recv_bytes(world: int, count: int) -> int:
+    return lib().tdg_allreduce_recv_bytes(world, count)
+
+
+def allreduce(symm: Symm, count: int, x_off: int, recv_off: int, tile_elems=0, ctas_per_rank=0,
+              timeout_ns=0, stream=None):
+    a = AllReduceArgs(world=symm.world, count=count, x_off=x_off, recv_off=recv_off,
+                      tile_elems=tile_elems, ctas_per_rank=ctas_per_rank, timeout_ns=timeout_ns)
+    _check(lib().tdg_allreduce(symm.h, ctypes.byref(a), _stream(stream)), "tdg_allreduce")
 
 
 def moe_workspace_bytes(world: int, T: int, E: int) -> int:
