@@ -69,7 +69,46 @@ __device__ __forceinline__ void ring_notify(const RingParams &p, int r, int step
     }
 }
 
-__global__ void __launch_bounds__(256) ring_allreduce_kernel(const __grid_constant__ RingParams p)
+// Element-wise body of one tile: UNROLL float4 loads of each operand are in
+// flight before any add or store (the loop is bound by memory latency).
+constexpr int UNROLL = 4;
+
+template <int KIND> // 0: out = a (+ b if has_b); 1: a = out2 = a + b; 2: out = a
+__device__ __forceinline__ void ring_tile(const float4 *a, const float4 *b, float4 *out, float4 *out2,
+                                          int64_t nv, bool has_b)
+{
+    const int64_t stride = (int64_t)blockDim.x * UNROLL;
+    for (int64_t i0 = threadIdx.x; i0 < nv; i0 += stride) {
+        float4 va[UNROLL], vb[UNROLL];
+#pragma unroll
+        for (int j = 0; j < UNROLL; ++j) {
+            const int64_t i = i0 + (int64_t)j * blockDim.x;
+            if (i < nv) {
+                va[j] = __ldcg(a + i);
+                if (has_b)
+                    vb[j] = __ldcg(b + i);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < UNROLL; ++j) {
+            const int64_t i = i0 + (int64_t)j * blockDim.x;
+            if (i < nv) {
+                float4 v = va[j];
+                if (has_b) { // local + incoming
+                    v.x += vb[j].x;
+                    v.y += vb[j].y;
+                    v.z += vb[j].z;
+                    v.w += vb[j].w;
+                }
+                if (KIND == 1)
+                    __stcg(out2 + i, v);
+                __stcg(out + i, v);
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(256, 2) ring_allreduce_kernel(const __grid_constant__ RingParams p)
 {
     const int r = blockIdx.x / p.G, g = blockIdx.x % p.G;
     const int W = p.W, nxt = (r + 1) % W;
@@ -83,42 +122,18 @@ __global__ void __launch_bounds__(256) ring_allreduce_kernel(const __grid_consta
                 ring_wait(p, r, s - 1, t, gave_up);
             if (s <= W - 2) { // reduce-scatter push
                 const int c = ((r - s) % W + W) % W;
-                const float4 *xl = reinterpret_cast<const float4 *>(ring_x(p, r, c) + e0);
-                const float4 *in = reinterpret_cast<const float4 *>(ring_recv(p, r, s - 1) + e0);
-                float4 *out = reinterpret_cast<float4 *>(ring_recv(p, nxt, s) + e0);
-                for (int64_t i = threadIdx.x; i < nv; i += blockDim.x) {
-                    float4 v = __ldcg(xl + i);
-                    if (s > 0) {
-                        const float4 u = __ldcg(in + i);
-                        v.x += u.x;
-                        v.y += u.y;
-                        v.z += u.z;
-                        v.w += u.w;
-                    }
-                    __stcg(out + i, v);
-                }
+                ring_tile<0>(reinterpret_cast<const float4 *>(ring_x(p, r, c) + e0),
+                             reinterpret_cast<const float4 *>(ring_recv(p, r, s - 1) + e0),
+                             reinterpret_cast<float4 *>(ring_recv(p, nxt, s) + e0), nullptr, nv, s > 0);
             } else if (s == W - 1) { // final reduction of chunk r+1, then the first all-gather push
                 const int f = nxt;
                 float4 *xl = reinterpret_cast<float4 *>(ring_x(p, r, f) + e0);
-                const float4 *in = reinterpret_cast<const float4 *>(ring_recv(p, r, W - 2) + e0);
-                float4 *out = reinterpret_cast<float4 *>(ring_x(p, nxt, f) + e0);
-                for (int64_t i = threadIdx.x; i < nv; i += blockDim.x) {
-                    float4 v = __ldcg(xl + i);
-                    const float4 u = __ldcg(in + i);
-                    v.x += u.x;
-                    v.y += u.y;
-                    v.z += u.z;
-                    v.w += u.w;
-                    __stcg(xl + i, v);
-                    __stcg(out + i, v);
-                }
+                ring_tile<1>(xl, reinterpret_cast<const float4 *>(ring_recv(p, r, W - 2) + e0),
+                             reinterpret_cast<float4 *>(ring_x(p, nxt, f) + e0), xl, nv, true);
             } else { // all-gather forward of the chunk that arrived at step s-1
-                const int sp = s - (W - 1);
-                const int c = ((r + 1 - sp) % W + W) % W;
-                const float4 *xl = reinterpret_cast<const float4 *>(ring_x(p, r, c) + e0);
-                float4 *out = reinterpret_cast<float4 *>(ring_x(p, nxt, c) + e0);
-                for (int64_t i = threadIdx.x; i < nv; i += blockDim.x)
-                    __stcg(out + i, __ldcg(xl + i));
+                const int c = ((r + 1 - (s - (W - 1))) % W + W) % W;
+                ring_tile<2>(reinterpret_cast<const float4 *>(ring_x(p, r, c) + e0), nullptr,
+                             reinterpret_cast<float4 *>(ring_x(p, nxt, c) + e0), nullptr, nv, false);
             }
             ring_notify(p, nxt, s, t);
         }
@@ -166,7 +181,8 @@ extern "C" int tdg_allreduce(tdg_symm *h, const tdg_allreduce_args *a, void *str
     const void *fn = reinterpret_cast<const void *>(&ring_allreduce_kernel);
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, 256, 0) != cudaSuccess || per_sm < 1)
         return TDG_ERR_CUDA;
-    int G = a->ctas_per_rank > 0 ? a->ctas_per_rank : (2 * h->sm_count) / W;
+    // default: as many CTAs per rank as can all be resident (every wait relies on it)
+    int G = a->ctas_per_rank > 0 ? a->ctas_per_rank : (per_sm * h->sm_count) / W;
     if (G < 1)
         G = 1;
     if ((int64_t)G > tiles)
