@@ -67,6 +67,23 @@ def test_integer_exact_larger_and_swizzle_invariance(pair, monkeypatch):
         assert np.array_equal(o, C16)
 
 
+@pytest.mark.parametrize("pair", ["1", "0"])
+@pytest.mark.parametrize("N", [2440, 2432])
+def test_split_tail_wave_bit_exact(N, pair, monkeypatch):
+    # 2048 x N: 80 pair tiles (160 single tiles) over 76 pairs (152 CTAs), so
+    # the last wave's few tiles are cut into 128-column halves; with N = 2440
+    # the last n tile is 136 wide (halves of 128 and 8), with N = 2432 it is
+    # 128 wide (its second half is empty and skipped by every role)
+    monkeypatch.setenv("TDG_PAIR", pair)
+    monkeypatch.setenv("TDG_SPLIT_TAIL", "1")
+    inp = synth.ag_inputs(8, 256, 64, N, "int2", seed=N)
+    _, C16 = oracle.ag_gemm(inp.shards, inp.B)
+    case = AGCase(inp)
+    for mode in ("ce", "sm", "serial"):
+        got, _ = case.run(rank=5, mode=mode)
+        assert np.array_equal(got, C16), mode
+
+
 def test_timeout_reported_then_next_call_succeeds():
     # fault injection on the host side: producers skip one notify; the consumer's
     # bounded wait must run out, report TIMEOUT with the signal index, and the

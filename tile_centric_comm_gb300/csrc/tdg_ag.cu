@@ -61,6 +61,7 @@ struct AgParams {
     uint32_t *flags_w;
     uint64_t skip_mask;
     int pair; // 1: CTA pairs (cta_group::2) with 256-row tiles
+    int split; // tiles of the last, partial wave split in two 128-column halves
     // LL mode: producer CTAs [0, n_send) send, [n_send, n_prod) receive
     int ll;
     int n_send;
@@ -71,20 +72,34 @@ template <int BMN> struct AgPolicy {
     using Params = AgParams;
     static constexpr int B_MN = BMN;
 
-    __device__ static int64_t num_items(const Params &p) { return (int64_t)p.m_tiles * p.n_tiles; }
+    // With a persistent grid of U scheduling units (CTAs or pairs) and T tiles,
+    // the last wave holds only T mod U tiles.  Optionally, when twice that still
+    // fits in a wave, those `split` tiles are cut into two 128-column halves.
+    __device__ static int64_t num_items(const Params &p) { return (int64_t)p.m_tiles * p.n_tiles + p.split; }
 
     // tiles are tile_m = 128 (one CTA) or 256 (CTA pair) rows; `half` picks this
     // CTA's 128-row slice
     __device__ static void tile(const Params &p, int64_t item, TileInfo &t, int half)
     {
         const int tm = p.pair ? 2 * gm::BM : gm::BM;
-        const int pm0 = (int)(item / p.n_tiles);
-        t.pn = (int)(item % p.n_tiles);
+        const int64_t full = (int64_t)p.m_tiles * p.n_tiles - p.split;
+        int64_t tid = item;
+        int nhalf = -1; // -1: whole tile; 0 / 1: a half of a split tail tile
+        if (item >= full) {
+            tid = full + (item - full) / 2;
+            nhalf = (int)((item - full) & 1);
+        }
+        const int pm0 = (int)(tid / p.n_tiles);
+        t.pn = (int)(tid % p.n_tiles);
         // the pages' swizzle: pid_m = (pid_m + rank * tiles_per_pe) % total
         const int pm = (pm0 + p.swz) % p.m_tiles;
         t.m0 = pm * tm + half * gm::BM;
         t.n0 = t.pn * gm::BN;
         t.n_valid = (int)min((int64_t)gm::BN, p.N - t.n0);
+        if (nhalf >= 0) {
+            t.n0 += nhalf * (gm::BN / 2);
+            t.n_valid = (int)min((int64_t)gm::BN / 2, p.N - t.n0); // <= 0: null item
+        }
         const int q = p.pair ? 32 : 16;
         t.n_mma = (t.n_valid + q - 1) / q * q;
         if (p.local_inplace && pm >= p.local_lo && pm < p.local_hi) {
@@ -381,7 +396,17 @@ int launch_ag(const AgParams &p, int b_layout, int grid, bool coop, cudaStream_t
         return rc;
     if (grid < 1 || grid < p.n_prod) // a copy-only launch has no consumers
         return TDG_ERR_UNSUPPORTED;
-    void *args[] = {const_cast<AgParams *>(&p)};
+    AgParams q = p;
+    const int64_t units = p.pair ? (grid - p.n_prod) / 2 : grid - p.n_prod;
+    const int64_t T = (int64_t)p.m_tiles * p.n_tiles;
+    q.split = 0;
+    // opt-in (TDG_SPLIT_TAIL=1): measured slower at the Qwen-32B up-projection
+    // shape, where the half-width tiles move more operand bytes per FLOP and the
+    // tail tiles wait on the shard that arrives last anyway
+    const char *st = getenv("TDG_SPLIT_TAIL");
+    if (st && st[0] == '1' && units > 0 && T > units && (T % units) > 0 && 2 * (T % units) <= units)
+        q.split = (int)(T % units);
+    void *args[] = {&q};
     cudaError_t e = launch(fn, dim3(grid), dim3(gm::NUM_THREADS), gm::SMEM_BYTES, s, args, coop,
                            p.pair ? 2 : 1);
     if (e != cudaSuccess && coop && p.pair) {

@@ -97,6 +97,7 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p)
 //   static constexpr int B_MN;                                   // 1: B is K x N
 //   __device__ static int64_t num_items(const Params&);
 //   __device__ static void tile(const Params&, int64_t item, TileInfo&, int half);
+//       (an item with n_valid <= 0 is a null item: every role skips it)
 //   __device__ static void before_a(const Params&, const TileInfo&, bool &gave_up);  // loader thread
 //   template <int PAIR> __device__ static void load_a(const Params&, const TileInfo&, void *dst,
 //                                                     uint32_t bar, int kb);
@@ -164,6 +165,8 @@ __device__ void gemm_consumer(const typename P::Params &p, uint8_t *smem, int un
             for (int64_t it = unit; it < items && !ps->abort; it += nunits) {
                 TileInfo ti;
                 P::tile(p, it, ti, half);
+                if (ti.n_valid <= 0)
+                    continue; // a null item (an empty half of a split tail tile)
                 P::before_a(p, ti, gave_up);
                 const int cols = PAIR ? ti.n_mma / 2 : ti.n_mma;
                 const int col0 = ti.n0 + (PAIR ? half * cols : 0);
@@ -200,6 +203,8 @@ __device__ void gemm_consumer(const typename P::Params &p, uint8_t *smem, int un
             for (int64_t it = unit; it < items && !ps->abort; it += nunits) {
                 TileInfo ti;
                 P::tile(p, it, ti, half);
+                if (ti.n_valid <= 0)
+                    continue;
                 const uint32_t idesc = idesc_bf16(S::TILE_M, ti.n_mma, P::B_MN);
                 if (!mbar_wait(&ps->tempty[acc], acc_phase ^ 1u, tmo)) {
                     report_fault(p.status, TDG_ERR_TIMEOUT, TDG_WHERE_PIPE, 1, p.epoch);
@@ -273,6 +278,8 @@ __device__ void gemm_consumer(const typename P::Params &p, uint8_t *smem, int un
         for (int64_t it = unit; it < items; it += nunits) {
             TileInfo ti;
             P::tile(p, it, ti, half);
+            if (ti.n_valid <= 0)
+                continue;
             bool ok = mbar_wait(&ps->tfull[acc], acc_phase, tmo);
             if (!ok || ps->abort) {
                 if (lane == 0 && !ok)
