@@ -178,6 +178,9 @@ typedef struct {
     size_t ll_off;       /* LL mode: LL buffer (M*K*4 bytes) in region(rank) */
     uint64_t test_skip_notify; /* tests only: producers skip the notify of
                                   signal groups whose bit (g % 64) is set   */
+    int source_order;    /* 0: one source at a time, rank+1, rank+2, ... (the
+                            pages' NVSwitch swizzle); 1: all sources at once,
+                            round robin over sources (their full-mesh order) */
 } tdg_ag_gemm_args;
 
 TDG_API int tdg_ag_gemm(tdg_symm *h, const tdg_ag_gemm_args *args, void *stream,
@@ -209,6 +212,8 @@ typedef struct {
     int b_layout;
     int mode;            /* TDG_MODE_SM (overlapped) or TDG_MODE_SERIAL      */
     uint64_t timeout_ns; /* bound of every device wait; 0 = 2 s             */
+    int owner_block;     /* tile order: owners per block, each rank's tiles of
+                            a block back to back (0 = 2; must divide world)  */
 } tdg_gemm_rs_args;
 
 /* Bytes of one owner's staging area for the given shape (all W partials). */

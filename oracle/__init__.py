@@ -74,6 +74,8 @@ def _L():
             lib.orc_ll_unpack.argtypes = [vp, i64, ctypes.c_uint32, vp]
             lib.orc_swizzle_order.argtypes = [i32, i64, i64, i64, vp, vp]
             lib.orc_allreduce.argtypes = [i32, i64, vp, vp]
+            lib.orc_attention_decode.argtypes = [i64, i64, i64, i64, i64, vp, vp, vp,
+                                                 ctypes.c_double, vp]
             _lib = lib
     return _lib
 
@@ -254,4 +256,20 @@ def allreduce(xs):
     assert all(x.size == n for x in xs)
     out = np.empty(n, np.float64)
     _L().orc_allreduce(len(xs), n, _ptr_array(xs), _p(out))
+    return out
+
+
+# ------------------------------------------------------ decode attention ----
+def attention_decode(q, k, v, scale=None):
+    """Softmax attention of one query token per (batch, head) over the whole
+    KV cache.  q: (B, Hq, D); k, v: (B, Hkv, S, D) bf16 bits.  Returns float64
+    (B, Hq, D)."""
+    q, k, v = _u16(q), _u16(k), _u16(v)
+    B, Hq, D = q.shape
+    _, Hkv, S, _ = k.shape
+    assert Hq % Hkv == 0 and k.shape == v.shape == (B, Hkv, S, D)
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    out = np.empty((B, Hq, D), np.float64)
+    _L().orc_attention_decode(B, Hq, Hkv, D, S, _p(q), _p(k), _p(v), float(scale), _p(out))
     return out

@@ -413,3 +413,55 @@ ORC_EXPORT void orc_allreduce(int W, int64_t n, const float *const *x, double *o
         out[i] = s;
     }
 }
+
+/* ------------------------------------------------------------------------ */
+/* Decode attention (the distributed flash-decoding workload)                */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Paper summary (hyper.ai, arXiv 2504.19442), section 实验: distributed flash
+ * decoding over long KV caches; "Triton-distributed完全指南", §5.2 (Fig. 5):
+ * flash-decode scaling over GPU count and KV length.  Splitting the KV cache
+ * over ranks and merging the partial results changes only the rounding, so the
+ * oracle is plain softmax attention of one query token over the whole cache:
+ *
+ *   s_t = scale * sum_d q[b][h][d] * k[b][g][t][d],   g = h / (Hq / Hkv)
+ *   out[b][h][d] = sum_t exp(s_t - max_t s) * v[b][g][t][d] / sum_t exp(s_t - max_t s)
+ *
+ * q: B x Hq x D, k and v: B x Hkv x S x D (bf16 bits); out64: B x Hq x D.
+ */
+ORC_EXPORT void orc_attention_decode(int64_t B, int64_t Hq, int64_t Hkv, int64_t D, int64_t S,
+                                     const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                                     double scale, double *out64)
+{
+    const int64_t G = Hq / Hkv;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t bh = 0; bh < B * Hq; ++bh) {
+        const int64_t b = bh / Hq, h = bh % Hq, g = h / G;
+        const uint16_t *qq = q + (b * Hq + h) * D;
+        const uint16_t *kk = k + (b * Hkv + g) * S * D;
+        const uint16_t *vv = v + (b * Hkv + g) * S * D;
+        double *s = (double *)malloc(sizeof(double) * (size_t)(S > 0 ? S : 1));
+        double mx = -INFINITY;
+        for (int64_t t = 0; t < S; ++t) {
+            double a = 0.0;
+            for (int64_t d = 0; d < D; ++d)
+                a += orc_bf16_to_f64(qq[d]) * orc_bf16_to_f64(kk[t * D + d]);
+            s[t] = scale * a;
+            if (s[t] > mx)
+                mx = s[t];
+        }
+        double den = 0.0;
+        for (int64_t t = 0; t < S; ++t) {
+            s[t] = exp(s[t] - mx);
+            den += s[t];
+        }
+        for (int64_t d = 0; d < D; ++d) {
+            double num = 0.0;
+            for (int64_t t = 0; t < S; ++t)
+                num += s[t] * orc_bf16_to_f64(vv[t * D + d]);
+            out64[bh * D + d] = num / den;
+        }
+        free(s);
+    }
+}

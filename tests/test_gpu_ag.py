@@ -114,6 +114,19 @@ def test_ll_mode_bit_exact_and_words_match_the_codec():
         assert np.array_equal(case.ll_words(rank), oracle.ll_pack(payload, epoch))
 
 
+@pytest.mark.parametrize("mode", ["sm", "ce", "ll", "serial"])
+def test_all_sources_at_once_order_bit_exact(mode):
+    # the full-mesh source order (round robin over sources) gives the same bits
+    inp = synth.ag_inputs(4, 96, 200, 136, "int2", seed=21)
+    _, C16 = oracle.ag_gemm(inp.shards, inp.B)
+    case = AGCase(inp, ll=True)
+    for rank in (0, 3):
+        got, _ = case.run(rank=rank, mode=mode, source_order=1, ll_off=case.ll_off,
+                          signal_rows=32)
+        assert np.array_equal(got, C16), (mode, rank)
+        _gathered_ok(case, rank)
+
+
 def test_ll_mode_float_parity():
     inp = synth.ag_inputs(4, 128, 256, 264, "normal", seed=12)
     C64, _ = oracle.ag_gemm(inp.shards, inp.B)

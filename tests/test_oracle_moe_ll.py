@@ -196,3 +196,70 @@ def test_allreduce_rank_permutation_invariance_and_single_rank():
     b = oracle.allreduce(xs[::-1])
     assert np.array_equal(a, b)          # integers: exact in any order
     assert np.array_equal(oracle.allreduce(xs[:1]), xs[0].astype(np.float64))
+
+
+# ----------------------------------------------------- decode attention ----
+def _bf(x):
+    return synth.f32_to_bf16_bits(np.asarray(x, np.float32))
+
+
+def test_attention_brute_force():
+    g = np.random.default_rng(5)
+    B, Hq, Hkv, S, D = 2, 4, 2, 7, 8
+    q = _bf(g.standard_normal((B, Hq, D)))
+    k = _bf(g.standard_normal((B, Hkv, S, D)))
+    v = _bf(g.standard_normal((B, Hkv, S, D)))
+    out = oracle.attention_decode(q, k, v)
+    qf, kf, vf = (oracle.bf16_to_f64(x) for x in (q, k, v))
+    for b in range(B):
+        for h in range(Hq):
+            kv = h // (Hq // Hkv)
+            s = [sum(qf[b, h, d] * kf[b, kv, t, d] for d in range(D)) / np.sqrt(D) for t in range(S)]
+            m = max(s)
+            e = [np.exp(x - m) for x in s]
+            want = [sum(e[t] * vf[b, kv, t, d] for t in range(S)) / sum(e) for d in range(D)]
+            np.testing.assert_allclose(out[b, h], want, rtol=1e-12, atol=1e-14)
+
+
+def test_attention_closed_forms():
+    g = np.random.default_rng(6)
+    B, Hq, Hkv, S, D = 1, 2, 1, 9, 16
+    q = _bf(g.standard_normal((B, Hq, D)))
+    v = _bf(g.standard_normal((B, Hkv, S, D)))
+    # identical keys: uniform weights, the output is the mean of the values
+    k = np.repeat(_bf(g.standard_normal((B, Hkv, 1, D))), S, axis=2)
+    out = oracle.attention_decode(q, k, v)
+    np.testing.assert_allclose(out[0, 0], oracle.bf16_to_f64(v)[0, 0].mean(0), rtol=1e-12)
+    # one token: the output is its value row
+    out1 = oracle.attention_decode(q, k[:, :, :1], v[:, :, :1])
+    np.testing.assert_array_equal(out1[0, 1], oracle.bf16_to_f64(v)[0, 0, 0])
+    # one key far above the rest takes all the weight
+    k2 = np.zeros((B, Hkv, S, D), np.float32)
+    qf = oracle.bf16_to_f64(q)[0, 0]
+    k2[0, 0, 4] = np.sign(qf) * 8.0
+    out2 = oracle.attention_decode(q[:, :1], _bf(k2), v)
+    np.testing.assert_allclose(out2[0, 0], oracle.bf16_to_f64(v)[0, 0, 4], rtol=1e-9, atol=1e-9)
+
+
+def test_attention_split_merge_identity():
+    # splitting the cache in two and merging by log-sum-exp gives the same
+    # result -- the identity the distributed kernel relies on (checked on the
+    # oracle with half caches and a pure-numpy merge)
+    g = np.random.default_rng(7)
+    B, Hq, Hkv, S, D = 1, 2, 1, 12, 8
+    q = _bf(g.standard_normal((B, Hq, D)))
+    k = _bf(g.standard_normal((B, Hkv, S, D)))
+    v = _bf(g.standard_normal((B, Hkv, S, D)))
+    full = oracle.attention_decode(q, k, v)
+    qf, kf = oracle.bf16_to_f64(q), oracle.bf16_to_f64(k)
+    parts = []
+    for lo, hi in ((0, 5), (5, 12)):
+        o = oracle.attention_decode(q, k[:, :, lo:hi], v[:, :, lo:hi])
+        s = np.einsum("bhd,bgtd->bhgt", qf, kf[:, :, lo:hi])[:, :, 0] / np.sqrt(D)
+        m = s.max(-1)
+        l = np.exp(s - m[..., None]).sum(-1)
+        parts.append((o, m, l))
+    M = np.maximum(parts[0][1], parts[1][1])
+    w = [p[2] * np.exp(p[1] - M) for p in parts]
+    merged = (parts[0][0] * w[0][..., None] + parts[1][0] * w[1][..., None]) / (w[0] + w[1])[..., None]
+    np.testing.assert_allclose(merged, full, rtol=1e-12, atol=1e-14)

@@ -1,0 +1,98 @@
+"""Distributed autotuner for the tile-centric kernels.
+
+The Triton-distributed paper summary (hyper.ai, arXiv 2504.19442, section 方法)
+describes an autotuner made for distributed kernels: it accounts for the
+synchronisation that launching them needs and synchronises the tuning results
+across devices, so that every device settles on the same, globally best
+configuration.  This module does that for the knobs of this library:
+
+* every candidate configuration is run through the C ABI (``run(cfg)``),
+  with warm-up, and timed with CUDA events on the launching stream;
+* under ``torch.distributed`` the per-rank times are combined with a MAX
+  all-reduce -- the job is as slow as its slowest rank -- and every rank picks
+  the candidate with the lowest combined time (ties to the earlier
+  candidate), so all ranks agree without any further message;
+* the decision is cached per (operation, shape) key.
+
+The host logic (``choose``) is separate from the timing so that it can be
+tested without a GPU.
+"""
+from __future__ import annotations
+
+import itertools
+import statistics
+from typing import Callable, Dict, List, Optional, Sequence, Tuple
+
+_cache: Dict[tuple, dict] = {}
+
+
+def choose(times: Sequence[float], group=None) -> Tuple[int, List[float]]:
+    """Index of the best candidate after combining `times` over the ranks of
+    `group` (max over ranks).  Without torch.distributed, the local times."""
+    t = [float(x) for x in times]
+    try:
+        import torch
+        import torch.distributed as dist
+        if dist.is_available() and dist.is_initialized():
+            ten = torch.tensor(t, dtype=torch.float64)
+            if dist.get_backend(group) == "nccl":
+                ten = ten.cuda()
+            dist.all_reduce(ten, op=dist.ReduceOp.MAX, group=group)
+            t = ten.cpu().tolist()
+    except ImportError:  # pragma: no cover
+        pass
+    best = min(range(len(t)), key=lambda i: (t[i], i))
+    return best, t
+
+
+def time_candidate(run: Callable[[dict], None], cfg: dict, warmup: int = 2, iters: int = 5,
+                   flush=None) -> float:
+    """Median device time (ms) of `run(cfg)` over `iters` launches."""
+    import torch
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        run(cfg)
+    ts = []
+    for _ in range(iters):
+        if flush is not None:
+            flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        run(cfg)
+        b.record(stream)
+        b.synchronize()
+        ts.append(a.elapsed_time(b))
+    return statistics.median(ts)
+
+
+def tune(key: tuple, candidates: List[dict], run: Callable[[dict], None], group=None,
+         warmup: int = 2, iters: int = 5, flush=None, use_cache: bool = True) -> Tuple[dict, List[dict]]:
+    """Time every candidate, agree on the best across ranks, cache it.
+    Returns (best config, table of {cfg, ms})."""
+    if use_cache and key in _cache:
+        return _cache[key], []
+    times = [time_candidate(run, c, warmup, iters, flush) for c in candidates]
+    best, combined = choose(times, group)
+    table = [dict(cfg=c, ms=t) for c, t in zip(candidates, combined)]
+    _cache[key] = candidates[best]
+    return candidates[best], table
+
+
+def ag_candidates(M: int, modes=("ce", "sm"), producers=(8, 16, 24), signal_rows=(0,),
+                  source_orders=(0, 1)) -> List[dict]:
+    out = []
+    for mode, so, sr in itertools.product(modes, source_orders, signal_rows):
+        if mode == "sm":
+            for pr in producers:
+                out.append(dict(mode=mode, producers=pr, signal_rows=sr, source_order=so))
+        else:
+            out.append(dict(mode=mode, producers=0, signal_rows=sr, source_order=so))
+    return out
+
+
+def rs_candidates(world: int) -> List[dict]:
+    return [dict(owner_block=ob) for ob in range(1, world + 1) if world % ob == 0]
+
+
+def clear_cache():
+    _cache.clear()

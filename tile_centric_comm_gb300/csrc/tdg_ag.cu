@@ -62,6 +62,7 @@ struct AgParams {
     uint64_t skip_mask;
     int pair; // 1: CTA pairs (cta_group::2) with 256-row tiles
     int split; // tiles of the last, partial wave split in two 128-column halves
+    int mesh;  // 1: producers take all sources at once (round robin over sources)
     // LL mode: producer CTAs [0, n_send) send, [n_send, n_prod) receive
     int ll;
     int n_send;
@@ -240,8 +241,10 @@ __device__ void ag_producer(const AgParams &p, uint8_t *smem)
     const int64_t nworkers = (int64_t)p.n_prod * PW;
     const uint64_t row_bytes = (uint64_t)p.K * 2;
     for (int64_t u = worker; u < p.n_units; u += nworkers) {
-        const int seq = (int)(u / p.units_per_shard);
-        const int64_t part = u % p.units_per_shard;
+        // one source at a time: all parts of source seq, then seq + 1, ...;
+        // all sources at once: part 0 of every source, then part 1, ...
+        const int seq = p.mesh ? (int)(u % p.W) : (int)(u / p.units_per_shard);
+        const int64_t part = p.mesh ? u / p.W : u % p.units_per_shard;
         const int shard = p.local_last ? (p.rank + 1 + seq) % p.W : (p.rank + seq) % p.W;
         const int64_t row0 = part * p.unit_rows;
         const int64_t rows = min(p.unit_rows, p.Ms - row0);
@@ -270,11 +273,24 @@ __device__ void ag_producer(const AgParams &p, uint8_t *smem)
 __device__ void ll_sender(const AgParams &p, int cta, int ncta)
 {
     const int64_t wps = p.Ms * p.K / 2; // words per shard
-    const int64_t total = wps * p.W;
+    // in the all-sources order every source's words are visited in runs of 64
+    // (the last run of a source padded), so the loop covers ceil(wps/64)*64*W
+    const int64_t total = p.mesh ? (wps + 63) / 64 * 64 * p.W : wps * p.W;
     const uint64_t hi = (uint64_t)p.epoch << 32;
     for (int64_t w = (int64_t)cta * blockDim.x + threadIdx.x; w < total; w += (int64_t)ncta * blockDim.x) {
-        const int seq = (int)(w / wps);
-        const int64_t off = w % wps;
+        // source order as for the bulk producers, in units of 64-word runs
+        int seq;
+        int64_t off;
+        if (p.mesh) {
+            const int64_t run = w / 64, in = w % 64;
+            seq = (int)(run % p.W);
+            off = (run / p.W) * 64 + in;
+            if (off >= wps)
+                continue;
+        } else {
+            seq = (int)(w / wps);
+            off = w % wps;
+        }
         const int shard = (p.rank + 1 + seq) % p.W;
         const int64_t gw = (int64_t)shard * wps + off;
         const int64_t g = (gw * 2 / p.K) / p.sig_rows;
@@ -516,6 +532,9 @@ extern "C" int tdg_ag_gemm(tdg_symm *h, const tdg_ag_gemm_args *a, void *stream,
     p.local_last = inplace ? 1 : 0;
     p.flags_w = flags;
     p.skip_mask = a->test_skip_notify;
+    if (a->source_order != 0 && a->source_order != 1)
+        return TDG_ERR_INVALID;
+    p.mesh = a->source_order;
 
     const int sms = h->sm_count;
     const int dev = h->device;
@@ -592,9 +611,11 @@ extern "C" int tdg_ag_gemm(tdg_symm *h, const tdg_ag_gemm_args *a, void *stream,
     if (e != cudaSuccess)
         rc = cuda_err(e, "ce events");
     const int64_t ups = Ms / sig_rows;
-    for (int seq = 0; seq < W && rc == TDG_OK; ++seq) {
+    for (int64_t u = 0; u < (int64_t)W * ups && rc == TDG_OK; ++u) {
+        const int seq = p.mesh ? (int)(u % W) : (int)(u / ups);
+        const int64_t part = p.mesh ? u / W : u % ups;
         const int shard = inplace ? (rank + 1 + seq) % W : (rank + seq) % W;
-        for (int64_t part = 0; part < ups && rc == TDG_OK; ++part) {
+        {
             const int64_t row0 = part * sig_rows;
             const int64_t grow = (int64_t)shard * Ms + row0;
             const uint8_t *src = h->base + (size_t)shard * h->region_bytes + a->a_off + (size_t)row0 * K * 2;

@@ -329,9 +329,9 @@ extern "C" int tdg_gemm_rs(tdg_symm *h, const tdg_gemm_rs_args *a, void *stream)
     p.order = getenv("TDG_RS_ORDER") ? atoi(getenv("TDG_RS_ORDER")) : 0;
     // two owners per block measured best at the Qwen-32B down-projection shape
     // (B_r streamed W/2 times instead of W; partials of a block stay L2-warm)
-    p.ob = getenv("TDG_RS_OB") ? atoi(getenv("TDG_RS_OB")) : 2;
-    if (p.ob < 1 || W % p.ob)
-        p.ob = W % 2 == 0 ? 2 : 1;
+    if (a->owner_block < 0 || (a->owner_block > 0 && W % a->owner_block))
+        return TDG_ERR_INVALID;
+    p.ob = a->owner_block > 0 ? a->owner_block : (W % 2 == 0 ? 2 : 1);
     p.fused_reduce = a->mode == TDG_MODE_SM ? 1 : 0;
     p.regions = h->base;
     p.region_bytes = R;

@@ -52,13 +52,13 @@ class AgGemmArgs(ctypes.Structure):
                 ("N", _i64), ("a_off", _sz), ("g_off", _sz), ("B", _vp), ("C", _vp),
                 ("b_layout", ctypes.c_int), ("mode", ctypes.c_int), ("producers", ctypes.c_int),
                 ("signal_rows", _i64), ("swizzle", ctypes.c_int), ("timeout_ns", _u64),
-                ("ll_off", _sz), ("test_skip_notify", _u64)]
+                ("ll_off", _sz), ("test_skip_notify", _u64), ("source_order", ctypes.c_int)]
 
 
 class GemmRsArgs(ctypes.Structure):
     _fields_ = [("world", ctypes.c_int), ("M", _i64), ("K", _i64), ("N", _i64), ("a_off", _sz),
                 ("b_off", _sz), ("stage_off", _sz), ("out_off", _sz), ("b_layout", ctypes.c_int),
-                ("mode", ctypes.c_int), ("timeout_ns", _u64)]
+                ("mode", ctypes.c_int), ("timeout_ns", _u64), ("owner_block", ctypes.c_int)]
 
 
 class MoeArgs(ctypes.Structure):
@@ -229,11 +229,13 @@ class Symm:
 
 def ag_gemm(symm: Symm, rank: int, Ms: int, K: int, N: int, a_off: int, g_off: int, B, C,
             mode="sm", b_layout=B_KN, producers=0, signal_rows=0, swizzle=True,
-            timeout_ns=0, ll_off=0, test_skip_notify=0, stream=None, side_stream=None):
+            timeout_ns=0, ll_off=0, test_skip_notify=0, source_order=0, stream=None,
+            side_stream=None):
     a = AgGemmArgs(world=symm.world, rank=rank, Ms=Ms, K=K, N=N, a_off=a_off, g_off=g_off,
                    B=B.data_ptr(), C=C.data_ptr(), b_layout=b_layout, mode=MODES[mode],
                    producers=producers, signal_rows=signal_rows, swizzle=1 if swizzle else 0,
-                   timeout_ns=timeout_ns, ll_off=ll_off, test_skip_notify=test_skip_notify)
+                   timeout_ns=timeout_ns, ll_off=ll_off, test_skip_notify=test_skip_notify,
+                   source_order=source_order)
     side = _vp(side_stream.cuda_stream) if side_stream is not None else _vp(None)
     _check(lib().tdg_ag_gemm(symm.h, ctypes.byref(a), _stream(stream), side), "tdg_ag_gemm")
 
@@ -243,10 +245,10 @@ def gemm_rs_stage_bytes(world: int, M: int, N: int) -> int:
 
 
 def gemm_rs(symm: Symm, M: int, K: int, N: int, a_off: int, b_off: int, stage_off: int,
-            out_off: int, mode="sm", b_layout=B_KN, timeout_ns=0, stream=None):
+            out_off: int, mode="sm", b_layout=B_KN, timeout_ns=0, owner_block=0, stream=None):
     a = GemmRsArgs(world=symm.world, M=M, K=K, N=N, a_off=a_off, b_off=b_off,
                    stage_off=stage_off, out_off=out_off, b_layout=b_layout,
-                   mode=MODES[mode], timeout_ns=timeout_ns)
+                   mode=MODES[mode], timeout_ns=timeout_ns, owner_block=owner_block)
     _check(lib().tdg_gemm_rs(symm.h, ctypes.byref(a), _stream(stream)), "tdg_gemm_rs")
 
 
