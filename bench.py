@@ -518,6 +518,7 @@ def main():
         del moe
         torch.cuda.empty_cache()
         # ring AllReduce over the 8 logical ranks, 32 Mi float32 per rank
+        torch.manual_seed(0)
         W, cnt = 8, 32 * 1024 * 1024
         rsym = tdg.Symm(W, _align(cnt * 4 + tdg.allreduce_recv_bytes(W, cnt) + 2048), 65536)
         for r in range(W):
@@ -534,6 +535,30 @@ def main():
             "ms": a_ms, "hbm_bytes": hbm, "gbs": hbm / a_ms / 1e6, "frac_of_hbm": hbm / a_ms / 1e6 / pk["hbm"],
             "busbw_gbs": 2 * (W - 1) / W * cnt * 4 / a_ms / 1e6}
         del rsym
+        torch.cuda.empty_cache()
+        # distributed flash decoding: 4 sequences x 64 heads (8 kv heads, d 128),
+        # 128 Ki cached tokens split over the 8 logical ranks
+        W, Bq, Hq, Hkv, D, S = 8, 4, 64, 8, 128, 131072
+        kvb = Bq * Hkv * (S // W) * D * 2
+        part = tdg.flash_decode_part_bytes(W, Bq, Hq, D, S)
+        fsym = tdg.Symm(W, _align(2 * _align(kvb) + part + 2048), 4096)
+        for r in range(W):
+            fsym.view(r, 0, (kvb // 2,), torch.bfloat16).normal_()
+            fsym.view(r, _align(kvb), (kvb // 2,), torch.bfloat16).normal_()
+        qf = torch.randn((Bq, Hq, D), device="cuda").to(torch.bfloat16)
+        of = torch.empty_like(qf)
+        fparts = timed_steps(torch, [lambda: tdg.flash_decode(fsym, Bq, Hq, Hkv, D, S, 0, _align(kvb),
+                                                              2 * _align(kvb), qf, of)],
+                             args.steps, args.warmup, flush)
+        f_ms = statistics.mean(fparts[0])
+        st = fsym.status()
+        if st["code"] != 0:
+            raise RuntimeError(f"device fault in flash decoding: {st}")
+        fbytes = 2 * kvb * W   # every cached K and V byte is read once
+        extras["flash_decode"] = {
+            "workload": "4 x 64 heads (8 kv heads, d 128), 128 Ki cached tokens over 8 logical ranks",
+            "ms": f_ms, "kv_bytes": fbytes, "gbs": fbytes / f_ms / 1e6, "frac_of_hbm": fbytes / f_ms / 1e6 / pk["hbm"]}
+        del fsym, qf, of
         torch.cuda.empty_cache()
         if rank == 0 and not args.no_cpu:
             r, s, desc = cpu_oracle_rate()

@@ -254,6 +254,36 @@ typedef struct {
 TDG_API size_t tdg_allreduce_recv_bytes(int world, int64_t count);
 TDG_API int tdg_allreduce(tdg_symm *h, const tdg_allreduce_args *args, void *stream);
 
+/* ---- distributed flash decoding -------------------------------------------- */
+/*
+ * Decode attention with the KV cache split over the W logical ranks (paper
+ * summary, 实验: distributed flash decoding; "Triton-distributed完全指南", §5.2).
+ * out[b][h] = softmax_t(scale * q[b][h] . k_t) v_t over all S cached tokens,
+ * kv head g = h / (Hq/Hkv).  Rank r holds tokens [r*S/W, (r+1)*S/W): K_r and
+ * V_r (B x Hkv x S/W x D bf16) at region(r) + k_off / v_off.  Every CTA
+ * reduces `chunk` tokens of one rank for one (batch, kv head) to a partial
+ * (row max, row sum, normalised output, fp32) and pushes it into region(root)
+ * + part_off; the CTA whose arrival completes the count for its (batch, kv
+ * head) merges all partials by log-sum-exp and writes out (bf16).
+ * q, out: B x Hq x D bf16 device pointers.  Counters: root's counter words
+ * [0, B*Hkv).  Requirements: D == 128, Hq % Hkv == 0, Hq/Hkv <= 16,
+ * S % world == 0, S > 0, chunk % 64 == 0 (0 = 512), offsets and pointers
+ * 16-byte aligned.
+ */
+typedef struct {
+    int world, root;
+    int64_t B, Hq, Hkv, D, S;
+    size_t k_off, v_off, part_off;
+    const void *q;
+    void *out;
+    int64_t chunk;
+    float scale; /* 0 = 1/sqrt(D) */
+} tdg_flash_decode_args;
+
+TDG_API size_t tdg_flash_decode_part_bytes(int world, int64_t B, int64_t Hq, int64_t D, int64_t S,
+                                           int64_t chunk);
+TDG_API int tdg_flash_decode(tdg_symm *h, const tdg_flash_decode_args *args, void *stream);
+
 /* ---- MoE dispatch / combine ------------------------------------------------ */
 /*
  * Expert-parallel AllToAll as a permutation (paper summary, 实验: AllToAll

@@ -90,6 +90,10 @@ def test_host_size_helpers(L):
     # ring AllReduce: W-1 receive slots of count/W float32
     assert L.tdg_allreduce_recv_bytes(8, 1 << 20) == 7 * (1 << 17) * 4
     assert L.tdg_allreduce_recv_bytes(1, 1024) == 0
+    # flash decoding partials: W * splits * B * Hq * (D + 2) float32
+    assert L.tdg_flash_decode_part_bytes(8, 4, 64, 128, 131072, 512) == 8 * 32 * 4 * 64 * 130 * 4
+    assert L.tdg_flash_decode_part_bytes(4, 1, 16, 128, 400, 64) == 4 * 2 * 1 * 16 * 130 * 4
+    assert L.tdg_flash_decode_part_bytes(3, 1, 16, 128, 400, 64) == 0        # S % W != 0
 
 
 def test_strerror_and_invalid_handles(L):
@@ -103,6 +107,7 @@ def test_strerror_and_invalid_handles(L):
     assert L.tdg_gemm_rs(None, None, None) == tdg.TDG_ERR_INVALID
     assert L.tdg_moe_dispatch_combine(None, None, None) == tdg.TDG_ERR_INVALID
     assert L.tdg_allreduce(None, None, None) == tdg.TDG_ERR_INVALID
+    assert L.tdg_flash_decode(None, None, None) == tdg.TDG_ERR_INVALID
     h = ctypes.c_void_p()
     # misaligned base / bad world are rejected before any CUDA call
     assert L.tdg_symm_alloc(ctypes.c_void_p(1024 + 16), 1 << 20, 2, 4096, 16,

@@ -35,7 +35,7 @@ EXPORTS = [
     "tdg_symm_flags", "tdg_symm_counters", "tdg_symm_epoch", "tdg_status", "tdg_strerror",
     "tdg_device_info", "tdg_ag_gemm", "tdg_gemm_rs_stage_bytes", "tdg_gemm_rs",
     "tdg_moe_workspace_bytes", "tdg_moe_dispatch_combine", "tdg_moe_dispatch_combine_noalloc",
-    "tdg_allreduce_recv_bytes", "tdg_allreduce",
+    "tdg_allreduce_recv_bytes", "tdg_allreduce", "tdg_flash_decode_part_bytes", "tdg_flash_decode",
 ]
 MOE_STATIC_WORKSPACE_BYTES = 2 * 1024 * 1024
 
@@ -72,6 +72,13 @@ class MoeArgs(ctypes.Structure):
 class AllReduceArgs(ctypes.Structure):
     _fields_ = [("world", ctypes.c_int), ("count", _i64), ("x_off", _sz), ("recv_off", _sz),
                 ("tile_elems", _i64), ("ctas_per_rank", ctypes.c_int), ("timeout_ns", _u64)]
+
+
+class FlashDecodeArgs(ctypes.Structure):
+    _fields_ = [("world", ctypes.c_int), ("root", ctypes.c_int), ("B", _i64), ("Hq", _i64),
+                ("Hkv", _i64), ("D", _i64), ("S", _i64), ("k_off", _sz), ("v_off", _sz),
+                ("part_off", _sz), ("q", _vp), ("out", _vp), ("chunk", _i64),
+                ("scale", ctypes.c_float)]
 
 
 class TdgError(RuntimeError):
@@ -127,6 +134,10 @@ def lib():
             L.tdg_allreduce_recv_bytes.argtypes = [ctypes.c_int, _i64]
             L.tdg_allreduce.restype = ctypes.c_int
             L.tdg_allreduce.argtypes = [_vp, ctypes.POINTER(AllReduceArgs), _vp]
+            L.tdg_flash_decode_part_bytes.restype = _sz
+            L.tdg_flash_decode_part_bytes.argtypes = [ctypes.c_int, _i64, _i64, _i64, _i64, _i64]
+            L.tdg_flash_decode.restype = ctypes.c_int
+            L.tdg_flash_decode.argtypes = [_vp, ctypes.POINTER(FlashDecodeArgs), _vp]
             L.tdg_moe_dispatch_combine_noalloc.restype = ctypes.c_int
             L.tdg_moe_dispatch_combine_noalloc.argtypes = [_vp, ctypes.POINTER(MoeArgs), _vp]
             _lib = L
@@ -261,6 +272,19 @@ def allreduce(symm: Symm, count: int, x_off: int, recv_off: int, tile_elems=0, c
     a = AllReduceArgs(world=symm.world, count=count, x_off=x_off, recv_off=recv_off,
                       tile_elems=tile_elems, ctas_per_rank=ctas_per_rank, timeout_ns=timeout_ns)
     _check(lib().tdg_allreduce(symm.h, ctypes.byref(a), _stream(stream)), "tdg_allreduce")
+
+
+def flash_decode_part_bytes(world: int, B: int, Hq: int, D: int, S: int, chunk: int = 0) -> int:
+    return lib().tdg_flash_decode_part_bytes(world, B, Hq, D, S, chunk)
+
+
+def flash_decode(symm: Symm, B: int, Hq: int, Hkv: int, D: int, S: int, k_off: int, v_off: int,
+                 part_off: int, q, out, root: int = 0, chunk: int = 0, scale: float = 0.0,
+                 stream=None):
+    a = FlashDecodeArgs(world=symm.world, root=root, B=B, Hq=Hq, Hkv=Hkv, D=D, S=S, k_off=k_off,
+                        v_off=v_off, part_off=part_off, q=q.data_ptr(), out=out.data_ptr(),
+                        chunk=chunk, scale=scale)
+    _check(lib().tdg_flash_decode(symm.h, ctypes.byref(a), _stream(stream)), "tdg_flash_decode")
 
 
 def moe_workspace_bytes(world: int, T: int, E: int) -> int:
