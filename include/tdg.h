@@ -263,12 +263,12 @@ TDG_API int tdg_allreduce(tdg_symm *h, const tdg_allreduce_args *args, void *str
  * V_r (B x Hkv x S/W x D bf16) at region(r) + k_off / v_off.  Every CTA
  * reduces `chunk` tokens of one rank for one (batch, kv head) to a partial
  * (row max, row sum, normalised output, fp32) and pushes it into region(root)
- * + part_off; the CTA whose arrival completes the count for its (batch, kv
- * head) merges all partials by log-sum-exp and writes out (bf16).
- * q, out: B x Hq x D bf16 device pointers.  Counters: root's counter words
- * [0, B*Hkv).  Requirements: D == 128, Hq % Hkv == 0, Hq/Hkv <= 16,
- * S % world == 0, S > 0, chunk % 64 == 0 (0 = 512), offsets and pointers
- * 16-byte aligned.
+ * + part_off; a second, stream-ordered launch on the root merges all partials
+ * by log-sum-exp and writes out (bf16).
+ * q, out: B x Hq x D bf16 device pointers.  Requirements: D == 128,
+ * Hq % Hkv == 0, Hq/Hkv <= 16, S % world == 0, S > 0, chunk % 64 == 0
+ * (0 = 2048 tokens), world * ceil(S/world/chunk) <= 12000, offsets and
+ * pointers 16-byte aligned.
  */
 typedef struct {
     int world, root;

@@ -92,6 +92,7 @@ def test_host_size_helpers(L):
     assert L.tdg_allreduce_recv_bytes(1, 1024) == 0
     # flash decoding partials: W * splits * B * Hq * (D + 2) float32
     assert L.tdg_flash_decode_part_bytes(8, 4, 64, 128, 131072, 512) == 8 * 32 * 4 * 64 * 130 * 4
+    assert L.tdg_flash_decode_part_bytes(8, 4, 64, 128, 131072, 0) == 8 * 8 * 4 * 64 * 130 * 4
     assert L.tdg_flash_decode_part_bytes(4, 1, 16, 128, 400, 64) == 4 * 2 * 1 * 16 * 130 * 4
     assert L.tdg_flash_decode_part_bytes(3, 1, 16, 128, 400, 64) == 0        # S % W != 0
 

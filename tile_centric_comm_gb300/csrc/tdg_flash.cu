@@ -8,9 +8,9 @@
 // (m16n8k16, fp32 accumulate; the G = Hq/Hkv query heads of the kv head are
 // the M rows) and keep an online softmax in fp32 (base-2 exponent).  The warps
 // merge in shared memory; the CTA pushes (max, sum, normalised output) into
-// the root rank's partial buffer and increments the (b, g) arrival counter;
-// the CTA that completes the count merges every partial by log-sum-exp and
-// writes the bf16 output, then resets the counter.  Nothing spins.
+// the root rank's partial buffer.  A second, stream-ordered launch on the root
+// merges every partial by log-sum-exp (one CTA per (batch, query head), one
+// thread per dimension) and writes the bf16 output.  Nothing spins.
 // Decode attention is bound by HBM (about 8 FLOP per cached byte), so the
 // register-level mma.sync suffices for the arithmetic.
 #include "tdg_internal.h"
@@ -38,7 +38,6 @@ struct FlashParams {
     float *part_ml; // [W*splits][B][Hq][2]
     const __nv_bfloat16 *q;
     __nv_bfloat16 *out;
-    uint32_t *counters; // root's, [B*Hkv]
 };
 
 __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
@@ -264,39 +263,54 @@ __global__ void __launch_bounds__(fd::WARPS * 32) flash_decode_kernel(const __gr
             __stcg(p.part_ml + (part_row0 + h) * 2 + 1, L);
         }
     }
-    // signal the arrival; the last of the W * splits CTAs merges
-    __shared__ uint32_t last;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        __threadfence();
-        const uint32_t total = (uint32_t)(p.W * p.splits);
-        const uint32_t old = atom_add_acq_rel_gpu(p.counters + (size_t)b * p.Hkv + g, 1u);
-        last = old == total - 1 ? 1u : 0u;
-    }
-    __syncthreads();
-    if (!last)
-        return;
-    __threadfence();
+}
+
+// The root merges every split's partial by log-sum-exp: one CTA per
+// (batch, query head), one thread per output dimension.  The split weights
+// l_j * 2^(m_j - M) are computed once per CTA in shared memory.
+__global__ void __launch_bounds__(fd::D) flash_combine_kernel(const __grid_constant__ FlashParams p)
+{
+    extern __shared__ float wsh[]; // [nsplit] weights, then [32] reduction scratch
+    const size_t row = blockIdx.x; // b * Hq + h
     const int nsplit = p.W * p.splits;
-    for (int idx = threadIdx.x; idx < p.G * fd::D; idx += blockDim.x) {
-        const int h = idx / fd::D, d = idx % fd::D;
-        const size_t row = (size_t)b * p.Hq + (size_t)g * p.G + h;
-        float M = -INFINITY;
-        for (int s2 = 0; s2 < nsplit; ++s2)
-            M = fmaxf(M, __ldcg(p.part_ml + ((size_t)s2 * p.B * p.Hq + row) * 2));
-        const float Ms = M == -INFINITY ? 0.f : M;
-        float L = 0.f, O = 0.f;
-        for (int s2 = 0; s2 < nsplit; ++s2) {
-            const size_t pr = (size_t)s2 * p.B * p.Hq + row;
-            const float w = __ldcg(p.part_ml + pr * 2 + 1) * exp2f(__ldcg(p.part_ml + pr * 2) - Ms);
-            L += w;
-            O += __ldcg(p.part_o + pr * fd::D + d) * w;
-        }
-        p.out[row * fd::D + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
+    const size_t stride = (size_t)p.B * p.Hq;
+    float mloc = -INFINITY;
+    for (int j = threadIdx.x; j < nsplit; j += blockDim.x)
+        mloc = fmaxf(mloc, __ldcg(p.part_ml + ((size_t)j * stride + row) * 2));
+    float *red = wsh + nsplit;
+    for (int o = 16; o > 0; o >>= 1)
+        mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, o));
+    if ((threadIdx.x & 31) == 0)
+        red[threadIdx.x >> 5] = mloc;
+    __syncthreads();
+    float M = -INFINITY;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w)
+        M = fmaxf(M, red[w]);
+    const float Ms = M == -INFINITY ? 0.f : M;
+    for (int j = threadIdx.x; j < nsplit; j += blockDim.x) {
+        const size_t pr = (size_t)j * stride + row;
+        wsh[j] = __ldcg(p.part_ml + pr * 2 + 1) * exp2f(__ldcg(p.part_ml + pr * 2) - Ms);
     }
     __syncthreads();
-    if (threadIdx.x == 0)
-        st_relaxed_gpu(p.counters + (size_t)b * p.Hkv + g, 0u);
+    const int d = threadIdx.x;
+    float L = 0.f, O = 0.f;
+    int j = 0;
+    for (; j + 8 <= nsplit; j += 8) {
+        float v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            v[u] = __ldcg(p.part_o + ((size_t)(j + u) * stride + row) * fd::D + d);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            L += wsh[j + u];
+            O += v[u] * wsh[j + u];
+        }
+    }
+    for (; j < nsplit; ++j) {
+        L += wsh[j];
+        O += __ldcg(p.part_o + ((size_t)j * stride + row) * fd::D + d) * wsh[j];
+    }
+    p.out[row * fd::D + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
 }
 
 } // namespace tdg
@@ -305,7 +319,7 @@ using namespace tdg;
 using namespace tdg_host;
 
 namespace {
-int64_t fd_chunk(int64_t c) { return c > 0 ? c : 512; }
+int64_t fd_chunk(int64_t c) { return c > 0 ? c : 2048; }
 } // namespace
 
 extern "C" size_t tdg_flash_decode_part_bytes(int world, int64_t B, int64_t Hq, int64_t D, int64_t S,
@@ -336,7 +350,7 @@ extern "C" int tdg_flash_decode(tdg_symm *h, const tdg_flash_decode_args *a, voi
     const uint64_t R = h->region_bytes;
     if (a->k_off + kv_bytes > R || a->v_off + kv_bytes > R || a->part_off + part > R)
         return TDG_ERR_NOMEM;
-    if ((uint64_t)a->B * a->Hkv > h->nsig || W * splits > 65535 || a->B * a->Hkv > 65535)
+    if (a->B * a->Hkv > 65535 || (int64_t)W * splits * 4 + 128 > 48 * 1024)
         return TDG_ERR_INVALID;
     FlashParams p;
     memset(&p, 0, sizeof p);
@@ -360,7 +374,6 @@ extern "C" int tdg_flash_decode(tdg_symm *h, const tdg_flash_decode_args *a, voi
     p.part_ml = p.part_o + (size_t)W * splits * a->B * a->Hq * fd::D;
     p.q = static_cast<const __nv_bfloat16 *>(a->q);
     p.out = static_cast<__nv_bfloat16 *>(a->out);
-    p.counters = tdg_symm_counters(h, a->root);
     static bool smem_set[64] = {};
     if (!smem_set[h->device & 63]) {
         cudaError_t e = set_smem(reinterpret_cast<const void *>(&flash_decode_kernel), fd::SMEM);
@@ -369,8 +382,14 @@ extern "C" int tdg_flash_decode(tdg_symm *h, const tdg_flash_decode_args *a, voi
         smem_set[h->device & 63] = true;
     }
     void *args[] = {&p};
-    return cuda_err(launch(reinterpret_cast<const void *>(&flash_decode_kernel),
-                           dim3((unsigned)(W * splits), (unsigned)(a->B * a->Hkv)), dim3(fd::WARPS * 32),
-                           fd::SMEM, static_cast<cudaStream_t>(stream), args, false),
-                    "flash launch");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int rc = cuda_err(launch(reinterpret_cast<const void *>(&flash_decode_kernel),
+                             dim3((unsigned)(W * splits), (unsigned)(a->B * a->Hkv)), dim3(fd::WARPS * 32),
+                             fd::SMEM, st, args, false),
+                      "flash launch");
+    if (rc != TDG_OK)
+        return rc;
+    return cuda_err(launch(reinterpret_cast<const void *>(&flash_combine_kernel), dim3((unsigned)(a->B * a->Hq)),
+                           dim3(fd::D), (size_t)(W * splits + 32) * sizeof(float), st, args, false),
+                    "flash combine launch");
 }
