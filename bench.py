@@ -42,9 +42,9 @@ WORKLOAD = ("qwen32b_mlp_tp8: AG-GEMM up-proj (W=8, A_r 1024x5120, B 5120x3200) 
 
 
 # DRAM traffic of one rs_gemm_kernel launch at this workload, dram__bytes_read.sum +
-# dram__bytes_write.sum from one ncu capture (2.632 GB read + 0.743 GB written).  It is
+# dram__bytes_write.sum from one ncu capture (2.541 GB read + 0.742 GB written).  It is
 # reported only while the kernel's sources still hash to the value the capture was taken with.
-RS_TRAFFIC = {"sources": "4a3dd7b362a71a12", "bytes": 2_631_706_000 + 742_750_208}
+RS_TRAFFIC = {"sources": "f0bdf75b30dd9473", "bytes": 2_541_417_000 + 742_486_784}
 RS_SOURCES = ["tdg_gemm.cuh", "tdg_rs.cu", "tdg_ptx.cuh"]
 
 
@@ -68,7 +68,8 @@ def parse():
     ap.add_argument("--producers", type=int, default=0)
     ap.add_argument("--no-extras", action="store_true", help="skip serial/e2e/MoE/CPU legs")
     ap.add_argument("--no-cpu", action="store_true")
-    ap.add_argument("--only", default="", help="measure 'ag' or 'rs' alone (not the bench line)")
+    ap.add_argument("--only", default="", help="measure one operation alone, not the bench line: "
+                    "ag, rs, moe, ring or flash")
     ap.add_argument("--ag-shape", default="", help="W,Ms,K,N for --only ag, e.g. 8,2048,8192,7168 "
                     "(the Llama-3-70B gate+up shape)")
     return ap.parse_args()
@@ -394,6 +395,83 @@ def run_reference(args, rank):
     print(json.dumps(line), flush=True)
 
 
+def leg_moe(torch, tdg, synth, args, flush, pk):
+    extras = {}
+    # MoE dispatch + combine
+    moe = MoEBench(torch, tdg, synth)
+    moe.call(tdg.MOE_ROUTE)
+    torch.cuda.synchronize()
+    mparts = timed_steps(torch, [lambda: moe.call(tdg.MOE_ROUTE), lambda: moe.call(tdg.MOE_DISPATCH),
+                                 lambda: moe.call(tdg.MOE_COMBINE)], args.steps, args.warmup, flush)
+    m_route, m_disp, m_comb = (statistics.mean(x) for x in mparts)
+    bytes_dc = moe.bytes_dispatch + moe.bytes_combine
+    extras["moe_dispatch_combine"] = {
+        "workload": "8 ranks x 4096 tokens, hidden 7168 bf16, 256 experts, top-8 Zipf(1.2)",
+        "route_ms": m_route, "dispatch_ms": m_disp, "combine_ms": m_comb,
+        "dispatch_gbs": moe.bytes_dispatch / m_disp / 1e6, "combine_gbs": moe.bytes_combine / m_comb / 1e6,
+        "gbs": bytes_dc / (m_disp + m_comb) / 1e6,
+        "frac_of_hbm": bytes_dc / (m_disp + m_comb) / 1e6 / pk["hbm"]}
+    st = moe.symm.status()
+    if st["code"] != 0:
+        raise RuntimeError(f"device fault in MoE: {st}")
+    del moe
+    torch.cuda.empty_cache()
+    return extras["moe_dispatch_combine"]
+
+
+def leg_ring(torch, tdg, synth, args, flush, pk):
+    extras = {}
+    # ring AllReduce over the 8 logical ranks, 32 Mi float32 per rank
+    torch.manual_seed(0)
+    W, cnt = 8, 32 * 1024 * 1024
+    rsym = tdg.Symm(W, _align(cnt * 4 + tdg.allreduce_recv_bytes(W, cnt) + 2048), 65536)
+    for r in range(W):
+        rsym.view(r, 0, (cnt,), torch.float32).normal_()
+    recv_off = _align(cnt * 4)
+    aparts = timed_steps(torch, [lambda: tdg.allreduce(rsym, cnt, 0, recv_off)], args.steps, args.warmup, flush)
+    a_ms = statistics.mean(aparts[0])
+    st = rsym.status()
+    if st["code"] != 0:
+        raise RuntimeError(f"device fault in the ring AllReduce: {st}")
+    hbm = (5 * W - 4) * cnt * 4   # bytes the ring reads and writes in HBM
+    extras["ring_allreduce"] = {
+        "workload": "8 logical ranks x 32 Mi float32, ring reduce-scatter + all-gather, 64 Ki-element tiles",
+        "ms": a_ms, "hbm_bytes": hbm, "gbs": hbm / a_ms / 1e6, "frac_of_hbm": hbm / a_ms / 1e6 / pk["hbm"],
+        "busbw_gbs": 2 * (W - 1) / W * cnt * 4 / a_ms / 1e6}
+    del rsym
+    torch.cuda.empty_cache()
+    return extras["ring_allreduce"]
+
+
+def leg_flash(torch, tdg, synth, args, flush, pk):
+    extras = {}
+    # distributed flash decoding: 4 sequences x 64 heads (8 kv heads, d 128),
+    # 128 Ki cached tokens split over the 8 logical ranks
+    W, Bq, Hq, Hkv, D, S = 8, 4, 64, 8, 128, 131072
+    kvb = Bq * Hkv * (S // W) * D * 2
+    part = tdg.flash_decode_part_bytes(W, Bq, Hq, D, S)
+    fsym = tdg.Symm(W, _align(2 * _align(kvb) + part + 2048), 4096)
+    for r in range(W):
+        fsym.view(r, 0, (kvb // 2,), torch.bfloat16).normal_()
+        fsym.view(r, _align(kvb), (kvb // 2,), torch.bfloat16).normal_()
+    qf = torch.randn((Bq, Hq, D), device="cuda").to(torch.bfloat16)
+    of = torch.empty_like(qf)
+    fparts = timed_steps(torch, [lambda: tdg.flash_decode(fsym, Bq, Hq, Hkv, D, S, 0, _align(kvb),
+                                                          2 * _align(kvb), qf, of)],
+                         args.steps, args.warmup, flush)
+    f_ms = statistics.mean(fparts[0])
+    st = fsym.status()
+    if st["code"] != 0:
+        raise RuntimeError(f"device fault in flash decoding: {st}")
+    fbytes = 2 * kvb * W   # every cached K and V byte is read once
+    extras["flash_decode"] = {
+        "workload": "4 x 64 heads (8 kv heads, d 128), 128 Ki cached tokens over 8 logical ranks",
+        "ms": f_ms, "kv_bytes": fbytes, "gbs": fbytes / f_ms / 1e6, "frac_of_hbm": fbytes / f_ms / 1e6 / pk["hbm"]}
+    del fsym, qf, of
+    torch.cuda.empty_cache()
+    return extras["flash_decode"]
+
+
 def main():
     args = parse()
     rank, world, local = dist_env()
@@ -418,6 +496,18 @@ def main():
         raise SystemExit("libtdg kernels need an sm_103 device")
     pk = peaks()
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.int32, device="cuda")
+    if args.only in ("moe", "ring", "flash"):
+        leg = {"moe": leg_moe, "ring": leg_ring, "flash": leg_flash}[args.only]
+        with Clocks(local) as clk:
+            res = leg(torch, tdg, synth, args, flush, pk)
+        if rank == 0:
+            print(json.dumps({"metric": f"{args.only} GB/s", "value": res["gbs"], "unit": "GB/s",
+                              "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                              "higher_is_better": True, "dtype": "bf16" if args.only != "ring" else "f32",
+                              "roofline": {"bound": "hbm", "achieved": res["gbs"], "peak": pk["hbm"],
+                                           "unit": "GB/s", "frac": res["frac_of_hbm"]},
+                              "clocks": clk.summary(), "detail": res}), flush=True)
+        return
     mlp = MLP(torch, tdg, synth, args.mode, args.producers)
     torch.cuda.synchronize()
 
@@ -498,68 +588,9 @@ def main():
             "ag_shape_tflops": AG_FLOP / l_ag / 1e9, "rs_shapes_tflops": RS_FLOP / l_rs / 1e9}
         del mlp, a_cat, b_rs, a_rs, c_rs
         torch.cuda.empty_cache()
-        # MoE dispatch + combine
-        moe = MoEBench(torch, tdg, synth)
-        moe.call(tdg.MOE_ROUTE)
-        torch.cuda.synchronize()
-        mparts = timed_steps(torch, [lambda: moe.call(tdg.MOE_ROUTE), lambda: moe.call(tdg.MOE_DISPATCH),
-                                     lambda: moe.call(tdg.MOE_COMBINE)], args.steps, args.warmup, flush)
-        m_route, m_disp, m_comb = (statistics.mean(x) for x in mparts)
-        bytes_dc = moe.bytes_dispatch + moe.bytes_combine
-        extras["moe_dispatch_combine"] = {
-            "workload": "8 ranks x 4096 tokens, hidden 7168 bf16, 256 experts, top-8 Zipf(1.2)",
-            "route_ms": m_route, "dispatch_ms": m_disp, "combine_ms": m_comb,
-            "dispatch_gbs": moe.bytes_dispatch / m_disp / 1e6, "combine_gbs": moe.bytes_combine / m_comb / 1e6,
-            "gbs": bytes_dc / (m_disp + m_comb) / 1e6,
-            "frac_of_hbm": bytes_dc / (m_disp + m_comb) / 1e6 / pk["hbm"]}
-        st = moe.symm.status()
-        if st["code"] != 0:
-            raise RuntimeError(f"device fault in MoE: {st}")
-        del moe
-        torch.cuda.empty_cache()
-        # ring AllReduce over the 8 logical ranks, 32 Mi float32 per rank
-        torch.manual_seed(0)
-        W, cnt = 8, 32 * 1024 * 1024
-        rsym = tdg.Symm(W, _align(cnt * 4 + tdg.allreduce_recv_bytes(W, cnt) + 2048), 65536)
-        for r in range(W):
-            rsym.view(r, 0, (cnt,), torch.float32).normal_()
-        recv_off = _align(cnt * 4)
-        aparts = timed_steps(torch, [lambda: tdg.allreduce(rsym, cnt, 0, recv_off)], args.steps, args.warmup, flush)
-        a_ms = statistics.mean(aparts[0])
-        st = rsym.status()
-        if st["code"] != 0:
-            raise RuntimeError(f"device fault in the ring AllReduce: {st}")
-        hbm = (5 * W - 4) * cnt * 4   # bytes the ring reads and writes in HBM
-        extras["ring_allreduce"] = {
-            "workload": "8 logical ranks x 32 Mi float32, ring reduce-scatter + all-gather, 64 Ki-element tiles",
-            "ms": a_ms, "hbm_bytes": hbm, "gbs": hbm / a_ms / 1e6, "frac_of_hbm": hbm / a_ms / 1e6 / pk["hbm"],
-            "busbw_gbs": 2 * (W - 1) / W * cnt * 4 / a_ms / 1e6}
-        del rsym
-        torch.cuda.empty_cache()
-        # distributed flash decoding: 4 sequences x 64 heads (8 kv heads, d 128),
-        # 128 Ki cached tokens split over the 8 logical ranks
-        W, Bq, Hq, Hkv, D, S = 8, 4, 64, 8, 128, 131072
-        kvb = Bq * Hkv * (S // W) * D * 2
-        part = tdg.flash_decode_part_bytes(W, Bq, Hq, D, S)
-        fsym = tdg.Symm(W, _align(2 * _align(kvb) + part + 2048), 4096)
-        for r in range(W):
-            fsym.view(r, 0, (kvb // 2,), torch.bfloat16).normal_()
-            fsym.view(r, _align(kvb), (kvb // 2,), torch.bfloat16).normal_()
-        qf = torch.randn((Bq, Hq, D), device="cuda").to(torch.bfloat16)
-        of = torch.empty_like(qf)
-        fparts = timed_steps(torch, [lambda: tdg.flash_decode(fsym, Bq, Hq, Hkv, D, S, 0, _align(kvb),
-                                                              2 * _align(kvb), qf, of)],
-                             args.steps, args.warmup, flush)
-        f_ms = statistics.mean(fparts[0])
-        st = fsym.status()
-        if st["code"] != 0:
-            raise RuntimeError(f"device fault in flash decoding: {st}")
-        fbytes = 2 * kvb * W   # every cached K and V byte is read once
-        extras["flash_decode"] = {
-            "workload": "4 x 64 heads (8 kv heads, d 128), 128 Ki cached tokens over 8 logical ranks",
-            "ms": f_ms, "kv_bytes": fbytes, "gbs": fbytes / f_ms / 1e6, "frac_of_hbm": fbytes / f_ms / 1e6 / pk["hbm"]}
-        del fsym, qf, of
-        torch.cuda.empty_cache()
+        extras["moe_dispatch_combine"] = leg_moe(torch, tdg, synth, args, flush, pk)
+        extras["ring_allreduce"] = leg_ring(torch, tdg, synth, args, flush, pk)
+        extras["flash_decode"] = leg_flash(torch, tdg, synth, args, flush, pk)
         if rank == 0 and not args.no_cpu:
             r, s, desc = cpu_oracle_rate()
             cpu = {"value": r, "unit": "TFLOP/s", "cores": omp_threads(), "kind": "oracle", "sample": desc,
