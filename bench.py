@@ -63,8 +63,9 @@ def parse():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="tdg", choices=["tdg", "reference"])
-    ap.add_argument("--mode", default="ce", choices=["sm", "ce"],
-                    help="AG-GEMM overlap: ce = copy engine + flags (default), sm = producer CTAs")
+    ap.add_argument("--mode", default="ce", choices=["sm", "ce", "serial"],
+                    help="AG-GEMM overlap: ce = copy engine + flags (default), sm = producer CTAs, "
+                         "serial = copy launch then GEMM launch (for measurement only)")
     ap.add_argument("--producers", type=int, default=0)
     ap.add_argument("--no-extras", action="store_true", help="skip serial/e2e/MoE/CPU legs")
     ap.add_argument("--no-cpu", action="store_true")
@@ -558,7 +559,7 @@ def main():
                              "overlap_gain_vs_serial": s_rs / rs_ms,
                              "frac_of_bf16_peak": RS_FLOP / rs_ms / 1e9 / pk["bf16"]}
         extras["overlap_gain_vs_serial"] = (s_ag + s_rs) / (ag_ms + rs_ms)
-        other = "sm" if args.mode == "ce" else "ce"
+        other = "sm" if args.mode != "sm" else "ce"
         cparts = timed_steps(torch, [lambda: mlp.ag_call(other)], args.steps, args.warmup, flush)
         c_ag = statistics.mean(cparts[0])
         extras["ag_gemm"]["mode"] = args.mode

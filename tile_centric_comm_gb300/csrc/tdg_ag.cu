@@ -63,6 +63,7 @@ struct AgParams {
     int pair; // 1: CTA pairs (cta_group::2) with 256-row tiles
     int split; // tiles of the last, partial wave split in two 128-column halves
     int mesh;  // 1: producers take all sources at once (round robin over sources)
+    int group_m; // m rows per raster group
     // LL mode: producer CTAs [0, n_send) send, [n_send, n_prod) receive
     int ll;
     int n_send;
@@ -90,8 +91,17 @@ template <int BMN> struct AgPolicy {
             tid = full + (item - full) / 2;
             nhalf = (int)((item - full) & 1);
         }
-        const int pm0 = (int)(tid / p.n_tiles);
-        t.pn = (int)(tid % p.n_tiles);
+        // grouped raster: groups of up to GM m rows, n outer inside a group, so
+        // a wave reuses GM rows of A and a few columns of B from L2 instead of
+        // streaming all of B (chosen when B does not fit in L2; otherwise GM
+        // covers every m row and the order is m-major, following the shards)
+        const int GM = p.group_m;
+        const int64_t per_group = (int64_t)GM * p.n_tiles;
+        const int grp = (int)(tid / per_group);
+        const int64_t in = tid % per_group;
+        const int rows = min(GM, p.m_tiles - grp * GM);
+        t.pn = (int)(in / rows);
+        const int pm0 = grp * GM + (int)(in % rows);
         // the pages' swizzle: pid_m = (pid_m + rank * tiles_per_pe) % total
         const int pm = (pm0 + p.swz) % p.m_tiles;
         t.m0 = pm * tm + half * gm::BM;
@@ -516,6 +526,8 @@ extern "C" int tdg_ag_gemm(tdg_symm *h, const tdg_ag_gemm_args *a, void *stream,
     p.Ms = Ms;
     p.pair = pair;
     p.m_tiles = (int)((M + TM - 1) / TM);
+    // B larger than about half of L2: group 8 m rows per raster group
+    p.group_m = ((uint64_t)K * N * 2 > (64ull << 20)) ? 8 : p.m_tiles;
     p.n_tiles = (int)((N + gm::BN - 1) / gm::BN);
     p.swz = a->swizzle ? (int)(((int64_t)rank * Ms / TM) % p.m_tiles) : 0;
     p.local_inplace = inplace ? 1 : 0;

@@ -64,20 +64,21 @@ __device__ void rs_reduce_rows(const RsParams &p, int o, int m_loc, int pn, int 
         return;
     uint8_t *out_base = p.regions + (uint64_t)o * p.region_bytes + p.out_off;
     const int64_t n0 = (int64_t)pn * gm::BN;
-    for (int rr = 0; rr < 32; rr += 2) {
-        float acc[2][8];
+    constexpr int RR = 4; // rows in flight per lane: RR x 8 ranks x 16 B
+    for (int rr = 0; rr < 32; rr += RR) {
+        float acc[RR][8];
 #pragma unroll
-        for (int a = 0; a < 2; ++a)
+        for (int a = 0; a < RR; ++a)
 #pragma unroll
             for (int j = 0; j < 8; ++j)
                 acc[a][j] = 0.f;
         for (int r0 = 0; r0 < p.W; r0 += 8) {
-            uint4 v[2][8];
+            uint4 v[RR][8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 if (r0 + j < p.W) {
 #pragma unroll
-                    for (int a = 0; a < 2; ++a)
+                    for (int a = 0; a < RR; ++a)
                         v[a][j] = __ldcg(reinterpret_cast<const uint4 *>(
                             rs_stage_row(p, o, r0 + j, m_loc, pn, row0 + rr + a) + col * 2));
                 }
@@ -86,7 +87,7 @@ __device__ void rs_reduce_rows(const RsParams &p, int o, int m_loc, int pn, int 
             for (int j = 0; j < 8; ++j) {
                 if (r0 + j < p.W) {
 #pragma unroll
-                    for (int a = 0; a < 2; ++a) {
+                    for (int a = 0; a < RR; ++a) {
                         const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&v[a][j]);
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
@@ -99,7 +100,7 @@ __device__ void rs_reduce_rows(const RsParams &p, int o, int m_loc, int pn, int 
             }
         }
 #pragma unroll
-        for (int a = 0; a < 2; ++a) {
+        for (int a = 0; a < RR; ++a) {
             const int64_t orow = (int64_t)m_loc * gm::BM + row0 + rr + a;
             uint4 w;
             w.x = pack_bf16x2(acc[a][0], acc[a][1]);
