@@ -44,7 +44,7 @@ WORKLOAD = ("qwen32b_mlp_tp8: AG-GEMM up-proj (W=8, A_r 1024x5120, B 5120x3200) 
 # DRAM traffic of one rs_gemm_kernel launch at this workload, dram__bytes_read.sum +
 # dram__bytes_write.sum from one ncu capture (2.541 GB read + 0.742 GB written).  It is
 # reported only while the kernel's sources still hash to the value the capture was taken with.
-RS_TRAFFIC = {"sources": "f0bdf75b30dd9473", "bytes": 2_541_417_000 + 742_486_784}
+RS_TRAFFIC = {"sources": "0f3af002ae3df248", "bytes": 2_591_494_656 + 743_805_184}
 RS_SOURCES = ["tdg_gemm.cuh", "tdg_rs.cu", "tdg_ptx.cuh"]
 
 
@@ -67,6 +67,8 @@ def parse():
                     help="AG-GEMM overlap: ce = copy engine + flags (default), sm = producer CTAs, "
                          "serial = copy launch then GEMM launch (for measurement only)")
     ap.add_argument("--producers", type=int, default=0)
+    ap.add_argument("--signal-rows", type=int, default=0,
+                    help="AG rows per signal group (0: the library's default for the mode)")
     ap.add_argument("--no-extras", action="store_true", help="skip serial/e2e/MoE/CPU legs")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--only", default="", help="measure one operation alone, not the bench line: "
@@ -172,8 +174,9 @@ def _align(x, a=1024):
 class MLP:
     """Inputs of both operations resident in two symmetric heaps."""
 
-    def __init__(self, torch, tdg, synth, mode, producers):
+    def __init__(self, torch, tdg, synth, mode, producers, signal_rows=0):
         self.torch, self.tdg, self.mode, self.producers = torch, tdg, mode, producers
+        self.signal_rows = signal_rows
         ag = synth.ag_inputs(AG["W"], AG["Ms"], AG["K"], AG["N"], "normal", seed=0)
         W, Ms, K, N = AG["W"], AG["Ms"], AG["K"], AG["N"]
         self.ag_a_off = 0
@@ -213,7 +216,8 @@ class MLP:
         if mode == "ce" and side is None:
             side = self._side()
         self.tdg.ag_gemm(self.ag, 0, AG["Ms"], AG["K"], AG["N"], self.ag_a_off, self.ag_g_off,
-                         self.ag_B, self.ag_C, mode=mode, producers=self.producers, side_stream=side)
+                         self.ag_B, self.ag_C, mode=mode, producers=self.producers,
+                         signal_rows=self.signal_rows, side_stream=side)
 
     def _side(self):
         if not hasattr(self, "_side_stream"):
@@ -509,7 +513,7 @@ def main():
                                            "unit": "GB/s", "frac": res["frac_of_hbm"]},
                               "clocks": clk.summary(), "detail": res}), flush=True)
         return
-    mlp = MLP(torch, tdg, synth, args.mode, args.producers)
+    mlp = MLP(torch, tdg, synth, args.mode, args.producers, args.signal_rows)
     torch.cuda.synchronize()
 
     fns = [lambda: mlp.ag_call(), lambda: mlp.rs_call("sm")]

@@ -91,17 +91,25 @@ template <int BMN> struct AgPolicy {
             tid = full + (item - full) / 2;
             nhalf = (int)((item - full) & 1);
         }
-        // grouped raster: groups of up to GM m rows, n outer inside a group, so
-        // a wave reuses GM rows of A and a few columns of B from L2 instead of
-        // streaming all of B (chosen when B does not fit in L2; otherwise GM
-        // covers every m row and the order is m-major, following the shards)
+        // Two rasters.  group_m == 0: m-major (all n tiles of one m row, then
+        // the next row), so the tiles of a wave follow the shards in arrival
+        // order and wait on as few signals as possible (B stays in L2).
+        // group_m > 0: groups of group_m m rows, n outer inside a group, so a
+        // wave reuses those rows of A and a few columns of B from L2 instead
+        // of streaming all of B (chosen when B does not fit in L2).
+        int pm0;
         const int GM = p.group_m;
-        const int64_t per_group = (int64_t)GM * p.n_tiles;
-        const int grp = (int)(tid / per_group);
-        const int64_t in = tid % per_group;
-        const int rows = min(GM, p.m_tiles - grp * GM);
-        t.pn = (int)(in / rows);
-        const int pm0 = grp * GM + (int)(in % rows);
+        if (GM <= 0) {
+            pm0 = (int)(tid / p.n_tiles);
+            t.pn = (int)(tid % p.n_tiles);
+        } else {
+            const int64_t per_group = (int64_t)GM * p.n_tiles;
+            const int grp = (int)(tid / per_group);
+            const int64_t in = tid % per_group;
+            const int rows = min(GM, p.m_tiles - grp * GM);
+            t.pn = (int)(in / rows);
+            pm0 = grp * GM + (int)(in % rows);
+        }
         // the pages' swizzle: pid_m = (pid_m + rank * tiles_per_pe) % total
         const int pm = (pm0 + p.swz) % p.m_tiles;
         t.m0 = pm * tm + half * gm::BM;
@@ -526,8 +534,9 @@ extern "C" int tdg_ag_gemm(tdg_symm *h, const tdg_ag_gemm_args *a, void *stream,
     p.Ms = Ms;
     p.pair = pair;
     p.m_tiles = (int)((M + TM - 1) / TM);
-    // B larger than about half of L2: group 8 m rows per raster group
-    p.group_m = ((uint64_t)K * N * 2 > (64ull << 20)) ? 8 : p.m_tiles;
+    // B larger than about half of L2: group 8 m rows per raster group;
+    // otherwise m-major
+    p.group_m = ((uint64_t)K * N * 2 > (64ull << 20)) ? 8 : 0;
     p.n_tiles = (int)((N + gm::BN - 1) / gm::BN);
     p.swz = a->swizzle ? (int)(((int64_t)rank * Ms / TM) % p.m_tiles) : 0;
     p.local_inplace = inplace ? 1 : 0;
