@@ -60,7 +60,8 @@ struct AgParams {
     int local_last;
     uint32_t *flags_w;
     uint64_t skip_mask;
-    int pair; // 1: CTA pairs (cta_group::2) with 256-row tiles
+    int pair; // 1: CTA pairs (cta_group::2)
+    int cl;   // CTAs per cluster (1, 2 or 4): tiles of 128 * cl rows
     int split; // tiles of the last, partial wave split in two 128-column halves
     int mesh;  // 1: producers take all sources at once (round robin over sources)
     int group_m; // m rows per raster group
@@ -74,16 +75,16 @@ template <int BMN> struct AgPolicy {
     using Params = AgParams;
     static constexpr int B_MN = BMN;
 
-    // With a persistent grid of U scheduling units (CTAs or pairs) and T tiles,
+    // With a persistent grid of U scheduling units (CTAs or clusters) and T tiles,
     // the last wave holds only T mod U tiles.  Optionally, when twice that still
     // fits in a wave, those `split` tiles are cut into two 128-column halves.
     __device__ static int64_t num_items(const Params &p) { return (int64_t)p.m_tiles * p.n_tiles + p.split; }
 
-    // tiles are tile_m = 128 (one CTA) or 256 (CTA pair) rows; `half` picks this
-    // CTA's 128-row slice
-    __device__ static void tile(const Params &p, int64_t item, TileInfo &t, int half)
+    // tiles are 128 * cl rows (one CTA, a CTA pair, or two pairs); `sub`
+    // picks this CTA's 128-row slice
+    __device__ static void tile(const Params &p, int64_t item, TileInfo &t, int sub)
     {
-        const int tm = p.pair ? 2 * gm::BM : gm::BM;
+        const int tm = p.cl * gm::BM;
         const int64_t full = (int64_t)p.m_tiles * p.n_tiles - p.split;
         int64_t tid = item;
         int nhalf = -1; // -1: whole tile; 0 / 1: a half of a split tail tile
@@ -112,7 +113,7 @@ template <int BMN> struct AgPolicy {
         }
         // the pages' swizzle: pid_m = (pid_m + rank * tiles_per_pe) % total
         const int pm = (pm0 + p.swz) % p.m_tiles;
-        t.m0 = pm * tm + half * gm::BM;
+        t.m0 = pm * tm + sub * gm::BM;
         t.n0 = t.pn * gm::BN;
         t.n_valid = (int)min((int64_t)gm::BN, p.N - t.n0);
         if (nhalf >= 0) {
@@ -154,31 +155,43 @@ template <int BMN> struct AgPolicy {
 
     // The TMA form is chosen at compile time: a kernel holds either only
     // cta_group::1 or only cta_group::2 instructions, never both.
-    template <int PAIR>
+    template <int CL>
     __device__ static void load(void *dst, const CUtensorMap *m, uint32_t bar, int x, int y)
     {
-        if constexpr (PAIR)
+        if constexpr (CL >= 2)
             tma_load_2d_pair(dst, m, bar, x, y);
         else
             tma_load_2d_addr(dst, m, bar, x, y);
     }
 
-    template <int PAIR>
+    template <int CL>
     __device__ static void load_a(const Params &p, const TileInfo &t, void *dst, uint32_t bar, int kb)
     {
-        load<PAIR>(dst, t.a_sel ? &p.tmA_l : &p.tmA_g, bar, kb * gm::BK, t.a_row);
+        load<CL>(dst, t.a_sel ? &p.tmA_l : &p.tmA_g, bar, kb * gm::BK, t.a_row);
     }
 
-    template <int PAIR>
+    // B slices of 64 columns (8 KB): MN-major boxes {64 cols, 64 K}; K-major
+    // boxes {64 K, 64 rows} with CL = 4, else one box of all the columns
+    template <int CL>
     __device__ static void load_b(const Params &p, const TileInfo &, void *dst, uint32_t bar, int kb,
-                                  int col0, int cols)
+                                  int col0, int cols, int pidx, int half)
     {
-        if (BMN) {
+        uint8_t *d = static_cast<uint8_t *>(dst);
+        if constexpr (CL == 4) {
+            const uint16_t mask = (uint16_t)((1u << half) | (1u << (2 + half)));
+            const int nch = BMN ? (cols + 63) >> 6 : 2;
+            for (int j = pidx; j < nch; j += 2) {
+                if (BMN)
+                    tma_load_2d_pair_mc(d + j * 8192, &p.tmB, bar, col0 + 64 * j, kb * gm::BK, mask);
+                else
+                    tma_load_2d_pair_mc(d + j * 8192, &p.tmB, bar, kb * gm::BK, col0 + 64 * j, mask);
+            }
+        } else if (BMN) {
             const int nch = (cols + 63) >> 6;
             for (int j = 0; j < nch; ++j)
-                load<PAIR>(static_cast<uint8_t *>(dst) + j * 8192, &p.tmB, bar, col0 + 64 * j, kb * gm::BK);
+                load<CL>(d + j * 8192, &p.tmB, bar, col0 + 64 * j, kb * gm::BK);
         } else {
-            load<PAIR>(dst, &p.tmB, bar, kb * gm::BK, col0);
+            load<CL>(dst, &p.tmB, bar, kb * gm::BK, col0);
         }
     }
 
@@ -355,13 +368,13 @@ __device__ void ll_receiver(const AgParams &p, int cta, int ncta)
     }
 }
 
-template <int BMN, int PAIR>
+template <int BMN, int CL>
 __global__ void __launch_bounds__(gm::NUM_THREADS, 1) ag_gemm_kernel(const __grid_constant__ AgParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
     if ((int)blockIdx.x < p.n_prod) {
-        // producer CTAs never take part in a pair
+        // producer CTAs fill whole clusters and take no part in the GEMM
         if (!p.ll)
             ag_producer(p, smem);
         else if ((int)blockIdx.x < p.n_send)
@@ -371,10 +384,7 @@ __global__ void __launch_bounds__(gm::NUM_THREADS, 1) ag_gemm_kernel(const __gri
         return;
     }
     const int c = (int)blockIdx.x - p.n_prod, nc = (int)gridDim.x - p.n_prod;
-    if (PAIR)
-        gemm_consumer<AgPolicy<BMN>, 1>(p, smem, c >> 1, nc >> 1);
-    else
-        gemm_consumer<AgPolicy<BMN>, 0>(p, smem, c, nc);
+    gemm_consumer<AgPolicy<BMN>, CL>(p, smem, c / CL, nc / CL);
 }
 
 } // namespace tdg
@@ -384,13 +394,15 @@ using namespace tdg_host;
 
 namespace {
 
-const void *ag_kernel_fn(int b_layout, int pair)
+const void *ag_kernel_fn(int b_layout, int cl)
 {
     if (b_layout == TDG_B_KN)
-        return pair ? reinterpret_cast<const void *>(&ag_gemm_kernel<1, 1>)
-                    : reinterpret_cast<const void *>(&ag_gemm_kernel<1, 0>);
-    return pair ? reinterpret_cast<const void *>(&ag_gemm_kernel<0, 1>)
-                : reinterpret_cast<const void *>(&ag_gemm_kernel<0, 0>);
+        return cl == 4   ? reinterpret_cast<const void *>(&ag_gemm_kernel<1, 4>)
+               : cl == 2 ? reinterpret_cast<const void *>(&ag_gemm_kernel<1, 2>)
+                         : reinterpret_cast<const void *>(&ag_gemm_kernel<1, 1>);
+    return cl == 4   ? reinterpret_cast<const void *>(&ag_gemm_kernel<0, 4>)
+           : cl == 2 ? reinterpret_cast<const void *>(&ag_gemm_kernel<0, 2>)
+                     : reinterpret_cast<const void *>(&ag_gemm_kernel<0, 1>);
 }
 
 int prepare(const void *fn, int dev)
@@ -413,25 +425,25 @@ int prepare(const void *fn, int dev)
 // grid for a launch with n_prod producer CTAs plus consumers on every other SM
 int ag_grid(const AgParams &p, int b_layout, int sms, int dev)
 {
-    if (!p.pair)
+    if (p.cl == 1)
         return sms;
-    if (prepare(ag_kernel_fn(b_layout, 1), dev) != TDG_OK)
+    if (prepare(ag_kernel_fn(b_layout, p.cl), dev) != TDG_OK)
         return 0;
-    const int mp = max_pairs(ag_kernel_fn(b_layout, 1), gm::NUM_THREADS, gm::SMEM_BYTES);
-    const int pairs = mp > 0 ? (mp < sms / 2 ? mp : sms / 2) : 0;
-    return 2 * pairs;
+    const int mc = max_clusters(ag_kernel_fn(b_layout, p.cl), gm::NUM_THREADS, gm::SMEM_BYTES, p.cl);
+    const int n = mc > 0 ? (mc < sms / p.cl ? mc : sms / p.cl) : 0;
+    return p.cl * n;
 }
 
 int launch_ag(const AgParams &p, int b_layout, int grid, bool coop, cudaStream_t s, int dev)
 {
-    const void *fn = ag_kernel_fn(b_layout, p.pair);
+    const void *fn = ag_kernel_fn(b_layout, p.cl);
     int rc = prepare(fn, dev);
     if (rc != TDG_OK)
         return rc;
     if (grid < 1 || grid < p.n_prod) // a copy-only launch has no consumers
         return TDG_ERR_UNSUPPORTED;
     AgParams q = p;
-    const int64_t units = p.pair ? (grid - p.n_prod) / 2 : grid - p.n_prod;
+    const int64_t units = (grid - p.n_prod) / p.cl;
     const int64_t T = (int64_t)p.m_tiles * p.n_tiles;
     q.split = 0;
     // opt-in (TDG_SPLIT_TAIL=1): measured slower at the Qwen-32B up-projection
@@ -441,13 +453,12 @@ int launch_ag(const AgParams &p, int b_layout, int grid, bool coop, cudaStream_t
     if (st && st[0] == '1' && units > 0 && T > units && (T % units) > 0 && 2 * (T % units) <= units)
         q.split = (int)(T % units);
     void *args[] = {&q};
-    cudaError_t e = launch(fn, dim3(grid), dim3(gm::NUM_THREADS), gm::SMEM_BYTES, s, args, coop,
-                           p.pair ? 2 : 1);
-    if (e != cudaSuccess && coop && p.pair) {
+    cudaError_t e = launch(fn, dim3(grid), dim3(gm::NUM_THREADS), gm::SMEM_BYTES, s, args, coop, p.cl);
+    if (e != cudaSuccess && coop && p.cl > 1) {
         // co-residency then rests on the grid being no larger than the number
         // of clusters that fit at once (the bounded waits cover the rest)
         (void)cudaGetLastError();
-        e = launch(fn, dim3(grid), dim3(gm::NUM_THREADS), gm::SMEM_BYTES, s, args, false, 2);
+        e = launch(fn, dim3(grid), dim3(gm::NUM_THREADS), gm::SMEM_BYTES, s, args, false, p.cl);
     }
     return cuda_err(e, "ag launch");
 }
@@ -493,9 +504,11 @@ extern "C" int tdg_ag_gemm(tdg_symm *h, const tdg_ag_gemm_args *a, void *stream,
     }
 
     const int BM = gm::BM;
-    // CTA pairs (256-row tiles) once there is more than one 128-row tile
+    // CTA pairs (256-row tiles) once there is more than one 128-row tile; two
+    // pairs sharing B (512-row tiles) when every shard is a whole number of them
     const int pair = (pairs_enabled() && M > BM && !ll) ? 1 : 0;
-    const int TM = pair ? 2 * BM : BM;
+    const int cl = pair ? ((quads_enabled() && Ms % (4 * BM) == 0) ? 4 : 2) : 1;
+    const int TM = cl * BM;
     const bool inplace = (Ms % TM) == 0;
     int64_t sig_rows = a->signal_rows;
     if (sig_rows <= 0)
@@ -517,7 +530,7 @@ extern "C" int tdg_ag_gemm(tdg_symm *h, const tdg_ag_gemm_args *a, void *stream,
     if (a->b_layout == TDG_B_KN)
         ok = ok && map_bf16_2d(&p.tmB, a->B, N, K, N * 2, 64, 64);
     else
-        ok = ok && map_bf16_2d(&p.tmB, a->B, K, N, K * 2, 64, pair ? 128 : 256);
+        ok = ok && map_bf16_2d(&p.tmB, a->B, K, N, K * 2, 64, cl == 4 ? 64 : (pair ? 128 : 256));
     ok = ok && map_bf16_2d(&p.tmC, a->C, N, M, N * 2, 64, 32);
     if (!ok)
         return TDG_ERR_CUDA;
@@ -533,6 +546,7 @@ extern "C" int tdg_ag_gemm(tdg_symm *h, const tdg_ag_gemm_args *a, void *stream,
     p.N = N;
     p.Ms = Ms;
     p.pair = pair;
+    p.cl = cl;
     p.m_tiles = (int)((M + TM - 1) / TM);
     // B larger than about half of L2: group 8 m rows per raster group;
     // otherwise m-major
@@ -579,8 +593,7 @@ extern "C" int tdg_ag_gemm(tdg_symm *h, const tdg_ag_gemm_args *a, void *stream,
     }
     if (a->mode == TDG_MODE_SM) {
         int nprod = a->producers > 0 ? a->producers : 16;
-        if (pair)
-            nprod = (nprod + 1) & ~1; // producer CTAs fill whole clusters
+        nprod = (nprod + cl - 1) / cl * cl; // producer CTAs fill whole clusters
         if (nprod >= ggrid)
             return TDG_ERR_INVALID;
         p.n_prod = nprod;
@@ -604,6 +617,7 @@ extern "C" int tdg_ag_gemm(tdg_symm *h, const tdg_ag_gemm_args *a, void *stream,
         c.n_units = (int64_t)W * c.units_per_shard;
         c.local_last = 0;
         c.pair = 0;
+        c.cl = 1;
         int rc = launch_ag(c, a->b_layout, sms, false, s, dev);
         if (rc != TDG_OK)
             return rc;

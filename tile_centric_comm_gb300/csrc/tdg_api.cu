@@ -122,15 +122,17 @@ cudaError_t launch(const void *fn, dim3 grid, dim3 block, size_t smem, cudaStrea
     return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
-int max_pairs(const void *fn, int block, int smem)
+int max_pairs(const void *fn, int block, int smem) { return max_clusters(fn, block, smem, 2); }
+
+int max_clusters(const void *fn, int block, int smem, int cl)
 {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2);
+    cfg.gridDim = dim3(cl);
     cfg.blockDim = dim3(block);
     cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.x = (unsigned)cl;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;

@@ -15,16 +15,22 @@
 //               128B-swizzled staging -> TMA store; then the policy's
 //               after-tile hook (the GEMM+RS signal and reduction).
 //
-// Two shapes of the same pipeline (template parameter PAIR):
-//   PAIR = 0  one CTA per SM owns a 128 x 256 tile; 4 stages of 48 KB.
-//   PAIR = 1  a cluster of two CTAs (an SM pair) owns a 256 x 256 tile:
-//             each CTA loads its 128 rows of A and half of the tile's columns
-//             of B; the leader CTA issues tcgen05.mma.cta_group::2, which
-//             reads both CTAs' shared memory and writes each CTA's TMEM
-//             (its own 128 rows).  Both CTAs' loads complete on the leader's
-//             barrier; the leader's commits arrive on both CTAs' barriers.
-//             Stages are 32 KB, so 6 are in flight, and each SM moves a third
-//             less operand data per FLOP than with PAIR = 0.
+// Three shapes of the same pipeline (template parameter CL, CTAs per cluster):
+//   CL = 1  one CTA per SM owns a 128 x 256 tile; 4 stages of 48 KB.
+//   CL = 2  a cluster of two CTAs (an SM pair) owns a 256 x 256 tile:
+//           each CTA loads its 128 rows of A and half of the tile's columns
+//           of B; the leader CTA issues tcgen05.mma.cta_group::2, which
+//           reads both CTAs' shared memory and writes each CTA's TMEM
+//           (its own 128 rows).  Both CTAs' loads complete on the leader's
+//           barrier; the leader's commits arrive on both CTAs' barriers.
+//           Stages are 32 KB, so 6 are in flight, and each SM moves a third
+//           less operand data per FLOP than with CL = 1.
+//   CL = 4  two such pairs stacked in M own a 512 x 256 tile and share B:
+//           each B slice (64 columns x 64 K) is fetched once from L2 by one
+//           pair and multicast into the same slot of the other pair, so
+//           every CTA requests 24 KB instead of 32 KB per stage.  A slot is
+//           refilled only after both pairs' MMAs have released it (each
+//           leader's commit arrives on the empty barrier of all four CTAs).
 // A tile at the right edge of N issues a narrower MMA and stores only its
 // valid columns; rows past M come from TMA zero fill and are not stored.
 // Operands: A is K-major (rows of K); B is either MN-major (K x N row-major,
@@ -61,7 +67,7 @@ static_assert(Shape<0>::STAGES == 4 && Shape<1>::STAGES == 6, "ring layout");
 } // namespace gm
 
 struct TileInfo {
-    int m0;      // first output row handled by THIS CTA (tile row + 128 * half)
+    int m0;      // first output row handled by THIS CTA (tile row + 128 * sub)
     int n0;      // first output column of the tile
     int n_valid; // columns of this tile inside N (1..BN)
     int n_mma;   // MMA N: n_valid rounded up (16 for one CTA, 32 for a pair)
@@ -96,34 +102,45 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p)
 //                   int k_blocks; };
 //   static constexpr int B_MN;                                   // 1: B is K x N
 //   __device__ static int64_t num_items(const Params&);
-//   __device__ static void tile(const Params&, int64_t item, TileInfo&, int half);
-//       (an item with n_valid <= 0 is a null item: every role skips it)
+//   __device__ static void tile(const Params&, int64_t item, TileInfo&, int sub);
+//       (sub: this CTA's 128-row slice of the cluster's tile; an item with
+//        n_valid <= 0 is a null item: every role skips it)
 //   __device__ static void before_a(const Params&, const TileInfo&, bool &gave_up);  // loader thread
-//   template <int PAIR> __device__ static void load_a(const Params&, const TileInfo&, void *dst,
-//                                                     uint32_t bar, int kb);
-//   template <int PAIR> __device__ static void load_b(const Params&, const TileInfo&, void *dst,
-//                                                     uint32_t bar, int kb, int col0, int cols);
+//   template <int CL> __device__ static void load_a(const Params&, const TileInfo&, void *dst,
+//                                                   uint32_t bar, int kb);
+//   template <int CL> __device__ static void load_b(const Params&, const TileInfo&, void *dst,
+//                                                   uint32_t bar, int kb, int col0, int cols,
+//                                                   int pidx, int half);
+//       (CL = 4: pair pidx fetches the 64-column slices j with j % 2 == pidx
+//        and multicasts each to CTA `half` of both pairs)
 //   __device__ static uint32_t b_bytes(const Params&, const TileInfo&, int cols);
 //   __device__ static void store_chunk(const Params&, const TileInfo&, const void *buf, int ch, int q);
 //   __device__ static void after_tile(const Params&, const TileInfo&, int q, int lane);  // per epilogue warp
-// The load hooks receive the mbarrier as a shared::cluster address (the
-// leader's barrier in pair mode) and issue pair TMA when PAIR is set.  All
+// The load hooks receive the mbarrier as a shared::cluster address (the pair
+// leader's barrier when CL >= 2) and issue pair TMA when CL >= 2.  All
 // tcgen05 and TMA instructions of one kernel use a single cta_group.
-template <class P, int PAIR>
+template <class P, int CL>
 __device__ void gemm_consumer(const typename P::Params &p, uint8_t *smem, int unit, int nunits)
 {
     using namespace gm;
+    constexpr int PAIR = CL >= 2 ? 1 : 0;
+    constexpr bool QUAD = CL == 4;
     using S = Shape<PAIR>;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int half = PAIR ? (int)cluster_ctarank() : 0;
+    const int crank = PAIR ? (int)cluster_ctarank() : 0; // this CTA's 128-row slice of the tile
+    const int half = crank & 1;                           // CTA in its pair
+    const int pidx = crank >> 1;                          // pair in the cluster
     const bool leader = half == 0;
+    const uint32_t lead_rank = (uint32_t)(crank & ~1);
+    const uint16_t pair_mask = (uint16_t)(3u << (2 * pidx));
+    const uint16_t empty_mask = QUAD ? (uint16_t)0xF : pair_mask;
     PipeSmem *ps = reinterpret_cast<PipeSmem *>(smem + OFF_BAR);
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < S::STAGES; ++i) {
             mbar_init(&ps->full[i], 1);
-            mbar_init(&ps->empty[i], 1);
+            mbar_init(&ps->empty[i], QUAD ? 2 : 1); // one commit per pair sharing the slot
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&ps->tfull[i], 1);
@@ -153,9 +170,10 @@ __device__ void gemm_consumer(const typename P::Params &p, uint8_t *smem, int un
     const uint32_t tmem_base = ps->tmem_base;
     const int64_t items = P::num_items(p);
     const uint64_t tmo = p.pipe_timeout_ns;
-    // the barrier a load completes on / an epilogue releases: the leader's
-    const uint32_t full0 = PAIR ? mapa_shared(smem_u32(&ps->full[0]), 0) : smem_u32(&ps->full[0]);
-    const uint32_t tempty0 = PAIR ? mapa_shared(smem_u32(&ps->tempty[0]), 0) : smem_u32(&ps->tempty[0]);
+    // the barrier a load completes on / an epilogue releases: the pair leader's
+    const uint32_t full0 = PAIR ? mapa_shared(smem_u32(&ps->full[0]), lead_rank) : smem_u32(&ps->full[0]);
+    const uint32_t tempty0 =
+        PAIR ? mapa_shared(smem_u32(&ps->tempty[0]), lead_rank) : smem_u32(&ps->tempty[0]);
 
     if (warp == 0) {
         if (lane == 0) {
@@ -164,7 +182,7 @@ __device__ void gemm_consumer(const typename P::Params &p, uint8_t *smem, int un
             bool gave_up = false;
             for (int64_t it = unit; it < items && !ps->abort; it += nunits) {
                 TileInfo ti;
-                P::tile(p, it, ti, half);
+                P::tile(p, it, ti, crank);
                 if (ti.n_valid <= 0)
                     continue; // a null item (an empty half of a split tail tile)
                 P::before_a(p, ti, gave_up);
@@ -182,8 +200,8 @@ __device__ void gemm_consumer(const typename P::Params &p, uint8_t *smem, int un
                     if (leader)
                         mbar_arrive_expect_tx(&ps->full[stage], PAIR ? 2 * my_bytes : my_bytes);
                     const uint32_t bar = full0 + stage * 8;
-                    P::template load_a<PAIR>(p, ti, sa, bar, kb);
-                    P::template load_b<PAIR>(p, ti, sa + A_BYTES, bar, kb, col0, cols);
+                    P::template load_a<CL>(p, ti, sa, bar, kb);
+                    P::template load_b<CL>(p, ti, sa + A_BYTES, bar, kb, col0, cols, pidx, half);
                     ps->issued += 1;
                     if (++stage == S::STAGES) {
                         stage = 0;
@@ -202,7 +220,7 @@ __device__ void gemm_consumer(const typename P::Params &p, uint8_t *smem, int un
             const uint32_t sbase = smem_u32(smem);
             for (int64_t it = unit; it < items && !ps->abort; it += nunits) {
                 TileInfo ti;
-                P::tile(p, it, ti, half);
+                P::tile(p, it, ti, crank);
                 if (ti.n_valid <= 0)
                     continue;
                 const uint32_t idesc = idesc_bf16(S::TILE_M, ti.n_mma, P::B_MN);
@@ -238,7 +256,7 @@ __device__ void gemm_consumer(const typename P::Params &p, uint8_t *smem, int un
                             umma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
                     }
                     if (PAIR)
-                        umma_commit_pair(&ps->empty[stage]);
+                        umma_commit_pair_mask(&ps->empty[stage], empty_mask);
                     else
                         umma_commit(&ps->empty[stage]);
                     ps->consumed += 1;
@@ -250,7 +268,7 @@ __device__ void gemm_consumer(const typename P::Params &p, uint8_t *smem, int un
                 if (!ok)
                     break;
                 if (PAIR)
-                    umma_commit_pair(&ps->tfull[acc]);
+                    umma_commit_pair_mask(&ps->tfull[acc], pair_mask);
                 else
                     umma_commit(&ps->tfull[acc]);
                 if (++acc == 2) {
@@ -261,7 +279,7 @@ __device__ void gemm_consumer(const typename P::Params &p, uint8_t *smem, int un
             if (ps->abort) {
                 // let every MMA this thread issued finish before TMEM is freed
                 if (PAIR)
-                    umma_commit_pair(&ps->drain);
+                    umma_commit_pair_mask(&ps->drain, pair_mask);
                 else
                     umma_commit(&ps->drain);
                 (void)mbar_wait(&ps->drain, 0, tmo);
@@ -277,7 +295,7 @@ __device__ void gemm_consumer(const typename P::Params &p, uint8_t *smem, int un
         int buf = 0;
         for (int64_t it = unit; it < items; it += nunits) {
             TileInfo ti;
-            P::tile(p, it, ti, half);
+            P::tile(p, it, ti, crank);
             if (ti.n_valid <= 0)
                 continue;
             bool ok = mbar_wait(&ps->tfull[acc], acc_phase, tmo);
@@ -349,7 +367,7 @@ __device__ void gemm_consumer(const typename P::Params &p, uint8_t *smem, int un
     }
     __syncthreads();
     if (PAIR)
-        cluster_sync(); // neither CTA leaves while the other may still touch it
+        cluster_sync(); // no CTA leaves while another may still touch it
     if (warp == 1) {
         tc_fence_after();
         if (PAIR)

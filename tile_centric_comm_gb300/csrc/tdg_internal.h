@@ -70,11 +70,20 @@ cudaError_t launch(const void *fn, dim3 grid, dim3 block, size_t smem, cudaStrea
 
 // Number of 2-CTA clusters of `fn` that can be resident at once (0 on error).
 int max_pairs(const void *fn, int block, int smem);
+// Number of `cl`-CTA clusters of `fn` that can be resident at once (0 on error).
+int max_clusters(const void *fn, int block, int smem, int cl);
 
 // CTA pairs (cta_group::2) unless TDG_PAIR=0 is set in the environment.
 inline bool pairs_enabled()
 {
     const char *e = getenv("TDG_PAIR");
+    return !(e && e[0] == '0');
+}
+
+// Clusters of two CTA pairs sharing B by multicast, unless TDG_QUAD=0.
+inline bool quads_enabled()
+{
+    const char *e = getenv("TDG_QUAD");
     return !(e && e[0] == '0');
 }
 

@@ -455,14 +455,43 @@ __device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, 
         : "memory");
 }
 
-// arrive on the mbarrier at this shared offset in both CTAs of the pair once
-// every tcgen05 operation issued so far by this thread has completed
-__device__ __forceinline__ void umma_commit_pair(uint64_t *bar)
+// arrive on the mbarrier at this shared offset in every CTA of `mask` (bit i:
+// cluster rank i) once every tcgen05 operation issued so far by this thread
+// has completed
+__device__ __forceinline__ void umma_commit_pair_mask(uint64_t *bar, uint16_t mask)
 {
     asm volatile(
         "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
         " [%0], %1;" ::"r"(smem_u32(bar)),
-        "h"((uint16_t)3)
+        "h"(mask)
+        : "memory");
+}
+
+// the same, on both CTAs of the pair formed by cluster ranks 0 and 1
+__device__ __forceinline__ void umma_commit_pair(uint64_t *bar) { umma_commit_pair_mask(bar, 3); }
+
+// Pair TMA loads multicast to the CTAs of `mask`: the tile lands at the same
+// shared offset in every destination CTA, and each destination's bytes are
+// counted on the barrier at `bar_cluster`'s offset in the leader (even rank)
+// of that destination's pair (bar_cluster names a leader's barrier).
+__device__ __forceinline__ void tma_load_2d_pair_mc(void *smem_dst, const CUtensorMap *map,
+                                                    uint32_t bar_cluster, int x, int y, uint16_t mask)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(smem_dst)),
+        "l"(map), "r"(bar_cluster), "r"(x), "r"(y), "h"(mask)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d_pair_mc(void *smem_dst, const CUtensorMap *map,
+                                                    uint32_t bar_cluster, int x, int y, int z,
+                                                    uint16_t mask)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        ".multicast::cluster [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(smem_dst)),
+        "l"(map), "r"(bar_cluster), "r"(x), "r"(y), "r"(z), "h"(mask)
         : "memory");
 }
 

@@ -35,8 +35,9 @@ struct RsParams {
     int W;
     int64_t M, K, N, Mo;
     int mt;      // 128-row tiles per owner (Mo / 128): the staging layout
-    int mtp;     // scheduled tiles per owner (Mo / 128, or Mo / 256 with pairs)
-    int pair;    // 1: CTA pairs (cta_group::2) with 256-row tiles
+    int mtp;     // scheduled tiles per owner (Mo / (128 * cl))
+    int pair;    // 1: CTA pairs (cta_group::2)
+    int cl;      // CTAs per cluster (1, 2 or 4): tiles of 128 * cl rows
     int n_tiles;
     int order;   // 0: owner blocks of `ob` owners, then rank, owner, m, n; 1: rank fastest
     int ob;      // owners per block in order 0 (1 = owner by owner, W = rank-major)
@@ -121,7 +122,7 @@ template <int BMN> struct RsPolicy {
         return (int64_t)p.W * p.W * p.mtp * p.n_tiles;
     }
 
-    __device__ static void tile(const Params &p, int64_t item, TileInfo &t, int half)
+    __device__ static void tile(const Params &p, int64_t item, TileInfo &t, int sub)
     {
         const int64_t per_rank = (int64_t)p.mtp * p.n_tiles;
         int o, r;
@@ -145,7 +146,7 @@ template <int BMN> struct RsPolicy {
         }
         t.owner = o;
         t.a_sel = r;
-        t.m_loc = (int)(rem / p.n_tiles) * (p.pair ? 2 : 1) + half; // 128-row tile in the owner
+        t.m_loc = (int)(rem / p.n_tiles) * p.cl + sub; // 128-row tile in the owner
         t.pn = (int)(rem % p.n_tiles);
         t.m0 = (o * p.mt + t.m_loc) * gm::BM;
         t.a_row = t.m0;
@@ -159,32 +160,45 @@ template <int BMN> struct RsPolicy {
 
     // The TMA form is chosen at compile time: a kernel holds either only
     // cta_group::1 or only cta_group::2 instructions, never both.
-    template <int PAIR>
+    template <int CL>
     __device__ static void load(void *dst, const CUtensorMap *m, uint32_t bar, int x, int y, int z)
     {
-        if constexpr (PAIR)
+        if constexpr (CL >= 2)
             tma_load_3d_pair(dst, m, bar, x, y, z);
         else
             tma_load_3d_addr(dst, m, bar, x, y, z);
     }
 
-    template <int PAIR>
+    template <int CL>
     __device__ static void load_a(const Params &p, const TileInfo &t, void *dst, uint32_t bar, int kb)
     {
-        load<PAIR>(dst, &p.tmA, bar, kb * gm::BK, t.a_row, t.a_sel);
+        load<CL>(dst, &p.tmA, bar, kb * gm::BK, t.a_row, t.a_sel);
     }
 
-    template <int PAIR>
+    // B slices of 64 columns (8 KB): MN-major boxes {64 cols, 64 K}; K-major
+    // boxes {64 K, 64 rows} with CL = 4, else one box of all the columns.
+    // With CL = 4 pair `pidx` fetches slices pidx, pidx + 2, ... and
+    // multicasts each to CTA `half` of both pairs.
+    template <int CL>
     __device__ static void load_b(const Params &p, const TileInfo &t, void *dst, uint32_t bar, int kb,
-                                  int col0, int cols)
+                                  int col0, int cols, int pidx, int half)
     {
-        if (BMN) {
+        uint8_t *d = static_cast<uint8_t *>(dst);
+        if constexpr (CL == 4) {
+            const uint16_t mask = (uint16_t)((1u << half) | (1u << (2 + half)));
+            const int nch = BMN ? (cols + 63) >> 6 : 2;
+            for (int j = pidx; j < nch; j += 2) {
+                if (BMN)
+                    tma_load_3d_pair_mc(d + j * 8192, &p.tmB, bar, col0 + 64 * j, kb * gm::BK, t.a_sel, mask);
+                else
+                    tma_load_3d_pair_mc(d + j * 8192, &p.tmB, bar, kb * gm::BK, col0 + 64 * j, t.a_sel, mask);
+            }
+        } else if (BMN) {
             const int nch = (cols + 63) >> 6;
             for (int j = 0; j < nch; ++j)
-                load<PAIR>(static_cast<uint8_t *>(dst) + j * 8192, &p.tmB, bar, col0 + 64 * j, kb * gm::BK,
-                           t.a_sel);
+                load<CL>(d + j * 8192, &p.tmB, bar, col0 + 64 * j, kb * gm::BK, t.a_sel);
         } else {
-            load<PAIR>(dst, &p.tmB, bar, kb * gm::BK, col0, t.a_sel);
+            load<CL>(dst, &p.tmB, bar, kb * gm::BK, col0, t.a_sel);
         }
     }
 
@@ -223,15 +237,12 @@ template <int BMN> struct RsPolicy {
     }
 };
 
-template <int BMN, int PAIR>
+template <int BMN, int CL>
 __global__ void __launch_bounds__(gm::NUM_THREADS, 1) rs_gemm_kernel(const __grid_constant__ RsParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
-    if (PAIR)
-        gemm_consumer<RsPolicy<BMN>, 1>(p, smem, (int)blockIdx.x >> 1, (int)gridDim.x >> 1);
-    else
-        gemm_consumer<RsPolicy<BMN>, 0>(p, smem, (int)blockIdx.x, (int)gridDim.x);
+    gemm_consumer<RsPolicy<BMN>, CL>(p, smem, (int)blockIdx.x / CL, (int)gridDim.x / CL);
 }
 
 // SERIAL reduction: one 4-warp CTA per output tile.
@@ -301,14 +312,18 @@ extern "C" int tdg_gemm_rs(tdg_symm *h, const tdg_gemm_rs_args *a, void *stream)
         return TDG_OK;
     }
 
+    // CTA pairs when every owner holds whole 256-row tiles; two pairs sharing
+    // B when it holds whole 512-row tiles
     const int pair = (pairs_enabled() && Mo % (2 * gm::BM) == 0) ? 1 : 0;
+    const int cl = pair ? ((quads_enabled() && Mo % (4 * gm::BM) == 0) ? 4 : 2) : 1;
     RsParams p;
     memset(&p, 0, sizeof p);
     bool ok = map_bf16_3d(&p.tmA, h->base + a->a_off, K, M, W, K * 2, R, 64, gm::BM, 1);
     if (a->b_layout == TDG_B_KN)
         ok = ok && map_bf16_3d(&p.tmB, h->base + a->b_off, N, K, W, N * 2, R, 64, 64, 1);
     else
-        ok = ok && map_bf16_3d(&p.tmB, h->base + a->b_off, K, N, W, K * 2, R, 64, pair ? 128 : 256, 1);
+        ok = ok && map_bf16_3d(&p.tmB, h->base + a->b_off, K, N, W, K * 2, R, 64,
+                               cl == 4 ? 64 : (pair ? 128 : 256), 1);
     const uint64_t rows_per_owner = (uint64_t)W * mt * n_tiles * gm::BM;
     ok = ok && map_bf16_3d(&p.tmS, h->base + a->stage_off, gm::BN, rows_per_owner, W, gm::BN * 2, R, 64, 32, 1);
     if (!ok)
@@ -325,7 +340,8 @@ extern "C" int tdg_gemm_rs(tdg_symm *h, const tdg_gemm_rs_args *a, void *stream)
     p.Mo = Mo;
     p.mt = mt;
     p.pair = pair;
-    p.mtp = pair ? mt / 2 : mt;
+    p.cl = cl;
+    p.mtp = mt / cl;
     p.n_tiles = n_tiles;
     p.order = getenv("TDG_RS_ORDER") ? atoi(getenv("TDG_RS_ORDER")) : 0;
     // two owners per block measured best at the Qwen-32B down-projection shape
@@ -343,13 +359,15 @@ extern "C" int tdg_gemm_rs(tdg_symm *h, const tdg_gemm_rs_args *a, void *stream)
 
     const void *fn;
     if (a->b_layout == TDG_B_KN)
-        fn = pair ? reinterpret_cast<const void *>(&rs_gemm_kernel<1, 1>)
-                  : reinterpret_cast<const void *>(&rs_gemm_kernel<1, 0>);
+        fn = cl == 4   ? reinterpret_cast<const void *>(&rs_gemm_kernel<1, 4>)
+             : cl == 2 ? reinterpret_cast<const void *>(&rs_gemm_kernel<1, 2>)
+                       : reinterpret_cast<const void *>(&rs_gemm_kernel<1, 1>);
     else
-        fn = pair ? reinterpret_cast<const void *>(&rs_gemm_kernel<0, 1>)
-                  : reinterpret_cast<const void *>(&rs_gemm_kernel<0, 0>);
-    static bool smem_set[2][2][64] = {};
-    bool &done = smem_set[a->b_layout & 1][pair][h->device & 63];
+        fn = cl == 4   ? reinterpret_cast<const void *>(&rs_gemm_kernel<0, 4>)
+             : cl == 2 ? reinterpret_cast<const void *>(&rs_gemm_kernel<0, 2>)
+                       : reinterpret_cast<const void *>(&rs_gemm_kernel<0, 1>);
+    static bool smem_set[2][3][64] = {};
+    bool &done = smem_set[a->b_layout & 1][cl >> 1][h->device & 63];
     if (!done) {
         cudaError_t e = set_smem(fn, gm::SMEM_BYTES);
         if (e != cudaSuccess)
@@ -357,16 +375,15 @@ extern "C" int tdg_gemm_rs(tdg_symm *h, const tdg_gemm_rs_args *a, void *stream)
         done = true;
     }
     int grid = h->sm_count;
-    if (pair) {
-        const int mp = max_pairs(fn, gm::NUM_THREADS, gm::SMEM_BYTES);
-        const int pairs = mp < h->sm_count / 2 ? mp : h->sm_count / 2;
-        if (pairs <= 0)
+    if (cl > 1) {
+        const int mc = max_clusters(fn, gm::NUM_THREADS, gm::SMEM_BYTES, cl);
+        const int n = mc < h->sm_count / cl ? mc : h->sm_count / cl;
+        if (n <= 0)
             return TDG_ERR_UNSUPPORTED;
-        grid = 2 * pairs;
+        grid = cl * n;
     }
     void *args[] = {&p};
-    int rc = cuda_err(launch(fn, dim3(grid), dim3(gm::NUM_THREADS), gm::SMEM_BYTES, s, args, false,
-                             pair ? 2 : 1),
+    int rc = cuda_err(launch(fn, dim3(grid), dim3(gm::NUM_THREADS), gm::SMEM_BYTES, s, args, false, cl),
                       "rs gemm launch");
     if (rc != TDG_OK || a->mode == TDG_MODE_SM)
         return rc;
