@@ -45,7 +45,7 @@ WORKLOAD = ("qwen32b_mlp_tp8: AG-GEMM up-proj (W=8, A_r 1024x5120, B 5120x3200) 
 # DRAM traffic of one rs_gemm_kernel launch at this workload, dram__bytes_read.sum +
 # dram__bytes_write.sum from one ncu capture (2.541 GB read + 0.742 GB written).  It is
 # reported only while the kernel's sources still hash to the value the capture was taken with.
-RS_TRAFFIC = {"sources": "0f3af002ae3df248", "bytes": 2_591_494_656 + 743_805_184}
+RS_TRAFFIC = {"sources": "b248b4d0144f1b6f", "bytes": 2_549_831_936 + 743_203_584}
 RS_SOURCES = ["tdg_gemm.cuh", "tdg_rs.cu", "tdg_ptx.cuh"]
 
 
@@ -73,8 +73,9 @@ def parse():
     ap.add_argument("--no-extras", action="store_true", help="skip serial/e2e/MoE/CPU legs")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--only", default="", help="measure one operation alone, not the bench line: "
-                    "ag, rs, moe, ring or flash")
-    ap.add_argument("--ag-shape", default="", help="W,Ms,K,N for --only ag, e.g. 8,2048,8192,7168 "
+                    "ag, rs, moe, ring or flash; 'library' times torch.matmul (cuBLAS) on the AG "
+                    "GEMM shape as context")
+    ap.add_argument("--ag-shape", default="", help="W,Ms,K,N for --only ag|library, e.g. 8,2048,8192,7168 "
                     "(the Llama-3-70B gate+up shape)")
     return ap.parse_args()
 
@@ -547,8 +548,8 @@ def main():
     args = parse()
     rank, world, local = dist_env()
     if args.ag_shape:
-        if args.only != "ag":
-            raise SystemExit("--ag-shape needs --only ag")
+        if args.only not in ("ag", "library"):
+            raise SystemExit("--ag-shape needs --only ag or --only library")
         W, Ms, K, N = (int(x) for x in args.ag_shape.split(","))
         AG.update(W=W, Ms=Ms, K=K, N=N)
     if args.impl == "reference":
@@ -567,6 +568,21 @@ def main():
         raise SystemExit("libtdg kernels need an sm_103 device")
     pk = peaks()
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.int32, device="cuda")
+    if args.only == "library":
+        # context only, not part of the path: the library GEMM on the gathered shape
+        M, K, N = AG["W"] * AG["Ms"], AG["K"], AG["N"]
+        torch.manual_seed(0)
+        a = torch.randn(M, K, device="cuda").to(torch.bfloat16)
+        b = (torch.randn(K, N, device="cuda") * 0.02).to(torch.bfloat16)
+        c = torch.empty(M, N, device="cuda", dtype=torch.bfloat16)
+        with Clocks(local) as clk:
+            lp = timed_steps(torch, [lambda: torch.matmul(a, b, out=c)], args.steps, args.warmup, flush)
+        ms = statistics.mean(lp[0])
+        if rank == 0:
+            print(json.dumps({"metric": "library GEMM TFLOP/s (context)", "value": 2 * M * K * N / ms / 1e9,
+                              "unit": "TFLOP/s", "ms": ms, "shape": [M, K, N], "steps": args.steps,
+                              "warmup": args.warmup, "clocks": clk.summary()}), flush=True)
+        return
     if args.only in ("moe", "ring", "flash"):
         leg = {"moe": leg_moe, "ring": leg_ring, "flash": leg_flash}[args.only]
         with Clocks(local) as clk:

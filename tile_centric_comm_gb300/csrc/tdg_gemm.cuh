@@ -180,6 +180,7 @@ __device__ void gemm_consumer(const typename P::Params &p, uint8_t *smem, int un
             int stage = 0;
             uint32_t phase = 0;
             bool gave_up = false;
+            uint32_t issued = 0; // kept in a register; published once for the abort drain
             for (int64_t it = unit; it < items && !ps->abort; it += nunits) {
                 TileInfo ti;
                 P::tile(p, it, ti, crank);
@@ -202,13 +203,14 @@ __device__ void gemm_consumer(const typename P::Params &p, uint8_t *smem, int un
                     const uint32_t bar = full0 + stage * 8;
                     P::template load_a<CL>(p, ti, sa, bar, kb);
                     P::template load_b<CL>(p, ti, sa + A_BYTES, bar, kb, col0, cols, pidx, half);
-                    ps->issued += 1;
+                    ++issued;
                     if (++stage == S::STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
             }
+            ps->issued = issued;
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -217,6 +219,7 @@ __device__ void gemm_consumer(const typename P::Params &p, uint8_t *smem, int un
             uint32_t phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
+            uint32_t consumed = 0; // kept in a register; published once for the abort drain
             const uint32_t sbase = smem_u32(smem);
             for (int64_t it = unit; it < items && !ps->abort; it += nunits) {
                 TileInfo ti;
@@ -242,14 +245,17 @@ __device__ void gemm_consumer(const typename P::Params &p, uint8_t *smem, int un
                     tc_fence_after();
                     const uint32_t a_addr = sbase + stage * S::STAGE_BYTES;
                     const uint32_t b_addr = a_addr + A_BYTES;
+                    // MN-major B: 64-column chunks 8 KB apart (LBO), 8 K-rows 1 KB
+                    // apart (SBO); a K step of 16 rows is 2 KB.  K-major B: same
+                    // form as A (a K step of 16 elements is 32 bytes).  The start
+                    // address field counts 16-byte units in the descriptor's low
+                    // bits, so the K steps are added to the stage's descriptors.
+                    const uint64_t ad0 = sdesc_sw128(a_addr, 16, 1024);
+                    const uint64_t bd0 = P::B_MN ? sdesc_sw128(b_addr, 8192, 1024) : sdesc_sw128(b_addr, 16, 1024);
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k) {
-                        const uint64_t ad = sdesc_sw128(a_addr + k * 32, 16, 1024);
-                        // MN-major B: 64-column chunks 8 KB apart (LBO), 8 K-rows
-                        // 1 KB apart (SBO); a K step of 16 rows is 2 KB.
-                        // K-major B: same form as A.
-                        const uint64_t bd = P::B_MN ? sdesc_sw128(b_addr + k * 2048, 8192, 1024)
-                                                    : sdesc_sw128(b_addr + k * 32, 16, 1024);
+                        const uint64_t ad = ad0 + (uint64_t)(k * 2);
+                        const uint64_t bd = bd0 + (uint64_t)(P::B_MN ? k * 128 : k * 2);
                         if (PAIR)
                             umma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
                         else
@@ -259,7 +265,7 @@ __device__ void gemm_consumer(const typename P::Params &p, uint8_t *smem, int un
                         umma_commit_pair_mask(&ps->empty[stage], empty_mask);
                     else
                         umma_commit(&ps->empty[stage]);
-                    ps->consumed += 1;
+                    ++consumed;
                     if (++stage == S::STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -276,6 +282,7 @@ __device__ void gemm_consumer(const typename P::Params &p, uint8_t *smem, int un
                     acc_phase ^= 1u;
                 }
             }
+            ps->consumed = consumed;
             if (ps->abort) {
                 // let every MMA this thread issued finish before TMEM is freed
                 if (PAIR)
@@ -298,7 +305,12 @@ __device__ void gemm_consumer(const typename P::Params &p, uint8_t *smem, int un
             P::tile(p, it, ti, crank);
             if (ti.n_valid <= 0)
                 continue;
-            bool ok = mbar_wait(&ps->tfull[acc], acc_phase, tmo);
+            // one lane polls the barrier; the warp follows it (fewer shared
+            // memory probes while the mainloop runs)
+            bool ok = true;
+            if (lane == 0)
+                ok = mbar_wait(&ps->tfull[acc], acc_phase, tmo);
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
             if (!ok || ps->abort) {
                 if (lane == 0 && !ok)
                     report_fault(p.status, TDG_ERR_TIMEOUT, TDG_WHERE_PIPE, 3, p.epoch);
