@@ -515,6 +515,41 @@ def leg_ring(torch, tdg, synth, args, flush, pk):
     return extras["ring_allreduce"]
 
 
+def leg_ag_config(torch, tdg, synth, args, flush, pk, W, Ms, K, N, dist, workload, modes=("ce", "sm")):
+    """One AllGather+GEMM config on its own: each overlapped mode against the
+    serial twin (copy launch, then GEMM launch), TFLOP/s and fraction of the
+    measured bf16 peak."""
+    inp = synth.ag_inputs(W, Ms, K, N, dist, seed=0)
+    g_off = _align(Ms * K * 2)
+    sym = tdg.Symm(W, _align(g_off + W * Ms * K * 2 + 1024), 65536)
+    for r in range(W):
+        sym.view(r, 0, (Ms, K), torch.bfloat16).copy_(_dev_bf16(inp.shards[r], torch))
+    B = _dev_bf16(inp.B, torch)
+    C = torch.empty((W * Ms, N), dtype=torch.bfloat16, device="cuda")
+    del inp
+    side = torch.cuda.Stream()
+    flop = 2 * W * Ms * K * N
+
+    def call(mode):
+        return lambda: tdg.ag_gemm(sym, 0, Ms, K, N, 0, g_off, B, C, mode=mode,
+                                   side_stream=side if mode == "ce" else None)
+    res = {"workload": workload}
+    times = {}
+    for mode in ("serial",) + tuple(modes):
+        times[mode] = statistics.mean(timed_steps(torch, [call(mode)], args.steps, args.warmup, flush)[0])
+        res[f"{mode}_ms"] = times[mode]
+        res[f"{mode}_tflops"] = flop / times[mode] / 1e9
+        res[f"{mode}_frac_of_bf16_peak"] = flop / times[mode] / 1e9 / pk["bf16"]
+        if mode != "serial":
+            res[f"{mode}_overlap_gain_vs_serial"] = times["serial"] / times[mode]
+    st = sym.status()
+    if st["code"] != 0:
+        raise RuntimeError(f"device fault in {workload}: {st}")
+    del sym, B, C
+    torch.cuda.empty_cache()
+    return res
+
+
 def leg_flash(torch, tdg, synth, args, flush, pk):
     extras = {}
     # distributed flash decoding: 4 sequences x 64 heads (8 kv heads, d 128),
@@ -683,6 +718,12 @@ def main():
             "ag_shape_tflops": AG_FLOP / l_ag / 1e9, "rs_shapes_tflops": RS_FLOP / l_rs / 1e9}
         del mlp, a_cat, b_rs, a_rs, c_rs
         torch.cuda.empty_cache()
+        extras["ag_llama70b_gateup"] = leg_ag_config(
+            torch, tdg, synth, args, flush, pk, 8, 2048, 8192, 7168, "normal",
+            "AG-GEMM Llama-3-70B gate+up: W=8, A_r 2048x8192, B 8192x7168")
+        extras["ag_tiny"] = leg_ag_config(
+            torch, tdg, synth, args, flush, pk, 2, 64, 256, 128, "int2",
+            "AG-GEMM tiny: W=2, A_r 64x256, B 256x128, integers (latency bound)")
         extras["moe_dispatch_combine"] = leg_moe(torch, tdg, synth, args, flush, pk)
         extras["ring_allreduce"] = leg_ring(torch, tdg, synth, args, flush, pk)
         extras["flash_decode"] = leg_flash(torch, tdg, synth, args, flush, pk)
