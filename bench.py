@@ -522,7 +522,9 @@ def leg_ag_config(torch, tdg, synth, args, flush, pk, W, Ms, K, N, dist, workloa
     measured bf16 peak."""
     inp = synth.ag_inputs(W, Ms, K, N, dist, seed=0)
     g_off = _align(Ms * K * 2)
-    sym = tdg.Symm(W, _align(g_off + W * Ms * K * 2 + 1024), 65536)
+    ll_off = _align(g_off + W * Ms * K * 2)    # LL words: 4 bytes per element
+    ll_bytes = W * Ms * K * 4 if "ll" in modes else 0
+    sym = tdg.Symm(W, _align(ll_off + ll_bytes + 1024), 65536)
     for r in range(W):
         sym.view(r, 0, (Ms, K), torch.bfloat16).copy_(_dev_bf16(inp.shards[r], torch))
     B = _dev_bf16(inp.B, torch)
@@ -532,7 +534,7 @@ def leg_ag_config(torch, tdg, synth, args, flush, pk, W, Ms, K, N, dist, workloa
     flop = 2 * W * Ms * K * N
 
     def call(mode):
-        return lambda: tdg.ag_gemm(sym, 0, Ms, K, N, 0, g_off, B, C, mode=mode,
+        return lambda: tdg.ag_gemm(sym, 0, Ms, K, N, 0, g_off, B, C, mode=mode, ll_off=ll_off,
                                    side_stream=side if mode == "ce" else None)
     res = {"workload": workload}
     times = {}
@@ -724,7 +726,7 @@ def main():
             "AG-GEMM Llama-3-70B gate+up: W=8, A_r 2048x8192, B 8192x7168")
         extras["ag_tiny"] = leg_ag_config(
             torch, tdg, synth, args, flush, pk, 2, 64, 256, 128, "int2",
-            "AG-GEMM tiny: W=2, A_r 64x256, B 256x128, integers (latency bound)")
+            "AG-GEMM tiny: W=2, A_r 64x256, B 256x128, integers (latency bound)", modes=("ce", "sm", "ll"))
         extras["moe_dispatch_combine"] = leg_moe(torch, tdg, synth, args, flush, pk)
         extras["ring_allreduce"] = leg_ring(torch, tdg, synth, args, flush, pk)
         extras["flash_decode"] = leg_flash(torch, tdg, synth, args, flush, pk)

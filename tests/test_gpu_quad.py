@@ -74,3 +74,21 @@ def test_rs_float_parity_and_same_bits_as_pairs(b_layout, monkeypatch):
         assert_close(got, out64)
         outs[quad] = got
     assert np.array_equal(outs["1"], outs["0"])
+
+
+@pytest.mark.parametrize("mode", ["sm", "ce"])
+def test_ag_missing_signal_times_out_then_next_call_succeeds(mode):
+    # two-pair clusters (Ms = 512): one signal group of shard 1 is never set
+    # (host-side injection), so the bounded wait of the CTAs that read those
+    # rows runs out; the call reports TIMEOUT with the group index and the
+    # next call (new epoch) gives the exact result
+    inp = synth.ag_inputs(2, 512, 128, 512, "int2", seed=5)
+    _, C16 = oracle.ag_gemm(inp.shards, inp.B)
+    case = AGCase(inp)
+    sig = 32 if mode == "sm" else 512
+    g = 512 // sig + 1 if mode == "sm" else 1   # a group of shard 1 (remote for rank 0)
+    _, st = case.run(rank=0, mode=mode, signal_rows=sig, test_skip_notify=1 << g,
+                     timeout_ns=20_000_000, check_status=False)
+    assert st["code"] == tdg.TDG_ERR_TIMEOUT and st["where"] == "ag_flag" and st["index"] == g
+    got, st = case.run(rank=0, mode=mode, signal_rows=sig)
+    assert st["code"] == 0 and np.array_equal(got, C16)
