@@ -108,7 +108,10 @@ TDG_API void *tdg_symm_at(const tdg_symm *h, const void *local_ptr, int rank);
 TDG_API uint32_t *tdg_symm_flags(const tdg_symm *h, int rank);
 TDG_API uint32_t *tdg_symm_counters(const tdg_symm *h, int rank);
 
-/* The epoch the next call will use (flags compare against it; never 0). */
+/* The epoch the next call will take when no other call comes first.  Epochs
+ * come from one counter shared by every handle of the process, in [1, 2^31),
+ * so no two calls share one: flags compare against it, and words that an
+ * earlier call left in memory never carry a later call's epoch. */
 TDG_API uint32_t tdg_symm_epoch(const tdg_symm *h);
 
 /* ---- device status ------------------------------------------------------- */
@@ -175,7 +178,11 @@ typedef struct {
     int64_t signal_rows; /* rows per signal; 0 = BM if Ms % BM == 0, else Ms */
     int swizzle;         /* 1 = rank-swizzled tile order, 0 = linear        */
     uint64_t timeout_ns; /* bound of every device wait; 0 = 2 s             */
-    size_t ll_off;       /* LL mode: LL buffer (M*K*4 bytes) in region(rank) */
+    size_t ll_off;       /* LL mode: LL buffer (M*K*4 bytes) in region(rank);
+                          * a word counts as delivered when its upper half is
+                          * the call's epoch, so memory that last held
+                          * anything but this process's LL words must be
+                          * zeroed once before its first LL call               */
     uint64_t test_skip_notify; /* tests only: producers skip the notify of
                                   signal groups whose bit (g % 64) is set   */
     int source_order;    /* 0: one source at a time, rank+1, rank+2, ... (the

@@ -183,3 +183,34 @@ def test_full_size_sampled(name):
         _gathered_ok(case, 3)
     del case
     torch.cuda.empty_cache()
+
+
+def test_ll_second_heap_on_the_same_memory():
+    # a heap laid over memory that an earlier heap's LL call filled with words:
+    # the new call's epoch differs from every earlier call's, so no stale word
+    # counts as delivered and the result is exact for the new inputs
+    first = synth.ag_inputs(2, 256, 64, 128, "int2", seed=21)
+    second = synth.ag_inputs(2, 256, 64, 128, "int2", seed=22)
+    case = AGCase(first, ll=True)
+    _, C1 = oracle.ag_gemm(first.shards, first.B)
+    for _ in range(3):
+        got, _ = case.run(rank=1, mode="ll", ll_off=case.ll_off)
+        assert np.array_equal(got, C1)
+    buf, region, nsig = case.symm.buf, case.symm.region_bytes, case.symm.nsig
+    case.symm.close()
+    again = AGCase.__new__(AGCase)
+    again.__dict__.update(case.__dict__)
+    again.inp = second
+    again.symm = tdg.Symm(2, region, nsig, buffer=buf)   # same memory, new handle
+    for s in range(2):
+        again.symm.view(s, again.a_off, (second.Ms, second.K), torch.bfloat16).copy_(
+            torch.from_numpy(second.shards[s].view(np.int16)).view(torch.bfloat16).cuda())
+    again.B = torch.from_numpy(second.B.view(np.int16)).view(torch.bfloat16).cuda()
+    _, C2 = oracle.ag_gemm(second.shards, second.B)
+    # two calls of another mode first: with epochs counted per handle, the LL
+    # call below would take the epoch of the stale words (the third call)
+    for _ in range(2):
+        got, _ = again.run(rank=1, mode="sm")
+        assert np.array_equal(got, C2)
+    got, _ = again.run(rank=1, mode="ll", ll_off=again.ll_off)
+    assert np.array_equal(got, C2)

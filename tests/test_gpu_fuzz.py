@@ -1,0 +1,69 @@
+"""Seeded random shapes through the C ABI, bit-exact against the oracle on
+integer inputs: W from 1 to 8, shards and owners that select every GEMM shape
+(one CTA, CTA pairs, two-pair clusters), ragged K and N tails, both B layouts,
+every mode."""
+import numpy as np
+import pytest
+
+import oracle
+from tile_centric_comm_gb300 import synth, tdg
+from gpu_util import AGCase, RSCase, to_bits
+
+pytestmark = pytest.mark.gpu
+
+
+def _ag_cases(n=16, seed=2024):
+    g = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        W = int(g.choice([1, 2, 3, 4, 8]))
+        Ms = int(g.choice([64, 128, 192, 256, 512, 1024]))
+        if W * Ms > 4096:
+            Ms = 512
+        K = int(g.choice([8, 64, 136, 256]))
+        N = int(g.choice([8, 72, 264, 520, 776]))
+        lay = int(g.integers(0, 2))
+        out.append((W, Ms, K, N, lay, 1000 + i))
+    return out
+
+
+def _rs_cases(n=12, seed=2025):
+    g = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        W = int(g.choice([1, 2, 4, 8]))
+        Mo = int(g.choice([128, 256, 512, 1024]))
+        if W * Mo > 4096:
+            Mo = 512
+        K = int(g.choice([8, 32, 64]))   # |partial| <= 4K <= 256: exact in bf16
+        N = int(g.choice([8, 264, 520, 1032]))
+        lay = int(g.integers(0, 2))
+        out.append((W, W * Mo, K, N, lay, 2000 + i))
+    return out
+
+
+@pytest.mark.parametrize("W,Ms,K,N,lay,seed", _ag_cases())
+def test_ag_random_shapes_bit_exact(W, Ms, K, N, lay, seed):
+    inp = synth.ag_inputs(W, Ms, K, N, "int2", seed=seed)
+    _, C16 = oracle.ag_gemm(inp.shards, inp.B)
+    b_layout = tdg.B_KN if lay == 0 else tdg.B_NK
+    case = AGCase(inp, b_layout=b_layout, ll=(W * Ms * K <= 1 << 20))
+    rank = seed % W
+    modes = ["sm", "ce", "serial"] + (["ll"] if W * Ms * K <= 1 << 20 else [])
+    for mode in modes:
+        kw = {"ll_off": case.ll_off} if mode == "ll" else {}
+        got, _ = case.run(rank=rank, mode=mode, **kw)
+        assert np.array_equal(got, C16), (mode, rank)
+        assert np.array_equal(to_bits(case.gathered(rank)), np.concatenate(inp.shards)), (mode, "gathered")
+
+
+@pytest.mark.parametrize("W,M,K,N,lay,seed", _rs_cases())
+def test_rs_random_shapes_bit_exact(W, M, K, N, lay, seed):
+    inp = synth.rs_inputs(W, M, K, N, "int2", seed=seed)
+    _, out16 = oracle.gemm_rs(inp.As, inp.Bs)
+    b_layout = tdg.B_KN if lay == 0 else tdg.B_NK
+    case = RSCase(inp, b_layout=b_layout)
+    for mode in ("sm", "serial", "sm"):
+        got, _ = case.run(mode=mode)
+        assert np.array_equal(got, out16), mode
+

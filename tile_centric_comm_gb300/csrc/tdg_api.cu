@@ -9,6 +9,8 @@
 #include <new>
 #include <string.h>
 
+#include <atomic>
+
 #include "tdg_internal.h"
 
 using namespace tdg_host;
@@ -121,6 +123,23 @@ cudaError_t launch(const void *fn, dim3 grid, dim3 block, size_t smem, cudaStrea
     cfg.numAttrs = n;
     return cudaLaunchKernelExC(&cfg, fn, args);
 }
+
+namespace {
+std::atomic<uint32_t> g_epoch{0};
+constexpr uint32_t EPOCH_LIMIT = 0x7FFFFFFFu;
+uint32_t epoch_after(uint32_t e) { return e >= EPOCH_LIMIT ? 1u : e + 1u; }
+} // namespace
+
+uint32_t next_epoch(tdg_symm *h)
+{
+    uint32_t cur = g_epoch.load(std::memory_order_relaxed);
+    while (!g_epoch.compare_exchange_weak(cur, epoch_after(cur), std::memory_order_relaxed)) {
+    }
+    h->epoch = epoch_after(cur);
+    return h->epoch;
+}
+
+uint32_t peek_epoch() { return epoch_after(g_epoch.load(std::memory_order_relaxed)); }
 
 int max_pairs(const void *fn, int block, int smem) { return max_clusters(fn, block, smem, 2); }
 
@@ -243,8 +262,7 @@ uint32_t tdg_symm_epoch(const tdg_symm *h)
 {
     if (!h)
         return 0;
-    uint32_t e = h->epoch + 1;
-    return e ? e : 1;
+    return tdg_host::peek_epoch();
 }
 
 int tdg_status(tdg_symm *h, void *stream, tdg_fault *out, int clear)

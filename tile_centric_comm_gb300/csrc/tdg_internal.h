@@ -30,14 +30,14 @@ namespace tdg_host {
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// next nonzero epoch of the handle
-inline uint32_t next_epoch(tdg_symm *h)
-{
-    h->epoch += 1;
-    if (h->epoch == 0)
-        h->epoch = 1;
-    return h->epoch;
-}
+// The epoch of a new call: one counter for every handle of the process, so no
+// two calls share an epoch.  Words that a call leaves in memory (LL words in a
+// caller's region, which a later heap over the same memory may not clear) can
+// then never carry a later call's epoch.  Epochs stay below 2^31, where a
+// zeroed flag compares as not yet reached.
+uint32_t next_epoch(tdg_symm *h);
+// The epoch the next call will take (when no other call comes first).
+uint32_t peek_epoch();
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline bool aligned16(size_t v) { return (v & 15u) == 0; }
