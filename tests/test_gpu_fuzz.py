@@ -67,3 +67,32 @@ def test_rs_random_shapes_bit_exact(W, M, K, N, lay, seed):
         got, _ = case.run(mode=mode)
         assert np.array_equal(got, out16), mode
 
+
+
+def _moe_cases(n=12, seed=2026):
+    g = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        W = int(g.choice([1, 2, 4, 8]))
+        E = W * int(g.choice([1, 2, 4, 16, 32]))
+        k = int(min(E, g.choice([1, 2, 3, 8])))
+        T = int(g.choice([1, 5, 63, 64, 65, 200]))
+        H = int(g.choice([8, 16, 72, 264, 1032]))
+        out.append((W, T, H, E, k, 3000 + i))
+    return out
+
+
+@pytest.mark.parametrize("W,T,H,E,k,seed", _moe_cases())
+def test_moe_random_shapes(W, T, H, E, k, seed):
+    from test_gpu_moe import MoECase, _check_route
+    from gpu_util import assert_close
+    inp = synth.moe_inputs(W, T, H, E, k, seed=seed)
+    r = oracle.moe_route(inp.topk, E)
+    case = MoECase(inp)
+    recv = oracle.moe_dispatch(inp.x, r["slot"], W * T * k)
+    _, out64 = oracle.moe_combine(recv, r["slot"], inp.gate)
+    for _ in range(2):   # the workspace and outputs are reused by the second call
+        case.run()
+        _check_route(case, r)
+        assert np.array_equal(to_bits(case.recv), recv)
+        assert_close(np.stack([to_bits(case.out(s)) for s in range(W)]), out64)
