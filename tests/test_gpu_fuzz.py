@@ -96,3 +96,50 @@ def test_moe_random_shapes(W, T, H, E, k, seed):
         _check_route(case, r)
         assert np.array_equal(to_bits(case.recv), recv)
         assert_close(np.stack([to_bits(case.out(s)) for s in range(W)]), out64)
+
+
+def _ring_cases(n=8, seed=2027):
+    g = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        W = int(g.choice([2, 3, 4, 5, 8]))
+        count = 4 * W * int(g.choice([1, 3, 250, 1000, 4099]))
+        tile = 4 * int(g.choice([0, 1, 16, 257]))
+        G = int(g.choice([0, 1, 3]))
+        out.append((W, count, tile, G, 4000 + i))
+    return out
+
+
+@pytest.mark.parametrize("W,count,tile,G,seed", _ring_cases())
+def test_ring_allreduce_random_shapes_bit_exact(W, count, tile, G, seed):
+    from test_gpu_allreduce import RingCase
+    case = RingCase(W, count, seed=seed, integer=True)
+    want = oracle.allreduce(case.xs)
+    for _ in range(2):
+        outs, _ = case.run(tile_elems=tile, ctas_per_rank=G)
+        for r in range(W):
+            assert np.array_equal(outs[r].astype(np.float64), want), r
+
+
+def _flash_cases(n=8, seed=2028):
+    g = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        W = int(g.choice([1, 2, 3, 4, 8]))
+        Hkv = int(g.choice([1, 2, 4]))
+        Hq = Hkv * int(g.choice([1, 2, 8, 16]))
+        B = int(g.choice([1, 2, 3]))
+        S = W * int(g.choice([1, 63, 64, 65, 300]))
+        chunk = int(g.choice([0, 64, 128]))
+        out.append((W, B, Hq, Hkv, S, chunk, 5000 + i))
+    return out
+
+
+@pytest.mark.parametrize("W,B,Hq,Hkv,S,chunk,seed", _flash_cases())
+def test_flash_decode_random_shapes(W, B, Hq, Hkv, S, chunk, seed):
+    from test_gpu_flash import FlashCase
+    from gpu_util import assert_close
+    case = FlashCase(W, B, Hq, Hkv, S, chunk=chunk, seed=seed, root=seed % W)
+    ref = oracle.attention_decode(case.q, case.full(case.k), case.full(case.v))
+    for _ in range(2):
+        assert_close(case.run(), ref)
