@@ -9,6 +9,8 @@ Recipe (numpy ``Generator(PCG64(seed))``, seed 0 unless stated):
   * "normal"  : ``standard_normal(float32) * std`` in float32, then bf16 by
                 round-to-nearest-even (torch's float32 -> bfloat16 cast).
   * "int2"    : integers uniform in {-2, -1, 0, 1, 2} (each 1/5), exact in bf16.
+                (`device_int2` draws the same distribution on the device with
+                torch's generator, for inputs too large for the host.)
   * Tensors are drawn in the order the workload lists them: AG-GEMM draws
     A_0 .. A_{W-1} then B; GEMM-RS draws A_0, B_0, A_1, B_1, ...; MoE draws x,
     then the routing noise, then the gate logits.
@@ -50,6 +52,14 @@ def draw(g: np.random.Generator, shape, dist: str, std: float = 1.0) -> np.ndarr
             x *= np.float32(std)
         return f32_to_bf16_bits(x)
     raise ValueError(f"unknown distribution {dist!r}")
+
+
+def device_int2(shape, seed: int, device="cuda") -> torch.Tensor:
+    """bf16 integers uniform in {-2..2} drawn on the device by torch's seeded
+    generator (for inputs too large to draw and hold on the host)."""
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    return torch.randint(-2, 3, shape, generator=g, device=device, dtype=torch.int8).to(torch.bfloat16)
 
 
 # ------------------------------------------------------------------ AG ----
