@@ -636,7 +636,9 @@ def main():
     mlp = MLP(torch, tdg, synth, args.mode, args.producers, args.signal_rows)
     torch.cuda.synchronize()
 
-    fns = [lambda: mlp.ag_call(), lambda: mlp.rs_call("sm")]
+    # --only rs --mode serial times the serial twin of the GEMM-RS (for captures)
+    rs_mode = "serial" if (args.only == "rs" and args.mode == "serial") else "sm"
+    fns = [lambda: mlp.ag_call(), lambda: mlp.rs_call(rs_mode)]
     if args.only == "ag":
         fns = fns[:1]
     elif args.only == "rs":
