@@ -14,8 +14,14 @@
 // CE mode: cudaMemcpyAsync per group on the side stream, each followed by a
 // stream-ordered cuStreamWriteValue32 of the flag; the GEMM-only launch on
 // the main stream waits on the flags.
+// LL mode: one cooperative launch of sender CTAs (8-byte {payload, epoch}
+// words into the rank's LL buffer), receiver CTAs (poll every word, unpack it
+// into the gathered buffer, release the group's flag) and the GEMM, which
+// waits on those flags as in SM mode.
 // SERIAL mode: a copy-only launch (all SMs), then a GEMM-only launch that does
 // not wait; the two are ordered by the stream.
+// Tile order: the pages' rank swizzle over m tiles; m-major while B fits in
+// about half of L2, else groups of 8 m tiles with n outer inside a group.
 #include "tdg_gemm.cuh"
 #include "tdg_internal.h"
 
