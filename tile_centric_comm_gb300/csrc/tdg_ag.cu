@@ -309,62 +309,89 @@ __device__ void ag_producer(const AgParams &p, uint8_t *smem)
 // in the gathered matrix.  Sources in the same order as the bulk producers.
 __device__ void ll_sender(const AgParams &p, int cta, int ncta)
 {
+    constexpr int LB = 8;               // words per thread per pass: independent loads in flight
     const int64_t wps = p.Ms * p.K / 2; // words per shard
     // in the all-sources order every source's words are visited in runs of 64
     // (the last run of a source padded), so the loop covers ceil(wps/64)*64*W
     const int64_t total = p.mesh ? (wps + 63) / 64 * 64 * p.W : wps * p.W;
     const uint64_t hi = (uint64_t)p.epoch << 32;
-    for (int64_t w = (int64_t)cta * blockDim.x + threadIdx.x; w < total; w += (int64_t)ncta * blockDim.x) {
-        // source order as for the bulk producers, in units of 64-word runs
-        int seq;
-        int64_t off;
-        if (p.mesh) {
-            const int64_t run = w / 64, in = w % 64;
-            seq = (int)(run % p.W);
-            off = (run / p.W) * 64 + in;
-            if (off >= wps)
+    for (int64_t w0 = ((int64_t)cta * blockDim.x + threadIdx.x) * LB; w0 < total;
+         w0 += (int64_t)ncta * blockDim.x * LB) {
+        int64_t gw[LB];
+        uint32_t payload[LB];
+#pragma unroll
+        for (int j = 0; j < LB; ++j) {
+            const int64_t w = w0 + j;
+            gw[j] = -1;
+            if (w >= total)
                 continue;
-        } else {
-            seq = (int)(w / wps);
-            off = w % wps;
+            // source order as for the bulk producers, in units of 64-word runs
+            int seq;
+            int64_t off;
+            if (p.mesh) {
+                const int64_t run = w / 64, in = w % 64;
+                seq = (int)(run % p.W);
+                off = (run / p.W) * 64 + in;
+                if (off >= wps)
+                    continue;
+            } else {
+                seq = (int)(w / wps);
+                off = w % wps;
+            }
+            const int shard = (p.rank + 1 + seq) % p.W;
+            const int64_t word = (int64_t)shard * wps + off;
+            const int64_t g = (word * 2 / p.K) / p.sig_rows;
+            if ((p.skip_mask >> (g & 63)) & 1ull)
+                continue;
+            gw[j] = word;
+            payload[j] = *reinterpret_cast<const uint32_t *>(
+                p.regions + (uint64_t)shard * p.region_bytes + p.a_off + (uint64_t)off * 4);
         }
-        const int shard = (p.rank + 1 + seq) % p.W;
-        const int64_t gw = (int64_t)shard * wps + off;
-        const int64_t g = (gw * 2 / p.K) / p.sig_rows;
-        if ((p.skip_mask >> (g & 63)) & 1ull)
-            continue;
-        const uint32_t payload = *reinterpret_cast<const uint32_t *>(
-            p.regions + (uint64_t)shard * p.region_bytes + p.a_off + (uint64_t)off * 4);
-        st_relaxed_gpu_u64(p.ll_buf + gw, hi | payload);
+#pragma unroll
+        for (int j = 0; j < LB; ++j)
+            if (gw[j] >= 0)
+                st_relaxed_gpu_u64(p.ll_buf + gw[j], hi | payload[j]);
     }
 }
 
 // LL receiver: spin (bounded) on every word of a signal group until its flag
 // is this call's epoch, unpack the payload into the gathered buffer, then hand
-// the group to the GEMM with one release of the group's flag.
+// the group to the GEMM with one release of the group's flag.  Each thread
+// loads LB consecutive words before it looks at any, so LB loads are in flight.
 __device__ void ll_receiver(const AgParams &p, int cta, int ncta)
 {
+    constexpr int LB = 8;
     const int64_t wpg = p.sig_rows * p.K / 2; // words per group
     const int64_t n_groups = p.M / p.sig_rows;
     uint32_t *g32 = reinterpret_cast<uint32_t *>(p.gathered);
     bool gave_up = false;
     for (int64_t g = cta; g < n_groups; g += ncta) {
-        for (int64_t i = threadIdx.x; i < wpg; i += blockDim.x) {
-            const int64_t w = g * wpg + i;
-            uint64_t v = ld_relaxed_gpu_u64(p.ll_buf + w);
-            if ((uint32_t)(v >> 32) != p.epoch && !gave_up) {
-                const uint64_t t0 = globaltimer();
-                while ((uint32_t)(v >> 32) != p.epoch) {
-                    __nanosleep(64);
-                    v = ld_relaxed_gpu_u64(p.ll_buf + w);
-                    if (globaltimer() - t0 > p.timeout_ns) {
-                        report_fault(p.status, TDG_ERR_TIMEOUT, TDG_WHERE_LL, (uint32_t)g, p.epoch);
-                        gave_up = true;
-                        break;
+        for (int64_t i0 = (int64_t)threadIdx.x * LB; i0 < wpg; i0 += (int64_t)blockDim.x * LB) {
+            const int64_t w0 = g * wpg + i0;
+            const int n = (int)min((int64_t)LB, wpg - i0);
+            uint64_t v[LB];
+#pragma unroll
+            for (int j = 0; j < LB; ++j)
+                if (j < n)
+                    v[j] = ld_relaxed_gpu_u64(p.ll_buf + w0 + j);
+#pragma unroll
+            for (int j = 0; j < LB; ++j) {
+                if (j >= n)
+                    continue;
+                if ((uint32_t)(v[j] >> 32) != p.epoch && !gave_up) {
+                    const uint64_t t0 = globaltimer();
+                    while ((uint32_t)(v[j] >> 32) != p.epoch) {
+                        __nanosleep(64);
+                        v[j] = ld_relaxed_gpu_u64(p.ll_buf + w0 + j);
+                        if (globaltimer() - t0 > p.timeout_ns) {
+                            report_fault(p.status, TDG_ERR_TIMEOUT, TDG_WHERE_LL, (uint32_t)g, p.epoch);
+                            gave_up = true;
+                            break;
+                        }
                     }
                 }
+                g32[w0 + j] = (uint32_t)v[j];
             }
-            g32[w] = (uint32_t)v;
         }
         __syncthreads();
         if (threadIdx.x == 0) {
@@ -512,7 +539,7 @@ extern "C" int tdg_ag_gemm(tdg_symm *h, const tdg_ag_gemm_args *a, void *stream,
     const int BM = gm::BM;
     // CTA pairs (256-row tiles) once there is more than one 128-row tile; two
     // pairs sharing B (512-row tiles) when every shard is a whole number of them
-    const int pair = (pairs_enabled() && M > BM && !ll) ? 1 : 0;
+    const int pair = (pairs_enabled() && M > BM) ? 1 : 0;
     const int cl = pair ? ((quads_enabled() && Ms % (4 * BM) == 0) ? 4 : 2) : 1;
     const int TM = cl * BM;
     const bool inplace = (Ms % TM) == 0;
@@ -586,7 +613,10 @@ extern "C" int tdg_ag_gemm(tdg_symm *h, const tdg_ag_gemm_args *a, void *stream,
         // sender and receiver CTAs beside the GEMM, all in one cooperative launch
         const int n_send = a->producers > 0 ? a->producers : 8;
         const int64_t groups = M / sig_rows;
-        const int n_recv = (int)(groups < 8 ? groups : 8);
+        // as many receivers as senders (8 by default), at most one per group
+        int n_recv = (int)(groups < n_send ? groups : n_send);
+        // senders and receivers fill whole clusters (spare receivers find no group)
+        n_recv = (n_send + n_recv + cl - 1) / cl * cl - n_send;
         if (n_send + n_recv >= ggrid)
             return TDG_ERR_INVALID;
         p.ll = 1;
