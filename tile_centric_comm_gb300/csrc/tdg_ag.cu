@@ -374,24 +374,37 @@ __device__ void ll_receiver(const AgParams &p, int cta, int ncta)
             for (int j = 0; j < LB; ++j)
                 if (j < n)
                     v[j] = ld_relaxed_gpu_u64(p.ll_buf + w0 + j);
+            // words not yet delivered are polled together: one round trip
+            // per poll for the whole batch
+            uint32_t pending = 0;
 #pragma unroll
-            for (int j = 0; j < LB; ++j) {
-                if (j >= n)
-                    continue;
-                if ((uint32_t)(v[j] >> 32) != p.epoch && !gave_up) {
-                    const uint64_t t0 = globaltimer();
-                    while ((uint32_t)(v[j] >> 32) != p.epoch) {
+            for (int j = 0; j < LB; ++j)
+                if (j < n && (uint32_t)(v[j] >> 32) != p.epoch)
+                    pending |= 1u << j;
+            if (pending && !gave_up) {
+                const uint64_t t0 = globaltimer();
+                for (int spin = 0; pending; ++spin) {
+                    if (spin >= 16)
                         __nanosleep(64);
-                        v[j] = ld_relaxed_gpu_u64(p.ll_buf + w0 + j);
-                        if (globaltimer() - t0 > p.timeout_ns) {
-                            report_fault(p.status, TDG_ERR_TIMEOUT, TDG_WHERE_LL, (uint32_t)g, p.epoch);
-                            gave_up = true;
-                            break;
-                        }
+#pragma unroll
+                    for (int j = 0; j < LB; ++j)
+                        if ((pending >> j) & 1u)
+                            v[j] = ld_relaxed_gpu_u64(p.ll_buf + w0 + j);
+#pragma unroll
+                    for (int j = 0; j < LB; ++j)
+                        if (((pending >> j) & 1u) && (uint32_t)(v[j] >> 32) == p.epoch)
+                            pending &= ~(1u << j);
+                    if (pending && globaltimer() - t0 > p.timeout_ns) {
+                        report_fault(p.status, TDG_ERR_TIMEOUT, TDG_WHERE_LL, (uint32_t)g, p.epoch);
+                        gave_up = true;
+                        break;
                     }
                 }
-                g32[w0 + j] = (uint32_t)v[j];
             }
+#pragma unroll
+            for (int j = 0; j < LB; ++j)
+                if (j < n)
+                    g32[w0 + j] = (uint32_t)v[j];
         }
         __syncthreads();
         if (threadIdx.x == 0) {
