@@ -489,8 +489,13 @@ int launch_ag(const AgParams &p, int b_layout, int grid, bool coop, cudaStream_t
     if (grid < 1 || grid < p.n_prod) // a copy-only launch has no consumers
         return TDG_ERR_UNSUPPORTED;
     AgParams q = p;
-    const int64_t units = (grid - p.n_prod) / p.cl;
+    int64_t units = (grid - p.n_prod) / p.cl;
     const int64_t T = (int64_t)p.m_tiles * p.n_tiles;
+    // no more GEMM clusters than tiles (a small problem launches few CTAs)
+    if (units > T && units > 0) {
+        units = T;
+        grid = p.n_prod + (int)(p.cl * units);
+    }
     q.split = 0;
     // opt-in (TDG_SPLIT_TAIL=1): measured slower at the Qwen-32B up-projection
     // shape, where the half-width tiles move more operand bytes per FLOP and the

@@ -382,6 +382,10 @@ extern "C" int tdg_gemm_rs(tdg_symm *h, const tdg_gemm_rs_args *a, void *stream)
             return TDG_ERR_UNSUPPORTED;
         grid = cl * n;
     }
+    // no more clusters than work items (a small problem launches few CTAs)
+    const int64_t items = (int64_t)W * W * p.mtp * n_tiles;
+    if (grid / cl > items)
+        grid = (int)(cl * items);
     void *args[] = {&p};
     int rc = cuda_err(launch(fn, dim3(grid), dim3(gm::NUM_THREADS), gm::SMEM_BYTES, s, args, false, cl),
                       "rs gemm launch");
