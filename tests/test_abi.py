@@ -117,3 +117,20 @@ def test_strerror_and_invalid_handles(L):
                             ctypes.byref(h)) == tdg.TDG_ERR_INVALID
     assert L.tdg_symm_alloc(ctypes.c_void_p(1024), 100, 2, 4096, 16,
                             ctypes.byref(h)) == tdg.TDG_ERR_NOMEM
+
+
+def test_binding_tensor_checks_on_the_host():
+    """The library sees raw pointers only, so the binding refuses a tensor
+    whose dtype, layout or size it cannot describe (checked before the device)."""
+    import torch
+    good = torch.zeros(4, 8, dtype=torch.bfloat16)
+    with pytest.raises(TypeError, match="bfloat16"):
+        tdg._tensor(good.float(), "B", torch.bfloat16, 32)
+    with pytest.raises(ValueError, match="contiguous"):
+        tdg._tensor(good.t(), "B", torch.bfloat16, 32)
+    with pytest.raises(ValueError, match="needs 33"):
+        tdg._tensor(good, "B", torch.bfloat16, 33)
+    with pytest.raises(ValueError, match="CUDA"):
+        tdg._tensor(good, "B", torch.bfloat16, 32)
+    with pytest.raises(TypeError, match="torch.Tensor"):
+        tdg._tensor([0] * 32, "B", torch.bfloat16, 32)

@@ -161,8 +161,9 @@ def test_degenerate_shapes():
     tdg.ag_gemm(case.symm, 0, 0, 8, 16, case.a_off, case.g_off, case.B, case.C)
     torch.cuda.synchronize()
     assert np.all(to_bits(case.C) == 7)
+    B12 = torch.zeros(12, 16, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(tdg.TdgError):     # K not a multiple of 8
-        tdg.ag_gemm(case.symm, 0, 64, 12, 16, case.a_off, case.g_off, case.B, case.C)
+        tdg.ag_gemm(case.symm, 0, 64, 12, 16, case.a_off, case.g_off, B12, case.C)
     with pytest.raises(tdg.TdgError):     # bad rank
         tdg.ag_gemm(case.symm, 2, 64, 8, 16, case.a_off, case.g_off, case.B, case.C)
 

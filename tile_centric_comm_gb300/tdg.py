@@ -153,6 +153,26 @@ def _check(rc, what):
         raise TdgError(rc, what)
 
 
+def _tensor(t, name, dtype, numel, device=None):
+    """Check a tensor handed to the library as a raw pointer: the library sees
+    neither strides nor dtype, so it must be a contiguous CUDA tensor of the
+    documented element type holding at least `numel` elements."""
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor, got {type(t).__name__}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous (the library reads it row-major)")
+    if t.numel() < numel:
+        raise ValueError(f"{name}: holds {t.numel()} elements, needs {numel}")
+    if not t.is_cuda:
+        raise ValueError(f"{name}: must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name}: on {t.device}, the heap is on {device}")
+    return t.data_ptr()
+
+
 def _stream(stream):
     import torch
     if stream is None:
@@ -177,6 +197,7 @@ class Symm:
         nbytes = L.tdg_symm_bytes(world, region_bytes, signals_per_rank)
         if buffer is None:
             buffer = torch.empty(nbytes + 1024, dtype=torch.uint8, device=device or "cuda")
+        _tensor(buffer, "buffer", torch.uint8, nbytes + 1024)
         self.buf = buffer
         self.base_off = (-buffer.data_ptr()) % 1024
         self.base = buffer.data_ptr() + self.base_off
@@ -210,17 +231,25 @@ class Symm:
         for d in shape:
             n *= int(d)
         esz = torch.empty((), dtype=dtype).element_size()
-        assert off % esz == 0 and off + n * esz <= self.region_bytes
+        if not 0 <= rank < self.world:
+            raise ValueError(f"rank {rank} outside [0, {self.world})")
+        if off < 0 or off % esz or off + n * esz > self.region_bytes:
+            raise ValueError(f"view of {n * esz} bytes at offset {off} does not fit a "
+                             f"{self.region_bytes}-byte region with {esz}-byte alignment")
         start = self.base_off + rank * self.region_bytes + off
         return self.buf[start:start + n * esz].view(dtype).view(*shape)
 
     def flags(self, rank: int, n: int):
         import torch
+        if not 0 <= rank < self.world or not 0 <= n <= self.nsig:
+            raise ValueError(f"flags({rank}, {n}) outside {self.world} ranks x {self.nsig} words")
         start = lib().tdg_symm_flags(self.h, rank) - self.buf.data_ptr()
         return self.buf[start:start + 4 * n].view(torch.int32)
 
     def counters(self, rank: int, n: int):
         import torch
+        if not 0 <= rank < self.world or not 0 <= n <= self.nsig:
+            raise ValueError(f"counters({rank}, {n}) outside {self.world} ranks x {self.nsig} words")
         start = lib().tdg_symm_counters(self.h, rank) - self.buf.data_ptr()
         return self.buf[start:start + 4 * n].view(torch.int32)
 
@@ -242,8 +271,12 @@ def ag_gemm(symm: Symm, rank: int, Ms: int, K: int, N: int, a_off: int, g_off: i
             mode="sm", b_layout=B_KN, producers=0, signal_rows=0, swizzle=True,
             timeout_ns=0, ll_off=0, test_skip_notify=0, source_order=0, stream=None,
             side_stream=None):
+    import torch
+    dev = symm.buf.device
     a = AgGemmArgs(world=symm.world, rank=rank, Ms=Ms, K=K, N=N, a_off=a_off, g_off=g_off,
-                   B=B.data_ptr(), C=C.data_ptr(), b_layout=b_layout, mode=MODES[mode],
+                   B=_tensor(B, "B", torch.bfloat16, K * N, dev),
+                   C=_tensor(C, "C", torch.bfloat16, symm.world * Ms * N, dev),
+                   b_layout=b_layout, mode=MODES[mode],
                    producers=producers, signal_rows=signal_rows, swizzle=1 if swizzle else 0,
                    timeout_ns=timeout_ns, ll_off=ll_off, test_skip_notify=test_skip_notify,
                    source_order=source_order)
@@ -281,10 +314,35 @@ def flash_decode_part_bytes(world: int, B: int, Hq: int, D: int, S: int, chunk: 
 def flash_decode(symm: Symm, B: int, Hq: int, Hkv: int, D: int, S: int, k_off: int, v_off: int,
                  part_off: int, q, out, root: int = 0, chunk: int = 0, scale: float = 0.0,
                  stream=None):
+    import torch
+    dev = symm.buf.device
     a = FlashDecodeArgs(world=symm.world, root=root, B=B, Hq=Hq, Hkv=Hkv, D=D, S=S, k_off=k_off,
-                        v_off=v_off, part_off=part_off, q=q.data_ptr(), out=out.data_ptr(),
+                        v_off=v_off, part_off=part_off,
+                        q=_tensor(q, "q", torch.bfloat16, B * Hq * D, dev),
+                        out=_tensor(out, "out", torch.bfloat16, B * Hq * D, dev),
                         chunk=chunk, scale=scale)
     _check(lib().tdg_flash_decode(symm.h, ctypes.byref(a), _stream(stream)), "tdg_flash_decode")
+
+
+def _moe_args(symm, T, H, E, k, x_off, topk_off, gate_off, out_off, recv, counts, base, slot,
+              y, row_src, row_tok, row_k, phases):
+    import torch
+    dev, W = symm.buf.device, symm.world
+    rows = W * T * k
+
+    def opt(t, name, dtype, n):
+        return None if t is None else _tensor(t, name, dtype, n, dev)
+    return MoeArgs(world=W, T=T, H=H, E=E, k=k, x_off=x_off, topk_off=topk_off,
+                   gate_off=gate_off, out_off=out_off,
+                   recv=opt(recv, "recv", torch.bfloat16, rows * H),
+                   y=opt(y, "y", torch.bfloat16, rows * H),
+                   counts=opt(counts, "counts", torch.int64, W * E),
+                   base=opt(base, "base", torch.int64, E + 1),
+                   slot=opt(slot, "slot", torch.int64, rows),
+                   row_src=opt(row_src, "row_src", torch.int32, rows),
+                   row_tok=opt(row_tok, "row_tok", torch.int32, rows),
+                   row_k=opt(row_k, "row_k", torch.int32, rows),
+                   workspace=None, workspace_bytes=0, phases=phases)
 
 
 def moe_workspace_bytes(world: int, T: int, E: int) -> int:
@@ -295,13 +353,12 @@ def moe_dispatch_combine(symm: Symm, T: int, H: int, E: int, k: int, x_off: int,
                          gate_off: int, out_off: int, recv, counts, base, slot, workspace,
                          y=None, row_src=None, row_tok=None, row_k=None, phases=MOE_ALL,
                          stream=None):
-    def p(t):
-        return t.data_ptr() if t is not None else None
-    a = MoeArgs(world=symm.world, T=T, H=H, E=E, k=k, x_off=x_off, topk_off=topk_off,
-                gate_off=gate_off, out_off=out_off, recv=p(recv), y=p(y), counts=p(counts),
-                base=p(base), slot=p(slot), row_src=p(row_src), row_tok=p(row_tok),
-                row_k=p(row_k), workspace=p(workspace),
-                workspace_bytes=workspace.numel() * workspace.element_size(), phases=phases)
+    import torch
+    _tensor(workspace, "workspace", torch.uint8, 0, symm.buf.device)
+    a = _moe_args(symm, T, H, E, k, x_off, topk_off, gate_off, out_off, recv, counts, base, slot,
+                  y, row_src, row_tok, row_k, phases)
+    a.workspace = workspace.data_ptr()
+    a.workspace_bytes = workspace.numel()
     _check(lib().tdg_moe_dispatch_combine(symm.h, ctypes.byref(a), _stream(stream)),
            "tdg_moe_dispatch_combine")
 
@@ -314,11 +371,7 @@ def moe_dispatch_combine_noalloc(symm: Symm, T: int, H: int, E: int, k: int, x_o
     memory when they call: the routing scratch is the library's fixed 2 MiB
     device array, so no workspace is passed.  Raises TdgError (TDG_ERR_NOMEM)
     when world * ceil(T/64) * E exceeds 262144."""
-    def p(t):
-        return t.data_ptr() if t is not None else None
-    a = MoeArgs(world=symm.world, T=T, H=H, E=E, k=k, x_off=x_off, topk_off=topk_off,
-                gate_off=gate_off, out_off=out_off, recv=p(recv), y=p(y), counts=p(counts),
-                base=p(base), slot=p(slot), row_src=p(row_src), row_tok=p(row_tok),
-                row_k=p(row_k), workspace=None, workspace_bytes=0, phases=phases)
+    a = _moe_args(symm, T, H, E, k, x_off, topk_off, gate_off, out_off, recv, counts, base, slot,
+                  y, row_src, row_tok, row_k, phases)
     _check(lib().tdg_moe_dispatch_combine_noalloc(symm.h, ctypes.byref(a), _stream(stream)),
            "tdg_moe_dispatch_combine_noalloc")
