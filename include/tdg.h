@@ -25,7 +25,11 @@
  *   - The library allocates no device memory.  Each entry point documents
  *     which caller-provided buffers it uses.
  *   - A handle is thread-compatible, not thread-safe: do not call into the
- *     same handle from two host threads at once.
+ *     same handle from two host threads at once.  Different handles may be
+ *     used from different threads.
+ *   - Every operation runs on the device the heap was allocated on
+ *     (tdg_symm_alloc records the current device); calling it while another
+ *     device is current returns TDG_ERR_INVALID.
  */
 #ifndef TDG_H_
 #define TDG_H_

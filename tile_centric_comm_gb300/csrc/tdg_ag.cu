@@ -451,39 +451,28 @@ const void *ag_kernel_fn(int b_layout, int cl)
                      : reinterpret_cast<const void *>(&ag_gemm_kernel<0, 1>);
 }
 
-int prepare(const void *fn, int dev)
+int prepare(const void *fn)
 {
-    static const void *done[8][64] = {};
-    for (int i = 0; i < 8; ++i) {
-        if (done[i][dev & 63] == fn)
-            return TDG_OK;
-        if (!done[i][dev & 63]) {
-            cudaError_t e = set_smem(fn, gm::SMEM_BYTES);
-            if (e != cudaSuccess)
-                return cuda_err(e, "ag set smem");
-            done[i][dev & 63] = fn;
-            return TDG_OK;
-        }
-    }
-    return cuda_err(set_smem(fn, gm::SMEM_BYTES), "ag set smem");
+    const cudaError_t e = set_smem(fn, gm::SMEM_BYTES);
+    return e == cudaSuccess ? TDG_OK : cuda_err(e, "ag set smem");
 }
 
 // grid for a launch with n_prod producer CTAs plus consumers on every other SM
-int ag_grid(const AgParams &p, int b_layout, int sms, int dev)
+int ag_grid(const AgParams &p, int b_layout, int sms)
 {
     if (p.cl == 1)
         return sms;
-    if (prepare(ag_kernel_fn(b_layout, p.cl), dev) != TDG_OK)
+    if (prepare(ag_kernel_fn(b_layout, p.cl)) != TDG_OK)
         return 0;
     const int mc = max_clusters(ag_kernel_fn(b_layout, p.cl), gm::NUM_THREADS, gm::SMEM_BYTES, p.cl);
     const int n = mc > 0 ? (mc < sms / p.cl ? mc : sms / p.cl) : 0;
     return p.cl * n;
 }
 
-int launch_ag(const AgParams &p, int b_layout, int grid, bool coop, cudaStream_t s, int dev)
+int launch_ag(const AgParams &p, int b_layout, int grid, bool coop, cudaStream_t s)
 {
     const void *fn = ag_kernel_fn(b_layout, p.cl);
-    int rc = prepare(fn, dev);
+    int rc = prepare(fn);
     if (rc != TDG_OK)
         return rc;
     if (grid < 1 || grid < p.n_prod) // a copy-only launch has no consumers
@@ -520,6 +509,8 @@ extern "C" int tdg_ag_gemm(tdg_symm *h, const tdg_ag_gemm_args *a, void *stream,
 {
     if (!h || !a)
         return TDG_ERR_INVALID;
+    if (const int drc = check_device(h))
+        return drc;
     const int W = a->world, rank = a->rank;
     if (W != h->world || rank < 0 || rank >= W || a->Ms < 0 || a->K < 0 || a->N < 0)
         return TDG_ERR_INVALID;
@@ -623,8 +614,7 @@ extern "C" int tdg_ag_gemm(tdg_symm *h, const tdg_ag_gemm_args *a, void *stream,
     p.mesh = a->source_order;
 
     const int sms = h->sm_count;
-    const int dev = h->device;
-    const int ggrid = ag_grid(p, a->b_layout, sms, dev); // GEMM-only grid
+    const int ggrid = ag_grid(p, a->b_layout, sms); // GEMM-only grid
     if (ggrid <= 0)
         return TDG_ERR_UNSUPPORTED;
     if (ll) {
@@ -643,7 +633,7 @@ extern "C" int tdg_ag_gemm(tdg_symm *h, const tdg_ag_gemm_args *a, void *stream,
         p.n_prod = n_send + n_recv;
         p.wait_flags = 1;
         p.n_units = 0;
-        return launch_ag(p, a->b_layout, ggrid, true, s, dev);
+        return launch_ag(p, a->b_layout, ggrid, true, s);
     }
     if (a->mode == TDG_MODE_SM) {
         int nprod = a->producers > 0 ? a->producers : 16;
@@ -656,7 +646,7 @@ extern "C" int tdg_ag_gemm(tdg_symm *h, const tdg_ag_gemm_args *a, void *stream,
         p.unit_rows = sig_rows;
         p.units_per_shard = Ms / sig_rows;
         p.n_units = (int64_t)W * p.units_per_shard;
-        return launch_ag(p, a->b_layout, ggrid, true, s, dev);
+        return launch_ag(p, a->b_layout, ggrid, true, s);
     }
     if (a->mode == TDG_MODE_SERIAL) {
         // copy phase: every SM copies, fine-grained units, no signals
@@ -672,7 +662,7 @@ extern "C" int tdg_ag_gemm(tdg_symm *h, const tdg_ag_gemm_args *a, void *stream,
         c.local_last = 0;
         c.pair = 0;
         c.cl = 1;
-        int rc = launch_ag(c, a->b_layout, sms, false, s, dev);
+        int rc = launch_ag(c, a->b_layout, sms, false, s);
         if (rc != TDG_OK)
             return rc;
         // GEMM phase: stream-ordered after the copy, no waits
@@ -680,7 +670,7 @@ extern "C" int tdg_ag_gemm(tdg_symm *h, const tdg_ag_gemm_args *a, void *stream,
         g.n_prod = 0;
         g.wait_flags = 0;
         g.n_units = 0;
-        return launch_ag(g, a->b_layout, ggrid, false, s, dev);
+        return launch_ag(g, a->b_layout, ggrid, false, s);
     }
     // CE mode
     cudaStream_t side = static_cast<cudaStream_t>(side_stream);
@@ -724,7 +714,7 @@ extern "C" int tdg_ag_gemm(tdg_symm *h, const tdg_ag_gemm_args *a, void *stream,
         g.n_prod = 0;
         g.wait_flags = 1;
         g.n_units = 0;
-        rc = launch_ag(g, a->b_layout, ggrid, false, s, dev);
+        rc = launch_ag(g, a->b_layout, ggrid, false, s);
     }
     // the call completes on the main stream only when the side stream has too
     e = cudaEventRecord(ev1, side);

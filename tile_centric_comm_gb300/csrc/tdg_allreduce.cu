@@ -156,6 +156,8 @@ extern "C" int tdg_allreduce(tdg_symm *h, const tdg_allreduce_args *a, void *str
 {
     if (!h || !a)
         return TDG_ERR_INVALID;
+    if (const int drc = check_device(h))
+        return drc;
     const int W = a->world;
     if (W != h->world || a->count < 0)
         return TDG_ERR_INVALID;

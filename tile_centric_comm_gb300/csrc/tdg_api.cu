@@ -10,6 +10,8 @@
 #include <string.h>
 
 #include <atomic>
+#include <mutex>
+#include <vector>
 
 #include "tdg_internal.h"
 
@@ -96,7 +98,32 @@ bool stream_write_u32(cudaStream_t s, uint32_t *dev_addr, uint32_t value)
 
 cudaError_t set_smem(const void *fn, int bytes)
 {
-    return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    struct Done {
+        const void *fn;
+        int dev, bytes;
+    };
+    static std::mutex mu;
+    static std::vector<Done> done;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    std::lock_guard<std::mutex> lock(mu);
+    for (const Done &d : done)
+        if (d.fn == fn && d.dev == dev && d.bytes >= bytes)
+            return cudaSuccess;
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess)
+        done.push_back({fn, dev, bytes});
+    return e;
+}
+
+int check_device(const tdg_symm *h)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return TDG_ERR_CUDA;
+    return dev == h->device ? TDG_OK : TDG_ERR_INVALID;
 }
 
 cudaError_t launch(const void *fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s,

@@ -336,6 +336,8 @@ extern "C" int tdg_flash_decode(tdg_symm *h, const tdg_flash_decode_args *a, voi
 {
     if (!h || !a)
         return TDG_ERR_INVALID;
+    if (const int drc = check_device(h))
+        return drc;
     const int W = a->world;
     if (W != h->world || a->root < 0 || a->root >= W || a->B <= 0 || a->Hq <= 0 || a->Hkv <= 0 ||
         a->D != fd::D || a->S <= 0 || a->S % W || a->Hq % a->Hkv || a->Hq / a->Hkv > 16)
@@ -374,13 +376,9 @@ extern "C" int tdg_flash_decode(tdg_symm *h, const tdg_flash_decode_args *a, voi
     p.part_ml = p.part_o + (size_t)W * splits * a->B * a->Hq * fd::D;
     p.q = static_cast<const __nv_bfloat16 *>(a->q);
     p.out = static_cast<__nv_bfloat16 *>(a->out);
-    static bool smem_set[64] = {};
-    if (!smem_set[h->device & 63]) {
-        cudaError_t e = set_smem(reinterpret_cast<const void *>(&flash_decode_kernel), fd::SMEM);
-        if (e != cudaSuccess)
-            return cuda_err(e, "flash smem");
-        smem_set[h->device & 63] = true;
-    }
+    if (cudaError_t e = set_smem(reinterpret_cast<const void *>(&flash_decode_kernel), fd::SMEM);
+        e != cudaSuccess)
+        return cuda_err(e, "flash smem");
     void *args[] = {&p};
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     int rc = cuda_err(launch(reinterpret_cast<const void *>(&flash_decode_kernel),

@@ -59,9 +59,14 @@ bool map_bf16_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uin
 // barrier before the write).  Returns false when unavailable or failing.
 bool stream_write_u32(cudaStream_t s, uint32_t *dev_addr, uint32_t value);
 
-// Opt a kernel into the large dynamic shared memory it needs (once per
-// function and device).
+// Opt a kernel into the large dynamic shared memory it needs on the current
+// device.  The attribute is set once per (function, device); safe to call from
+// several host threads.
 cudaError_t set_smem(const void *fn, int bytes);
+
+// TDG_OK when the current device is the one the heap was allocated on,
+// TDG_ERR_INVALID when it is another, TDG_ERR_CUDA when it cannot be read.
+int check_device(const tdg_symm *h);
 
 // Launch with the cooperative attribute (all CTAs co-resident, which the
 // cross-CTA signal waits rely on).

@@ -347,6 +347,8 @@ extern "C" int tdg_moe_dispatch_combine(tdg_symm *h, const tdg_moe_args *a, void
 {
     if (!h || !a)
         return TDG_ERR_INVALID;
+    if (const int drc = check_device(h))
+        return drc;
     const int W = a->world, E = a->E, k = a->k;
     const int64_t T = a->T, H = a->H;
     if (W != h->world || T < 0 || H < 0 || E <= 0 || E > moe::MAX_E || E % W || k < 1 || k > 32 || k > E)
@@ -423,13 +425,9 @@ extern "C" int tdg_moe_dispatch_combine(tdg_symm *h, const tdg_moe_args *a, void
             return cuda_err(e, "moe slot");
     }
     if (disp) {
-        static bool smem_set[64] = {};
-        if (!smem_set[h->device & 63]) {
-            e = set_smem(reinterpret_cast<const void *>(&moe_dispatch_kernel), moe::D_SMEM);
-            if (e != cudaSuccess)
-                return cuda_err(e, "moe dispatch smem");
-            smem_set[h->device & 63] = true;
-        }
+        e = set_smem(reinterpret_cast<const void *>(&moe_dispatch_kernel), moe::D_SMEM);
+        if (e != cudaSuccess)
+            return cuda_err(e, "moe dispatch smem");
         const uint64_t row_bytes = (uint64_t)H * 2;
         const int cpr = (int)((row_bytes + moe::DCHUNK - 1) / moe::DCHUNK);
         // equal chunks, 16-byte multiples
@@ -477,6 +475,8 @@ extern "C" int tdg_moe_dispatch_combine_noalloc(tdg_symm *h, const tdg_moe_args 
 {
     if (!h || !a)
         return TDG_ERR_INVALID;
+    if (const int drc = check_device(h))
+        return drc;
     if ((a->phases & TDG_MOE_ROUTE) &&
         tdg_moe_workspace_bytes(a->world, a->T, a->E) > (size_t)TDG_MOE_STATIC_WORKSPACE_BYTES) {
         if (getenv("TDG_LOG"))

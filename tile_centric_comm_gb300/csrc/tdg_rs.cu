@@ -276,6 +276,8 @@ extern "C" int tdg_gemm_rs(tdg_symm *h, const tdg_gemm_rs_args *a, void *stream)
 {
     if (!h || !a)
         return TDG_ERR_INVALID;
+    if (const int drc = check_device(h))
+        return drc;
     const int W = a->world;
     if (W != h->world || a->M < 0 || a->K < 0 || a->N < 0)
         return TDG_ERR_INVALID;
@@ -366,14 +368,8 @@ extern "C" int tdg_gemm_rs(tdg_symm *h, const tdg_gemm_rs_args *a, void *stream)
         fn = cl == 4   ? reinterpret_cast<const void *>(&rs_gemm_kernel<0, 4>)
              : cl == 2 ? reinterpret_cast<const void *>(&rs_gemm_kernel<0, 2>)
                        : reinterpret_cast<const void *>(&rs_gemm_kernel<0, 1>);
-    static bool smem_set[2][3][64] = {};
-    bool &done = smem_set[a->b_layout & 1][cl >> 1][h->device & 63];
-    if (!done) {
-        cudaError_t e = set_smem(fn, gm::SMEM_BYTES);
-        if (e != cudaSuccess)
-            return cuda_err(e, "rs set smem");
-        done = true;
-    }
+    if (cudaError_t e = set_smem(fn, gm::SMEM_BYTES); e != cudaSuccess)
+        return cuda_err(e, "rs set smem");
     int grid = h->sm_count;
     if (cl > 1) {
         const int mc = max_clusters(fn, gm::NUM_THREADS, gm::SMEM_BYTES, cl);
