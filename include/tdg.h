@@ -213,8 +213,15 @@ TDG_API int tdg_ag_gemm(tdg_symm *h, const tdg_ag_gemm_args *args, void *stream,
  * count of W acquires it, sums the W partials in fixed rank order in fp32
  * and writes the bf16 result, then resets the counter to 0.  SERIAL mode
  * runs the GEMM for all partials first and the reduction after it.
+ * partial_f32 = 1 pushes the partial tiles as fp32 instead of bf16: the
+ * staging area is twice tdg_gemm_rs_stage_bytes(), and the only rounding is
+ * the final one of the fp32 sum to bf16 (the pages leave the partial type
+ * open; bf16 is the default).
  * Requirements: M % W == 0, (M/W) % 128 == 0, K % 8 == 0, N % 8 == 0, the
- * offsets 16-byte aligned, W*(M/W/128)*ceil(N/256) <= signals_per_rank.
+ * offsets 16-byte aligned, W*(M/W/128)*ceil(N/256) <= signals_per_rank,
+ * partial_f32 0 or 1, and the staging area and out_o overlapping neither
+ * each other nor A_r / B_r (TDG_ERR_INVALID otherwise; TDG_ERR_NOMEM when a
+ * buffer runs past its region).
  */
 typedef struct {
     int world;
@@ -225,9 +232,11 @@ typedef struct {
     uint64_t timeout_ns; /* bound of every device wait; 0 = 2 s             */
     int owner_block;     /* tile order: owners per block, each rank's tiles of
                             a block back to back (0 = 2; must divide world)  */
+    int partial_f32;     /* 1: fp32 partials (twice the staging), 0: bf16     */
 } tdg_gemm_rs_args;
 
-/* Bytes of one owner's staging area for the given shape (all W partials). */
+/* Bytes of one owner's staging area for the given shape (all W partials),
+ * with bf16 partials; fp32 partials need twice as many. */
 TDG_API size_t tdg_gemm_rs_stage_bytes(int world, int64_t M, int64_t N);
 
 TDG_API int tdg_gemm_rs(tdg_symm *h, const tdg_gemm_rs_args *args, void *stream);

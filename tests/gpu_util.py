@@ -84,14 +84,15 @@ class AGCase:
 class RSCase:
     """Inputs of one GEMM+ReduceScatter call laid out in a symmetric heap."""
 
-    def __init__(self, inp, b_layout=tdg.B_KN, device="cuda"):
+    def __init__(self, inp, b_layout=tdg.B_KN, device="cuda", f32=False):
         self.inp = inp
+        self.f32 = f32           # fp32 partials: the staging area is twice as large
         W, M, K, N = inp.W, inp.M, inp.K, inp.N
         self.Mo = M // W
         self.a_off = 0
         self.b_off = align(M * K * 2)
         self.stage_off = align(self.b_off + K * N * 2)
-        self.out_off = align(self.stage_off + tdg.gemm_rs_stage_bytes(W, M, N))
+        self.out_off = align(self.stage_off + tdg.gemm_rs_stage_bytes(W, M, N) * (2 if f32 else 1))
         region = align(self.out_off + self.Mo * N * 2 + 1024)
         n_tiles = (N + 255) // 256
         nsig = max(1024, (self.Mo // 128) * n_tiles * 4)
@@ -109,6 +110,7 @@ class RSCase:
         inp = self.inp
         for o in range(inp.W):
             self.out(o).view(torch.int16).fill_(POISON)
+        kw.setdefault("partial_f32", self.f32)
         tdg.gemm_rs(self.symm, inp.M, inp.K, inp.N, self.a_off, self.b_off, self.stage_off,
                     self.out_off, mode=mode, b_layout=self.b_layout, **kw)
         torch.cuda.synchronize()

@@ -54,7 +54,10 @@ int main(void) {
   printf("tdg_fault %zu\n", sizeof(tdg_fault));
   F(tdg_ag_gemm_args, B); F(tdg_ag_gemm_args, signal_rows); F(tdg_ag_gemm_args, timeout_ns);
   F(tdg_ag_gemm_args, test_skip_notify);
-  F(tdg_gemm_rs_args, out_off); F(tdg_gemm_rs_args, timeout_ns);
+  F(tdg_gemm_rs_args, out_off); F(tdg_gemm_rs_args, timeout_ns); F(tdg_gemm_rs_args, partial_f32);
+  printf("tdg_allreduce_args %zu\n", sizeof(tdg_allreduce_args));
+  printf("tdg_flash_decode_args %zu\n", sizeof(tdg_flash_decode_args));
+  F(tdg_allreduce_args, timeout_ns); F(tdg_flash_decode_args, out); F(tdg_flash_decode_args, scale);
   F(tdg_moe_args, recv); F(tdg_moe_args, workspace_bytes); F(tdg_moe_args, phases);
   return 0;
 }
@@ -68,11 +71,14 @@ int main(void) {
     assert int(got["tdg_gemm_rs_args"]) == ctypes.sizeof(tdg.GemmRsArgs)
     assert int(got["tdg_moe_args"]) == ctypes.sizeof(tdg.MoeArgs)
     assert int(got["tdg_fault"]) == ctypes.sizeof(tdg.TdgFault)
+    assert int(got["tdg_allreduce_args"]) == ctypes.sizeof(tdg.AllReduceArgs)
+    assert int(got["tdg_flash_decode_args"]) == ctypes.sizeof(tdg.FlashDecodeArgs)
     for key, val in got.items():
         if "." in key:
             s, f = key.split(".")
             cls = {"tdg_ag_gemm_args": tdg.AgGemmArgs, "tdg_gemm_rs_args": tdg.GemmRsArgs,
-                   "tdg_moe_args": tdg.MoeArgs}[s]
+                   "tdg_moe_args": tdg.MoeArgs, "tdg_allreduce_args": tdg.AllReduceArgs,
+                   "tdg_flash_decode_args": tdg.FlashDecodeArgs}[s]
             assert getattr(cls, f).offset == int(val), key
 
 

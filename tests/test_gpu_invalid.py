@@ -65,6 +65,11 @@ def test_gemm_rs_rejections():
     assert rc(owner_block=3) == tdg.TDG_ERR_INVALID                   # does not divide W
     assert rc(world=3) == tdg.TDG_ERR_INVALID                         # not the heap's world
     assert rc(mode=tdg.MODE_CE) == tdg.TDG_ERR_INVALID                # SM or SERIAL only
+    assert rc(partial_f32=2) == tdg.TDG_ERR_INVALID
+    assert rc(partial_f32=1) == tdg.TDG_ERR_NOMEM                     # fp32 staging runs past the region
+    assert rc(out_off=c.stage_off) == tdg.TDG_ERR_INVALID             # out overlaps the staging
+    assert rc(stage_off=c.b_off) == tdg.TDG_ERR_INVALID               # staging overlaps B
+    assert rc(out_off=c.a_off) == tdg.TDG_ERR_INVALID                 # out overlaps A
     assert rc(M=1 << 20) == tdg.TDG_ERR_NOMEM
     torch.cuda.synchronize()
     assert c.symm.status()["code"] == 0

@@ -76,3 +76,42 @@ def test_full_size_sampled():
         assert_close(flat[rows, cols], ref)
     del case
     torch.cuda.empty_cache()
+
+
+def _bf16_ulp(x):
+    e = np.floor(np.log2(np.maximum(np.abs(x), 2.0 ** -126)))
+    return 2.0 ** (e - 7)
+
+
+@pytest.mark.parametrize("M", [256, 512, 1024])   # W = 2: 128-row tiles, CTA pairs, two pairs
+def test_f32_partials_integer_bit_exact_where_bf16_partials_round(M):
+    # K = 1024: a partial reaches |.| = 4096, beyond the integers bf16 holds
+    # exactly (256), but fp32 holds every partial and the sum exactly, so the
+    # fp32-partial path must give the oracle's bits in both modes
+    inp = synth.rs_inputs(2, M, 1024, 264, "int2", seed=M + 3)
+    _, out16 = oracle.gemm_rs(inp.As, inp.Bs)
+    case = RSCase(inp, f32=True)
+    for mode in ("sm", "serial"):
+        got, _ = case.run(mode=mode)
+        assert np.array_equal(got, out16), mode
+
+
+@pytest.mark.parametrize("b_layout", [tdg.B_KN, tdg.B_NK])
+def test_f32_partials_float_within_one_ulp(b_layout):
+    # one rounding (the fp32 sum to bf16): every output within one bf16 ulp of
+    # the exact sum plus the fp32 accumulation bound 2 (K + W) 2^-24 sum|a b|
+    # (which matters only where the sum cancels), and no worse than the
+    # bf16-partial path
+    W, M, K, N = 4, 2048, 320, 520
+    inp = synth.rs_inputs(W, M, K, N, "normal", seed=31)
+    out64, _ = oracle.gemm_rs(inp.As, inp.Bs)
+    absdot, _ = oracle.gemm_rs([a & 0x7FFF for a in inp.As], [b & 0x7FFF for b in inp.Bs])
+    f32 = RSCase(inp, b_layout=b_layout, f32=True)
+    got, _ = f32.run(mode="sm")
+    got64 = (got.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    bound = _bf16_ulp(out64) + 2 * (K + W) * 2.0 ** -24 * absdot
+    assert np.all(np.abs(got64 - out64) <= bound)
+    assert_close(got, out64)
+    bf16, _ = RSCase(inp, b_layout=b_layout).run(mode="sm")
+    b64 = (bf16.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    assert np.max(np.abs(got64 - out64)) <= np.max(np.abs(b64 - out64))

@@ -206,6 +206,8 @@ template <int BMN> struct AgPolicy {
         return BMN ? (uint32_t)(((cols + 63) >> 6) * 8192) : (uint32_t)((p.pair ? gm::BN / 2 : gm::BN) * gm::BK * 2);
     }
 
+    static constexpr bool F32_OUT = false; // C is always bf16
+
     __device__ static void store_chunk(const Params &p, const TileInfo &t, const void *buf, int ch, int q)
     {
         const int row = t.m0 + 32 * q;

@@ -87,6 +87,16 @@ bool map_bf16_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uin
                         CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+bool map_f32_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2,
+                uint64_t s1_bytes, uint64_t s2_bytes, uint32_t b0, uint32_t b1, uint32_t b2)
+{
+    const uint64_t dims[3] = {d0, d1, d2};
+    const uint64_t str[2] = {s1_bytes, s2_bytes};
+    const uint32_t box[3] = {b0, b1, b2};
+    return encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, str, box,
+                        CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
 bool stream_write_u32(cudaStream_t s, uint32_t *dev_addr, uint32_t value)
 {
     static PFN_writeValue32_t fn = reinterpret_cast<PFN_writeValue32_t>(driver_fn("cuStreamWriteValue32"));

@@ -12,7 +12,8 @@
 //               instruction) into one of two TMEM accumulators (2 x 256 fp32
 //               columns) and frees ring slots with tcgen05.commit.
 //   warps 2..5  epilogue: tcgen05.ld -> bf16 (round to nearest even) ->
-//               128B-swizzled staging -> TMA store; then the policy's
+//               128B-swizzled staging -> TMA store (or fp32 as it is, when the
+//               policy asks); then the policy's
 //               after-tile hook (the GEMM+RS signal and reduction).
 //
 // Three shapes of the same pipeline (template parameter CL, CTAs per cluster):
@@ -115,6 +116,11 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p)
 //        and multicasts each to CTA `half` of both pairs)
 //   __device__ static uint32_t b_bytes(const Params&, const TileInfo&, int cols);
 //   __device__ static void store_chunk(const Params&, const TileInfo&, const void *buf, int ch, int q);
+//       (stores the bf16 rows [32q, 32q + 32) x columns [64ch, 64ch + 64) staged in buf)
+//   static constexpr bool F32_OUT;  // true: the policy may ask for fp32 output, then
+//   __device__ static bool out_f32(const Params&);
+//   __device__ static void store_chunk_f32(const Params&, const TileInfo&, const void *buf, int sub, int q);
+//       (fp32 rows [32q, 32q + 32) x columns [32sub, 32sub + 32))
 //   __device__ static void after_tile(const Params&, const TileInfo&, int q, int lane);  // per epilogue warp
 // The load hooks receive the mbarrier as a shared::cluster address (the pair
 // leader's barrier when CL >= 2) and issue pair TMA when CL >= 2.  All
@@ -326,6 +332,31 @@ __device__ void gemm_consumer(const typename P::Params &p, uint8_t *smem, int un
                 tmem_ld_32x32b_x32(taddr, r0);
                 tmem_ld_32x32b_x32(taddr + 32, r1);
                 tmem_ld_wait();
+                if constexpr (P::F32_OUT) {
+                    if (P::out_f32(p)) {
+                        // fp32 output: two 32-column chunks, stored as they are
+#pragma unroll
+                        for (int hf = 0; hf < 2; ++hf) {
+                            const uint32_t *src = hf ? r1 : r0;
+                            if (lane == 0)
+                                bulk_wait_read<1>();
+                            __syncwarp();
+                            uint8_t *frow = bufs + buf * EPI_BUF + lane * 128;
+#pragma unroll
+                            for (int j = 0; j < 8; ++j)
+                                *reinterpret_cast<uint4 *>(frow + ((j ^ (lane & 7)) << 4)) =
+                                    make_uint4(src[4 * j], src[4 * j + 1], src[4 * j + 2], src[4 * j + 3]);
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) {
+                                P::store_chunk_f32(p, ti, bufs + buf * EPI_BUF, 2 * ch + hf, q);
+                                bulk_commit();
+                            }
+                            buf ^= 1;
+                        }
+                        continue;
+                    }
+                }
                 if (lane == 0)
                     bulk_wait_read<1>();
                 __syncwarp();

@@ -54,6 +54,9 @@ bool map_bf16_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t oute
 // bf16 3-D map (dim 2 stride given in bytes, e.g. the region size).
 bool map_bf16_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2,
                  uint64_t s1_bytes, uint64_t s2_bytes, uint32_t b0, uint32_t b1, uint32_t b2);
+// The same for fp32 elements.
+bool map_f32_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2,
+                uint64_t s1_bytes, uint64_t s2_bytes, uint32_t b0, uint32_t b1, uint32_t b2);
 
 // cuStreamWriteValue32 (stream-ordered flag write, with the default memory
 // barrier before the write).  Returns false when unavailable or failing.

@@ -26,7 +26,7 @@ namespace tdg {
 struct RsParams {
     CUtensorMap tmA; // {K, M, W}, plane stride = region bytes, box {64, 128, 1}
     CUtensorMap tmB; // KN: {N, K, W} box {64, 64, 1}; NK: {K, N, W} box {64, 256, 1}
-    CUtensorMap tmS; // staging {256, rows per owner, W}, box {64, 32, 1}
+    CUtensorMap tmS; // staging {256, rows per owner, W}: bf16 box {64, 32, 1}, fp32 box {32, 32, 1}
     DevStatus *status;
     uint32_t epoch;
     uint64_t timeout_ns;      // bound of a cross-CTA signal wait
@@ -47,17 +47,20 @@ struct RsParams {
     uint64_t stage_off, out_off;
     uint32_t *counters;
     uint64_t nsig;
+    int f32; // 1: partials are pushed as fp32, 0: as bf16
 };
 
 __device__ __forceinline__ uint8_t *rs_stage_row(const RsParams &p, int o, int r, int m_loc, int pn, int row)
 {
     const uint64_t idx = ((uint64_t)r * p.mt + m_loc) * p.n_tiles + pn;
-    return p.regions + (uint64_t)o * p.region_bytes + p.stage_off + (idx * 128 + row) * 512;
+    return p.regions + (uint64_t)o * p.region_bytes + p.stage_off + ((idx * 128 + row) << (p.f32 ? 10 : 9));
 }
 
 // Sum the W partial rows [row0, row0 + 32) of tile (o, m_loc, pn) in rank
 // order and write the bf16 result into out_o.  One warp; lane l owns columns
-// [8l, 8l + 8) of the tile.
+// [8l, 8l + 8) of the tile, which are one 16-byte unit of each bf16 partial
+// row or two units of each fp32 one (p.f32); the units are loaded one after
+// the other, so both forms keep the same 4 rows x 8 ranks in flight.
 __device__ void rs_reduce_rows(const RsParams &p, int o, int m_loc, int pn, int n_valid, int row0, int lane)
 {
     const int col = lane * 8;
@@ -65,6 +68,9 @@ __device__ void rs_reduce_rows(const RsParams &p, int o, int m_loc, int pn, int 
         return;
     uint8_t *out_base = p.regions + (uint64_t)o * p.region_bytes + p.out_off;
     const int64_t n0 = (int64_t)pn * gm::BN;
+    const bool f32 = p.f32 != 0;
+    const int units = f32 ? 2 : 1;
+    const int lane_off = col * (f32 ? 4 : 2);
     constexpr int RR = 4; // rows in flight per lane: RR x 8 ranks x 16 B
     for (int rr = 0; rr < 32; rr += RR) {
         float acc[RR][8];
@@ -73,28 +79,40 @@ __device__ void rs_reduce_rows(const RsParams &p, int o, int m_loc, int pn, int 
 #pragma unroll
             for (int j = 0; j < 8; ++j)
                 acc[a][j] = 0.f;
-        for (int r0 = 0; r0 < p.W; r0 += 8) {
-            uint4 v[RR][8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                if (r0 + j < p.W) {
+        for (int u = 0; u < 2; ++u) {
+            if (u >= units)
+                break;
+            for (int r0 = 0; r0 < p.W; r0 += 8) {
+                uint4 v[RR][8];
 #pragma unroll
-                    for (int a = 0; a < RR; ++a)
-                        v[a][j] = __ldcg(reinterpret_cast<const uint4 *>(
-                            rs_stage_row(p, o, r0 + j, m_loc, pn, row0 + rr + a) + col * 2));
+                for (int j = 0; j < 8; ++j) {
+                    if (r0 + j < p.W) {
+#pragma unroll
+                        for (int a = 0; a < RR; ++a)
+                            v[a][j] = __ldcg(reinterpret_cast<const uint4 *>(
+                                rs_stage_row(p, o, r0 + j, m_loc, pn, row0 + rr + a) + lane_off + 16 * u));
+                    }
                 }
-            }
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                if (r0 + j < p.W) {
+                for (int j = 0; j < 8; ++j) {
+                    if (r0 + j < p.W) {
 #pragma unroll
-                    for (int a = 0; a < RR; ++a) {
-                        const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&v[a][j]);
+                        for (int a = 0; a < RR; ++a) {
+                            if (f32) {
+                                const float *f = reinterpret_cast<const float *>(&v[a][j]);
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float2 f = __bfloat1622float2(h[e]);
-                            acc[a][2 * e] += f.x;
-                            acc[a][2 * e + 1] += f.y;
+                                for (int e = 0; e < 4; ++e)
+                                    acc[a][4 * u + e] += f[e];
+                            } else {
+                                const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&v[a][j]);
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    const float2 f = __bfloat1622float2(h[e]);
+                                    acc[a][2 * e] += f.x;
+                                    acc[a][2 * e + 1] += f.y;
+                                }
+                            }
                         }
                     }
                 }
@@ -207,11 +225,21 @@ template <int BMN> struct RsPolicy {
         return BMN ? (uint32_t)(((cols + 63) >> 6) * 8192) : (uint32_t)((p.pair ? gm::BN / 2 : gm::BN) * gm::BK * 2);
     }
 
-    // push: the partial tile goes to the owner's staging area
+    // push: the partial tile goes to the owner's staging area, as bf16 chunks
+    // of 64 columns or (F32_OUT, when p.f32) fp32 chunks of 32 columns
+    static constexpr bool F32_OUT = true;
+    __device__ static bool out_f32(const Params &p) { return p.f32 != 0; }
+
     __device__ static void store_chunk(const Params &p, const TileInfo &t, const void *buf, int ch, int q)
     {
         const uint64_t idx = ((uint64_t)t.a_sel * p.mt + t.m_loc) * p.n_tiles + t.pn;
         tma_store_3d(&p.tmS, buf, 64 * ch, (int)(idx * 128 + 32 * q), t.owner);
+    }
+
+    __device__ static void store_chunk_f32(const Params &p, const TileInfo &t, const void *buf, int sub, int q)
+    {
+        const uint64_t idx = ((uint64_t)t.a_sel * p.mt + t.m_loc) * p.n_tiles + t.pn;
+        tma_store_3d(&p.tmS, buf, 32 * sub, (int)(idx * 128 + 32 * q), t.owner);
     }
 
     __device__ static void after_tile(const Params &p, const TileInfo &t, int q, int lane)
@@ -285,6 +313,9 @@ extern "C" int tdg_gemm_rs(tdg_symm *h, const tdg_gemm_rs_args *a, void *stream)
         return TDG_ERR_INVALID;
     if (a->b_layout != TDG_B_KN && a->b_layout != TDG_B_NK)
         return TDG_ERR_INVALID;
+    if (a->partial_f32 != 0 && a->partial_f32 != 1)
+        return TDG_ERR_INVALID;
+    const int f32 = a->partial_f32;
     const int64_t M = a->M, K = a->K, N = a->N;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (M == 0 || N == 0)
@@ -296,11 +327,18 @@ extern "C" int tdg_gemm_rs(tdg_symm *h, const tdg_gemm_rs_args *a, void *stream)
         !aligned16(a->stage_off) || !aligned16(a->out_off) || M > INT32_MAX || K > INT32_MAX ||
         N > INT32_MAX)
         return TDG_ERR_INVALID;
-    const size_t stage_bytes = tdg_gemm_rs_stage_bytes(W, M, N);
+    const size_t stage_bytes = tdg_gemm_rs_stage_bytes(W, M, N) * (f32 ? 2 : 1);
     const uint64_t R = h->region_bytes;
-    if (a->a_off + (uint64_t)M * K * 2 > R || a->b_off + (uint64_t)K * N * 2 > R ||
-        a->stage_off + stage_bytes > R || a->out_off + (uint64_t)Mo * N * 2 > R)
+    const uint64_t a_end = a->a_off + (uint64_t)M * K * 2, b_end = a->b_off + (uint64_t)K * N * 2;
+    const uint64_t s_end = a->stage_off + stage_bytes, o_end = a->out_off + (uint64_t)Mo * N * 2;
+    if (a_end > R || b_end > R || s_end > R || o_end > R)
         return TDG_ERR_NOMEM;
+    // the buffers written (staging, out) overlap nothing else
+    auto meet = [](uint64_t x0, uint64_t x1, uint64_t y0, uint64_t y1) { return x0 < y1 && y0 < x1; };
+    if (meet(a->stage_off, s_end, a->a_off, a_end) || meet(a->stage_off, s_end, a->b_off, b_end) ||
+        meet(a->stage_off, s_end, a->out_off, o_end) || meet(a->out_off, o_end, a->a_off, a_end) ||
+        meet(a->out_off, o_end, a->b_off, b_end))
+        return TDG_ERR_INVALID;
     const int mt = (int)(Mo / gm::BM);
     const int n_tiles = (int)((N + gm::BN - 1) / gm::BN);
     if ((size_t)mt * n_tiles * 4 > h->nsig)
@@ -327,7 +365,10 @@ extern "C" int tdg_gemm_rs(tdg_symm *h, const tdg_gemm_rs_args *a, void *stream)
         ok = ok && map_bf16_3d(&p.tmB, h->base + a->b_off, K, N, W, K * 2, R, 64,
                                cl == 4 ? 64 : (pair ? 128 : 256), 1);
     const uint64_t rows_per_owner = (uint64_t)W * mt * n_tiles * gm::BM;
-    ok = ok && map_bf16_3d(&p.tmS, h->base + a->stage_off, gm::BN, rows_per_owner, W, gm::BN * 2, R, 64, 32, 1);
+    if (f32)
+        ok = ok && map_f32_3d(&p.tmS, h->base + a->stage_off, gm::BN, rows_per_owner, W, gm::BN * 4, R, 32, 32, 1);
+    else
+        ok = ok && map_bf16_3d(&p.tmS, h->base + a->stage_off, gm::BN, rows_per_owner, W, gm::BN * 2, R, 64, 32, 1);
     if (!ok)
         return TDG_ERR_CUDA;
     p.status = h->status;
@@ -358,6 +399,7 @@ extern "C" int tdg_gemm_rs(tdg_symm *h, const tdg_gemm_rs_args *a, void *stream)
     p.out_off = a->out_off;
     p.counters = h->counters;
     p.nsig = h->nsig;
+    p.f32 = f32;
 
     const void *fn;
     if (a->b_layout == TDG_B_KN)

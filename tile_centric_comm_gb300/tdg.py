@@ -58,7 +58,8 @@ class AgGemmArgs(ctypes.Structure):
 class GemmRsArgs(ctypes.Structure):
     _fields_ = [("world", ctypes.c_int), ("M", _i64), ("K", _i64), ("N", _i64), ("a_off", _sz),
                 ("b_off", _sz), ("stage_off", _sz), ("out_off", _sz), ("b_layout", ctypes.c_int),
-                ("mode", ctypes.c_int), ("timeout_ns", _u64), ("owner_block", ctypes.c_int)]
+                ("mode", ctypes.c_int), ("timeout_ns", _u64), ("owner_block", ctypes.c_int),
+                ("partial_f32", ctypes.c_int)]
 
 
 class MoeArgs(ctypes.Structure):
@@ -289,10 +290,14 @@ def gemm_rs_stage_bytes(world: int, M: int, N: int) -> int:
 
 
 def gemm_rs(symm: Symm, M: int, K: int, N: int, a_off: int, b_off: int, stage_off: int,
-            out_off: int, mode="sm", b_layout=B_KN, timeout_ns=0, owner_block=0, stream=None):
+            out_off: int, mode="sm", b_layout=B_KN, timeout_ns=0, owner_block=0,
+            partial_f32=False, stream=None):
+    """partial_f32: push fp32 partials (the staging area must then hold
+    2 * gemm_rs_stage_bytes(world, M, N) bytes)."""
     a = GemmRsArgs(world=symm.world, M=M, K=K, N=N, a_off=a_off, b_off=b_off,
                    stage_off=stage_off, out_off=out_off, b_layout=b_layout,
-                   mode=MODES[mode], timeout_ns=timeout_ns, owner_block=owner_block)
+                   mode=MODES[mode], timeout_ns=timeout_ns, owner_block=owner_block,
+                   partial_f32=1 if partial_f32 else 0)
     _check(lib().tdg_gemm_rs(symm.h, ctypes.byref(a), _stream(stream)), "tdg_gemm_rs")
 
 
