@@ -513,6 +513,34 @@ def leg_moe(torch, tdg, synth, args, flush, pk):
     return extras["moe_dispatch_combine"]
 
 
+def leg_rs_f32(torch, tdg, args, flush, pk):
+    """The GEMM-RS of the step with fp32 partials (one rounding, twice the
+    staging bytes), overlapped and serial, timed in interleaved rounds."""
+    W, M, K, N = RS["W"], RS["M"], RS["K"], RS["N"]
+    a_off, b_off = 0, _align(M * K * 2)
+    s_off = _align(b_off + K * N * 2)
+    o_off = _align(s_off + 2 * tdg.gemm_rs_stage_bytes(W, M, N))
+    sym = tdg.Symm(W, _align(o_off + (M // W) * N * 2 + 1024), 65536)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(0)
+    for r in range(W):
+        sym.view(r, a_off, (M, K), torch.bfloat16).copy_(torch.randn(M, K, device="cuda", generator=g))
+        sym.view(r, b_off, (K, N), torch.bfloat16).copy_(torch.randn(K, N, device="cuda", generator=g) * 0.02)
+    call = lambda mode: (lambda: tdg.gemm_rs(sym, M, K, N, a_off, b_off, s_off, o_off, mode=mode,
+                                             partial_f32=True))
+    iv = interleaved_steps(torch, {"sm": [call("sm")], "serial": [call("serial")]}, 3,
+                           max(4, args.steps // 5), flush)
+    st = sym.status()
+    if st["code"] != 0:
+        raise RuntimeError(f"device fault in GEMM-RS with fp32 partials: {st}")
+    del sym
+    torch.cuda.empty_cache()
+    return {"workload": "the step's GEMM-RS (W=8, A_r 8192x3200, B_r 3200x5120) with fp32 partials",
+            "sm_ms": iv["sm"][0], "sm_tflops": RS_FLOP / iv["sm"][0] / 1e9,
+            "serial_ms": iv["serial"][0], "serial_tflops": RS_FLOP / iv["serial"][0] / 1e9,
+            "note": "synthetic N(0,1) A_r, 0.02*N(0,1) B_r generated on the device; modes in 3 interleaved rounds"}
+
+
 def leg_ring(torch, tdg, synth, args, flush, pk):
     extras = {}
     # ring AllReduce over the 8 logical ranks, 32 Mi float32 per rank
@@ -772,6 +800,7 @@ def main():
         extras["ag_tiny"] = leg_ag_config(
             torch, tdg, synth, args, flush, pk, 2, 64, 256, 128, "int2",
             "AG-GEMM tiny: W=2, A_r 64x256, B 256x128, integers (latency bound)", modes=("ce", "sm", "ll"))
+        extras["gemm_rs_f32_partials"] = leg_rs_f32(torch, tdg, args, flush, pk)
         extras["moe_dispatch_combine"] = leg_moe(torch, tdg, synth, args, flush, pk)
         extras["ring_allreduce"] = leg_ring(torch, tdg, synth, args, flush, pk)
         extras["flash_decode"] = leg_flash(torch, tdg, synth, args, flush, pk)

@@ -68,6 +68,34 @@ def test_rs_random_shapes_bit_exact(W, M, K, N, lay, seed):
         assert np.array_equal(got, out16), mode
 
 
+def _rs_f32_cases(n=8, seed=2027):
+    # fp32 partials hold integer partials up to 2^24 exactly, so K can reach
+    # the thousands (ragged k blocks included) and the result stays bit-exact
+    g = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        W = int(g.choice([1, 2, 4]))
+        Mo = int(g.choice([128, 256, 512]))
+        K = int(g.choice([200, 1032, 2056]))
+        N = int(g.choice([136, 264, 520]))
+        while W * W * Mo * K * N > 2_000_000_000 and Mo > 128:
+            Mo //= 2
+        lay = int(g.integers(0, 2))
+        out.append((W, W * Mo, K, N, lay, 3000 + i))
+    return out
+
+
+@pytest.mark.parametrize("W,M,K,N,lay,seed", _rs_f32_cases())
+def test_rs_f32_partials_random_shapes_bit_exact(W, M, K, N, lay, seed):
+    inp = synth.rs_inputs(W, M, K, N, "int2", seed=seed)
+    _, out16 = oracle.gemm_rs(inp.As, inp.Bs)
+    b_layout = tdg.B_KN if lay == 0 else tdg.B_NK
+    case = RSCase(inp, b_layout=b_layout, f32=True)
+    for mode in ("sm", "serial"):
+        got, _ = case.run(mode=mode)
+        assert np.array_equal(got, out16), mode
+
+
 
 def _moe_cases(n=12, seed=2026):
     g = np.random.default_rng(seed)
