@@ -43,13 +43,15 @@ def test_ag_gathered_buffer_past_4gb(mode):
     torch.cuda.empty_cache()
 
 
-def test_rs_staging_past_4gb():
-    W, M, K, N = 8, 131072, 64, 16640          # staging per region: 8 x 16384 x 16640 bf16 = 4.36 GB
+@pytest.mark.parametrize("f32", [False, True])
+def test_rs_staging_past_4gb(f32):
+    # staging per region: 8 x 16384 x 16640 partials = 4.36 GB in bf16, 8.72 GB in fp32
+    W, M, K, N = 8, 131072, 64, 16640
     inp = synth.rs_inputs(W, M, K, N, "int2", seed=7)
     Mo = M // W
     a_off, b_off = 0, align(M * K * 2)
     s_off = align(b_off + K * N * 2)
-    o_off = align(s_off + tdg.gemm_rs_stage_bytes(W, M, N))
+    o_off = align(s_off + tdg.gemm_rs_stage_bytes(W, M, N) * (2 if f32 else 1))
     assert tdg.gemm_rs_stage_bytes(W, M, N) > (1 << 32)
     symm = tdg.Symm(W, align(o_off + Mo * N * 2 + 1024), (Mo // 128) * ((N + 255) // 256) * 4)
     for r in range(W):
@@ -65,7 +67,7 @@ def test_rs_staging_past_4gb():
     # round-to-nearest-even bf16 of the exact sum
     want = oracle.f64_to_bf16(oracle.gemm_rs_sampled(inp.As, inp.Bs, rows, cols))
     for mode in ("sm", "serial"):
-        tdg.gemm_rs(symm, M, K, N, a_off, b_off, s_off, o_off, mode=mode)
+        tdg.gemm_rs(symm, M, K, N, a_off, b_off, s_off, o_off, mode=mode, partial_f32=f32)
         torch.cuda.synchronize()
         assert symm.status()["code"] == 0
         got = np.empty(len(rows), np.uint16)

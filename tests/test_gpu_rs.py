@@ -115,3 +115,26 @@ def test_f32_partials_float_within_one_ulp(b_layout):
     bf16, _ = RSCase(inp, b_layout=b_layout).run(mode="sm")
     b64 = (bf16.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
     assert np.max(np.abs(got64 - out64)) <= np.max(np.abs(b64 - out64))
+
+
+@pytest.mark.parametrize("red_rows", ["4", "8", "32"])
+def test_owed_reductions_worked_off_in_slices(red_rows, monkeypatch):
+    # many tiles per epilogue warp (W = 8, 2 x 8 quad tiles per owner), fp32
+    # partials: the last arriver queues its reduction and works it off a few
+    # rows per tile (with 4 rows a third owed reduction often finishes the
+    # oldest at once); every output must match the oracle and the separate
+    # reduction launch bit for bit (integer inputs: exact)
+    monkeypatch.setenv("TDG_RS_RED_ROWS", red_rows)
+    W, M, K, N = 8, 8192, 64, 2048
+    inp = synth.rs_inputs(W, M, K, N, "int2", seed=41)
+    case = RSCase(inp, f32=True)
+    fused, _ = case.run(mode="sm")
+    serial, _ = case.run(mode="serial")
+    assert np.array_equal(fused, serial)
+    g = np.random.default_rng(5)
+    rows = np.concatenate([g.integers(0, M, 3000), [0, M - 1]])
+    cols = np.concatenate([g.integers(0, N, 3000), [0, N - 1]])
+    want = oracle.f64_to_bf16(oracle.gemm_rs_sampled(inp.As, inp.Bs, rows, cols))
+    assert np.array_equal(fused.reshape(M, N)[rows, cols], want)
+    for o in range(W):
+        assert int(case.symm.counters(o, case.symm.nsig).abs().sum()) == 0

@@ -215,7 +215,8 @@ template <int BMN> struct AgPolicy {
             tma_store_2d(&p.tmC, buf, t.n0 + 64 * ch, row);
     }
 
-    __device__ static void after_tile(const Params &, const TileInfo &, int, int) {}
+    struct EpiState {};
+    __device__ static void after_tile(const Params &, const TileInfo &, int, int, EpiState &, bool) {}
 };
 
 // One copy worker: copy `bytes` from src to dst through its ring.  Returns

@@ -121,7 +121,10 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p)
 //   __device__ static bool out_f32(const Params&);
 //   __device__ static void store_chunk_f32(const Params&, const TileInfo&, const void *buf, int sub, int q);
 //       (fp32 rows [32q, 32q + 32) x columns [32sub, 32sub + 32))
-//   __device__ static void after_tile(const Params&, const TileInfo&, int q, int lane);  // per epilogue warp
+//   struct EpiState;  // per epilogue warp, zero-initialised, kept across its tiles
+//   __device__ static void after_tile(const Params&, const TileInfo&, int q, int lane, EpiState&,
+//                                     bool tail);  // per epilogue warp after each tile; once
+//       more with tail = true (and no tile) after the last one
 // The load hooks receive the mbarrier as a shared::cluster address (the pair
 // leader's barrier when CL >= 2) and issue pair TMA when CL >= 2.  All
 // tcgen05 and TMA instructions of one kernel use a single cta_group.
@@ -306,8 +309,16 @@ __device__ void gemm_consumer(const typename P::Params &p, uint8_t *smem, int un
         int acc = 0;
         uint32_t acc_phase = 0;
         int buf = 0;
-        for (int64_t it = unit; it < items; it += nunits) {
+        typename P::EpiState est{};
+        // after the last tile one more pass, with no tile, lets the policy
+        // finish work it deferred (a single call site keeps it inline once)
+        for (int64_t it = unit;; it += nunits) {
             TileInfo ti;
+            if (it >= items) {
+                if (!ps->abort)
+                    P::after_tile(p, ti, q, lane, est, true);
+                break;
+            }
             P::tile(p, it, ti, crank);
             if (ti.n_valid <= 0)
                 continue;
@@ -390,7 +401,7 @@ __device__ void gemm_consumer(const typename P::Params &p, uint8_t *smem, int un
                 acc = 0;
                 acc_phase ^= 1u;
             }
-            P::after_tile(p, ti, q, lane);
+            P::after_tile(p, ti, q, lane, est, false);
         }
         if (lane == 0)
             bulk_wait<0>();

@@ -48,6 +48,7 @@ struct RsParams {
     uint32_t *counters;
     uint64_t nsig;
     int f32; // 1: partials are pushed as fp32, 0: as bf16
+    int red_rows; // rows of owed reductions an epilogue warp works off per tile
 };
 
 __device__ __forceinline__ uint8_t *rs_stage_row(const RsParams &p, int o, int r, int m_loc, int pn, int row)
@@ -56,12 +57,14 @@ __device__ __forceinline__ uint8_t *rs_stage_row(const RsParams &p, int o, int r
     return p.regions + (uint64_t)o * p.region_bytes + p.stage_off + ((idx * 128 + row) << (p.f32 ? 10 : 9));
 }
 
-// Sum the W partial rows [row0, row0 + 32) of tile (o, m_loc, pn) in rank
-// order and write the bf16 result into out_o.  One warp; lane l owns columns
+// Sum the W partial rows [row0, row1) of tile (o, m_loc, pn) in rank order
+// (row1 - row0 a multiple of 4) and write the bf16 result into out_o.  One
+// warp; lane l owns columns
 // [8l, 8l + 8) of the tile, which are one 16-byte unit of each bf16 partial
 // row or two units of each fp32 one (p.f32); the units are loaded one after
 // the other, so both forms keep the same 4 rows x 8 ranks in flight.
-__device__ void rs_reduce_rows(const RsParams &p, int o, int m_loc, int pn, int n_valid, int row0, int lane)
+__device__ void rs_reduce_rows(const RsParams &p, int o, int m_loc, int pn, int n_valid, int row0, int row1,
+                               int lane)
 {
     const int col = lane * 8;
     if (col >= n_valid)
@@ -72,7 +75,7 @@ __device__ void rs_reduce_rows(const RsParams &p, int o, int m_loc, int pn, int 
     const int units = f32 ? 2 : 1;
     const int lane_off = col * (f32 ? 4 : 2);
     constexpr int RR = 4; // rows in flight per lane: RR x 8 ranks x 16 B
-    for (int rr = 0; rr < 32; rr += RR) {
+    for (int rr = row0; rr < row1; rr += RR) {
         float acc[RR][8];
 #pragma unroll
         for (int a = 0; a < RR; ++a)
@@ -91,7 +94,7 @@ __device__ void rs_reduce_rows(const RsParams &p, int o, int m_loc, int pn, int 
 #pragma unroll
                         for (int a = 0; a < RR; ++a)
                             v[a][j] = __ldcg(reinterpret_cast<const uint4 *>(
-                                rs_stage_row(p, o, r0 + j, m_loc, pn, row0 + rr + a) + lane_off + 16 * u));
+                                rs_stage_row(p, o, r0 + j, m_loc, pn, rr + a) + lane_off + 16 * u));
                     }
                 }
 #pragma unroll
@@ -120,7 +123,7 @@ __device__ void rs_reduce_rows(const RsParams &p, int o, int m_loc, int pn, int 
         }
 #pragma unroll
         for (int a = 0; a < RR; ++a) {
-            const int64_t orow = (int64_t)m_loc * gm::BM + row0 + rr + a;
+            const int64_t orow = (int64_t)m_loc * gm::BM + rr + a;
             uint4 w;
             w.x = pack_bf16x2(acc[a][0], acc[a][1]);
             w.y = pack_bf16x2(acc[a][2], acc[a][3]);
@@ -242,26 +245,66 @@ template <int BMN> struct RsPolicy {
         tma_store_3d(&p.tmS, buf, 32 * sub, (int)(idx * 128 + 32 * q), t.owner);
     }
 
-    __device__ static void after_tile(const Params &p, const TileInfo &t, int q, int lane)
+    // The reductions an epilogue warp owes, oldest first: rows [row0, 32) of
+    // its quarter of tile (o0, m0, pn0), then all of tile 1.  At most two wait;
+    // a third finishes the oldest at once.
+    struct EpiState {
+        int n;
+        int o0, m0, pn0, nv0, row0;
+        int o1, m1, pn1, nv1;
+        int o2, m2, pn2, nv2;
+    };
+
+    // After each tile: signal the push (increment the tile quarter's arrival
+    // counter); the warp whose increment completes the count of W owes the
+    // reduction of that quarter.  Each warp then works off at most red_rows
+    // rows of what it owes, so that no single tile's drain waits behind a
+    // whole 32-row reduction; the tail pass after the last tile finishes all.
+    __device__ static void after_tile(const Params &p, const TileInfo &t, int q, int lane, EpiState &st,
+                                      bool tail)
     {
         if (!p.fused_reduce)
             return;
-        uint32_t *ctr = p.counters + (uint64_t)t.owner * p.nsig +
-                        ((uint64_t)t.m_loc * p.n_tiles + t.pn) * 4 + q;
-        uint32_t old = 0;
-        if (lane == 0) {
-            bulk_wait<0>();             // this warp's pushed rows are written ...
-            fence_proxy_async_global(); // ... and ordered before the signal
-            old = atom_add_acq_rel_gpu(ctr, 1u);
+        int budget = tail ? 96 : p.red_rows;
+        if (!tail) {
+            uint32_t *ctr = p.counters + (uint64_t)t.owner * p.nsig +
+                            ((uint64_t)t.m_loc * p.n_tiles + t.pn) * 4 + q;
+            uint32_t old = 0;
+            if (lane == 0) {
+                bulk_wait<0>();             // this warp's pushed rows are written ...
+                fence_proxy_async_global(); // ... and ordered before the signal
+                old = atom_add_acq_rel_gpu(ctr, 1u);
+            }
+            old = __shfl_sync(0xffffffffu, old, 0);
+            if (old == (uint32_t)(p.W - 1)) {
+                __threadfence();
+                if (st.n == 0) {
+                    st.o0 = t.owner, st.m0 = t.m_loc, st.pn0 = t.pn, st.nv0 = t.n_valid, st.row0 = 0;
+                } else if (st.n == 1) {
+                    st.o1 = t.owner, st.m1 = t.m_loc, st.pn1 = t.pn, st.nv1 = t.n_valid;
+                } else {
+                    st.o2 = t.owner, st.m2 = t.m_loc, st.pn2 = t.pn, st.nv2 = t.n_valid;
+                    budget += 32 - st.row0; // the oldest is finished now
+                }
+                ++st.n;
+            }
         }
-        old = __shfl_sync(0xffffffffu, old, 0);
-        if (old != (uint32_t)(p.W - 1))
-            return;
-        __threadfence();
-        rs_reduce_rows(p, t.owner, t.m_loc, t.pn, t.n_valid, 32 * q, lane);
-        __syncwarp();
-        if (lane == 0)
-            st_relaxed_gpu(ctr, 0u);
+        while (st.n > 0 && budget > 0) {
+            const int rows = min(budget, 32 - st.row0);
+            rs_reduce_rows(p, st.o0, st.m0, st.pn0, st.nv0, 32 * q + st.row0, 32 * q + st.row0 + rows, lane);
+            st.row0 += rows;
+            budget -= rows;
+            if (st.row0 == 32) {
+                __syncwarp();
+                if (lane == 0) // ready for the next call
+                    st_relaxed_gpu(p.counters + (uint64_t)st.o0 * p.nsig +
+                                       ((uint64_t)st.m0 * p.n_tiles + st.pn0) * 4 + q,
+                                   0u);
+                st.o0 = st.o1, st.m0 = st.m1, st.pn0 = st.pn1, st.nv0 = st.nv1, st.row0 = 0;
+                st.o1 = st.o2, st.m1 = st.m2, st.pn1 = st.pn2, st.nv1 = st.nv2;
+                --st.n;
+            }
+        }
     }
 };
 
@@ -282,7 +325,8 @@ __global__ void __launch_bounds__(128) rs_reduce_kernel(const __grid_constant__ 
     const int rem = (int)(tile % per_owner);
     const int m_loc = rem / p.n_tiles, pn = rem % p.n_tiles;
     const int n_valid = (int)min((int64_t)gm::BN, p.N - (int64_t)pn * gm::BN);
-    rs_reduce_rows(p, o, m_loc, pn, n_valid, 32 * (threadIdx.x >> 5), threadIdx.x & 31);
+    const int row0 = 32 * (int)(threadIdx.x >> 5);
+    rs_reduce_rows(p, o, m_loc, pn, n_valid, row0, row0 + 32, threadIdx.x & 31);
 }
 
 } // namespace tdg
@@ -400,6 +444,15 @@ extern "C" int tdg_gemm_rs(tdg_symm *h, const tdg_gemm_rs_args *a, void *stream)
     p.counters = h->counters;
     p.nsig = h->nsig;
     p.f32 = f32;
+    // measured at the Qwen-32B down-projection shape: a bf16 quarter's
+    // reduction fits in the slack of one tile, so it is done at once; an fp32
+    // one (twice the bytes) goes fastest in slices of 8 rows per tile
+    p.red_rows = f32 ? 8 : 32;
+    if (const char *rr = getenv("TDG_RS_RED_ROWS")) {
+        const int v = atoi(rr);
+        if (v >= 4 && v <= 32 && 32 % v == 0)
+            p.red_rows = v;
+    }
 
     const void *fn;
     if (a->b_layout == TDG_B_KN)
