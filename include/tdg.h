@@ -131,6 +131,7 @@ typedef struct {
 #define TDG_WHERE_LL 3         /* LL receiver waiting on a data+flag word     */
 #define TDG_WHERE_MOE_EXPERT 4 /* an expert id outside [0, E)                 */
 #define TDG_WHERE_RING 5       /* ring AllReduce waiting on a tile of a step   */
+#define TDG_WHERE_RS_SIGNAL 6  /* GEMM-RS arrival counter update did not settle */
 
 /*
  * Copy the status block to *out (may be NULL) after synchronising `stream`,
@@ -211,8 +212,10 @@ TDG_API int tdg_ag_gemm(tdg_symm *h, const tdg_ag_gemm_args *args, void *stream,
  * tdg_gemm_rs_stage_bytes), then increments the owner's per-tile arrival
  * counter with release semantics.  The CTA whose increment completes the
  * count of W acquires it, sums the W partials in fixed rank order in fp32
- * and writes the bf16 result, then resets the counter to 0.  SERIAL mode
- * runs the GEMM for all partials first and the reduction after it.
+ * and writes the bf16 result.  Each counter word carries the call's epoch
+ * next to its count, so a count left by an earlier call (one that ended on
+ * a fault) is ignored.  SERIAL mode runs the GEMM for all partials first
+ * and the reduction after it.
  * partial_f32 = 1 pushes the partial tiles as fp32 instead of bf16: the
  * staging area is twice tdg_gemm_rs_stage_bytes(), and the only rounding is
  * the final one of the fp32 sum to bf16 (the pages leave the partial type

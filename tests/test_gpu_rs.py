@@ -138,3 +138,29 @@ def test_owed_reductions_worked_off_in_slices(red_rows, monkeypatch):
     assert np.array_equal(fused.reshape(M, N)[rows, cols], want)
     for o in range(W):
         assert int(case.symm.counters(o, case.symm.nsig).abs().sum()) == 0
+
+
+@pytest.mark.parametrize("f32", [False, True])
+def test_counts_left_by_an_earlier_call_are_ignored(f32):
+    # an earlier call that ended early (on a fault, say) can leave arrival
+    # counts behind; emulate that on the host by writing counter words tagged
+    # with the last epoch used (the one before tdg_symm_epoch, which names the
+    # next call's) and counts 1..W-1: the next call must ignore them and give
+    # the oracle's bits
+    W = 4
+    inp = synth.rs_inputs(W, 2048, 64, 520, "int2", seed=43)
+    _, out16 = oracle.gemm_rs(inp.As, inp.Bs)
+    case = RSCase(inp, f32=f32)
+    g = np.random.default_rng(7)
+    for _ in range(2):
+        tag = ((case.symm.epoch() - 1) & 0x01FFFFFF) << 7
+        stage = tdg.gemm_rs_stage_bytes(W, inp.M, inp.N) * (2 if f32 else 1)
+        for o in range(W):
+            n = case.symm.nsig
+            stale = (tag | g.integers(1, W, n)).astype(np.uint32).view(np.int32)
+            case.symm.counters(o, n).copy_(torch.from_numpy(stale))
+            # NaN in the staging area: a reduction that started before all W
+            # pushes landed would read it
+            case.symm.view(o, case.stage_off, (stage // 2,), torch.int16).fill_(0x7FC1)
+        got, _ = case.run(mode="sm")
+        assert np.array_equal(got, out16)

@@ -121,6 +121,15 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p)
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
+__device__ __forceinline__ uint32_t atom_cas_acq_rel_gpu(uint32_t *p, uint32_t cmp, uint32_t v)
+{
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.cas.b32 %0, [%1], %2, %3;"
+                 : "=r"(old)
+                 : "l"(p), "r"(cmp), "r"(v)
+                 : "memory");
+    return old;
+}
 __device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t *p, uint32_t v)
 {
     uint32_t old;

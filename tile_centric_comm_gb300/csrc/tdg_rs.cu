@@ -11,11 +11,13 @@
 // partial tile (tile-contiguous, 128 x 256) into owner o's staging area
 // (region o) with TMA, waits for the write to complete, fences the async
 // proxy, and increments the owner's per-(tile, row-quarter) arrival counter
-// with acq_rel semantics (the pages' "increment" signal).  The epilogue warp
-// whose increment completes the count of W acquires the other W-1 pushes,
-// sums the W partials of its 32 rows in fixed rank order (fp32, 16-byte
-// coalesced loads), writes the bf16 rows of out_o and resets the counter.
-// No CTA ever spins on another: the last arriver does the work.
+// with acq_rel semantics (the pages' "increment" signal; the counter word is
+// tagged with the call's epoch).  The epilogue warp whose increment completes
+// the count of W acquires the other W-1 pushes and owes the reduction of its
+// 32 rows: summing the W partials in fixed rank order (fp32, 16-byte
+// coalesced loads) and writing the bf16 rows of out_o, all at once or a few
+// rows after each of its next tiles.  No CTA ever spins on another: the last
+// arriver does the work.
 // SERIAL mode: the GEMM stores every partial, then a separate reduction
 // launch (all SMs) sums them -- same arithmetic, no overlap.
 #include "tdg_gemm.cuh"
@@ -132,6 +134,27 @@ __device__ void rs_reduce_rows(const RsParams &p, int o, int m_loc, int pn, int 
             *reinterpret_cast<uint4 *>(out_base + ((uint64_t)orow * p.N + n0 + col) * 2) = w;
         }
     }
+}
+
+// The push signal of a tile quarter: increment its arrival counter and return
+// the count before this push.  The word holds the call's epoch in bits 31..7
+// (its low 25 bits) and the count in bits 6..0 (W <= 64), so a word left by
+// an earlier call -- one that ended early on a fault, say -- counts as 0
+// instead of corrupting this call.  A CAS that keeps losing (it cannot: each
+// loss is another push landing) is bounded and reported.
+__device__ __forceinline__ uint32_t rs_arrive(const RsParams &p, uint32_t *ctr)
+{
+    const uint32_t tag = (p.epoch & 0x01FFFFFFu) << 7;
+    uint32_t v = *reinterpret_cast<volatile uint32_t *>(ctr);
+    for (int i = 0; i < 4096; ++i) {
+        const bool same = (v & ~0x7Fu) == tag;
+        const uint32_t seen = atom_cas_acq_rel_gpu(ctr, v, same ? v + 1 : (tag | 1u));
+        if (seen == v)
+            return same ? (v & 0x7Fu) : 0u;
+        v = seen;
+    }
+    report_fault(p.status, TDG_ERR_TIMEOUT, TDG_WHERE_RS_SIGNAL, 0, p.epoch);
+    return 0xFFFFFFFFu; // never the last arriver
 }
 
 template <int BMN> struct RsPolicy {
@@ -273,7 +296,7 @@ template <int BMN> struct RsPolicy {
             if (lane == 0) {
                 bulk_wait<0>();             // this warp's pushed rows are written ...
                 fence_proxy_async_global(); // ... and ordered before the signal
-                old = atom_add_acq_rel_gpu(ctr, 1u);
+                old = rs_arrive(p, ctr);
             }
             old = __shfl_sync(0xffffffffu, old, 0);
             if (old == (uint32_t)(p.W - 1)) {
@@ -296,7 +319,7 @@ template <int BMN> struct RsPolicy {
             budget -= rows;
             if (st.row0 == 32) {
                 __syncwarp();
-                if (lane == 0) // ready for the next call
+                if (lane == 0) // tidy; any value from an earlier call counts as 0
                     st_relaxed_gpu(p.counters + (uint64_t)st.o0 * p.nsig +
                                        ((uint64_t)st.m0 * p.n_tiles + st.pn0) * 4 + q,
                                    0u);

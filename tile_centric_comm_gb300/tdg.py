@@ -27,7 +27,7 @@ MODE_SM, MODE_CE, MODE_LL, MODE_SERIAL = 0, 1, 2, 3
 MODES = {"sm": MODE_SM, "ce": MODE_CE, "ll": MODE_LL, "serial": MODE_SERIAL}
 B_KN, B_NK = 0, 1
 MOE_ROUTE, MOE_DISPATCH, MOE_COMBINE, MOE_ALL = 1, 2, 4, 7
-WHERE = {1: "ag_flag", 2: "pipe", 3: "ll", 4: "moe_expert", 5: "ring"}
+WHERE = {1: "ag_flag", 2: "pipe", 3: "ll", 4: "moe_expert", 5: "ring", 6: "rs_signal"}
 
 # every symbol include/tdg.h declares
 EXPORTS = [
