@@ -272,6 +272,9 @@ typedef struct {
     int64_t tile_elems;  /* elements per signalled tile (0 = 65536)            */
     int ctas_per_rank;   /* 0 = default                                        */
     uint64_t timeout_ns; /* bound of every device wait; 0 = 2 s                */
+    uint64_t test_skip_signal; /* tests only: when nonzero, the notify of rank
+                                  0's signal test_skip_signal - 1 is skipped,
+                                  so rank 0's wait on it runs out            */
 } tdg_allreduce_args;
 
 TDG_API size_t tdg_allreduce_recv_bytes(int world, int64_t count);

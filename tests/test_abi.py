@@ -57,7 +57,7 @@ int main(void) {
   F(tdg_gemm_rs_args, out_off); F(tdg_gemm_rs_args, timeout_ns); F(tdg_gemm_rs_args, partial_f32);
   printf("tdg_allreduce_args %zu\n", sizeof(tdg_allreduce_args));
   printf("tdg_flash_decode_args %zu\n", sizeof(tdg_flash_decode_args));
-  F(tdg_allreduce_args, timeout_ns); F(tdg_flash_decode_args, out); F(tdg_flash_decode_args, scale);
+  F(tdg_allreduce_args, timeout_ns); F(tdg_allreduce_args, test_skip_signal); F(tdg_flash_decode_args, out); F(tdg_flash_decode_args, scale);
   F(tdg_moe_args, recv); F(tdg_moe_args, workspace_bytes); F(tdg_moe_args, phases);
   return 0;
 }

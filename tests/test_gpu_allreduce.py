@@ -68,3 +68,19 @@ def test_degenerate_and_invalid():
     one = tdg.Symm(1, 4096, 64)
     tdg.allreduce(one, 16, 0, 2048)                                # single rank: no-op
     torch.cuda.synchronize()
+
+
+def test_missing_signal_times_out_then_next_call_succeeds():
+    # host-side injection: rank 0's signal for (step 2, tile 1) is never
+    # notified; rank 0's bounded wait must run out and report it, the launch
+    # must still end, and the next call (a new epoch) must give the sum
+    W, count, tile = 4, 4 * 4096, 1024
+    tiles = (count // W) // tile
+    case = RingCase(W, count, seed=3, integer=True)
+    want = oracle.allreduce(case.xs)
+    sig = 2 * tiles + 1
+    _, st = case.run(check_status=False, tile_elems=tile, timeout_ns=20_000_000, test_skip_signal=sig + 1)
+    assert st["code"] == tdg.TDG_ERR_TIMEOUT and st["where"] == "ring" and st["index"] == sig
+    outs, st = case.run(tile_elems=tile)
+    for r in range(W):
+        assert np.array_equal(outs[r].astype(np.float64), want), r

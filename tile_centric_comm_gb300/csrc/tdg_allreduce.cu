@@ -31,6 +31,7 @@ struct RingParams {
     uint64_t x_off, recv_off;
     uint32_t *flags;  // rank 0's flag words
     uint64_t nsig;    // flag words per rank
+    uint64_t skip;    // tests only: rank 0's signal skip - 1 is never notified (0: none)
 };
 
 __device__ __forceinline__ float *ring_x(const RingParams &p, int r, int c)
@@ -63,7 +64,7 @@ __device__ __forceinline__ void ring_wait(const RingParams &p, int r, int step, 
 __device__ __forceinline__ void ring_notify(const RingParams &p, int r, int step, int64_t t)
 {
     __syncthreads();
-    if (threadIdx.x == 0) {
+    if (threadIdx.x == 0 && !(p.skip && r == 0 && (uint64_t)step * p.tiles + t == p.skip - 1)) {
         __threadfence();
         st_release_gpu(ring_flag(p, r, step, t), p.epoch);
     }
@@ -207,6 +208,7 @@ extern "C" int tdg_allreduce(tdg_symm *h, const tdg_allreduce_args *a, void *str
     p.recv_off = a->recv_off;
     p.flags = h->flags;
     p.nsig = h->nsig;
+    p.skip = a->test_skip_signal;
     void *args[] = {&p};
     return cuda_err(launch(fn, dim3(W * G), dim3(256), 0, static_cast<cudaStream_t>(stream), args, true),
                     "allreduce launch");

@@ -72,7 +72,8 @@ class MoeArgs(ctypes.Structure):
 
 class AllReduceArgs(ctypes.Structure):
     _fields_ = [("world", ctypes.c_int), ("count", _i64), ("x_off", _sz), ("recv_off", _sz),
-                ("tile_elems", _i64), ("ctas_per_rank", ctypes.c_int), ("timeout_ns", _u64)]
+                ("tile_elems", _i64), ("ctas_per_rank", ctypes.c_int), ("timeout_ns", _u64),
+                ("test_skip_signal", _u64)]
 
 
 class FlashDecodeArgs(ctypes.Structure):
@@ -306,9 +307,10 @@ def allreduce_recv_bytes(world: int, count: int) -> int:
 
 
 def allreduce(symm: Symm, count: int, x_off: int, recv_off: int, tile_elems=0, ctas_per_rank=0,
-              timeout_ns=0, stream=None):
+              timeout_ns=0, test_skip_signal=0, stream=None):
     a = AllReduceArgs(world=symm.world, count=count, x_off=x_off, recv_off=recv_off,
-                      tile_elems=tile_elems, ctas_per_rank=ctas_per_rank, timeout_ns=timeout_ns)
+                      tile_elems=tile_elems, ctas_per_rank=ctas_per_rank, timeout_ns=timeout_ns,
+                      test_skip_signal=test_skip_signal)
     _check(lib().tdg_allreduce(symm.h, ctypes.byref(a), _stream(stream)), "tdg_allreduce")
 
 
