@@ -310,8 +310,8 @@ __device__ void gemm_consumer(const typename P::Params &p, uint8_t *smem, int un
         uint32_t acc_phase = 0;
         int buf = 0;
         typename P::EpiState est{};
-        // after the last tile one more pass, with no tile, lets the policy
-        // finish work it deferred (a single call site keeps it inline once)
+        // after the last tile, one more pass with no tile (tail = true) lets
+        // the policy finish work it deferred
         for (int64_t it = unit;; it += nunits) {
             TileInfo ti;
             if (it >= items) {
