@@ -401,7 +401,7 @@ def interleaved_steps(torch, variants, rounds, steps, flush):
     return {n: [statistics.mean(x) for x in acc[n]] for n in names}
 
 
-def cpu_oracle_rate(sample_rows_ag=256, sample_rows_rs=64):
+def cpu_oracle_rate(sample_rows_ag=1280, sample_rows_rs=320):
     """The oracle, as it stands, on a bounded sample of the same workload:
     full output rows of AG-GEMM and GEMM-RS.  Returns (TFLOP/s, seconds, desc)."""
     import numpy as np
