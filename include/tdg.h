@@ -198,6 +198,46 @@ typedef struct {
 TDG_API int tdg_ag_gemm(tdg_symm *h, const tdg_ag_gemm_args *args, void *stream,
                 void *side_stream);
 
+/* ---- AllGather + GEMM for every rank at once ------------------------------ */
+/*
+ * For every rank r: C_r = concat_rows(A_0, ..., A_{W-1}) @ B_r -- the
+ * AllGather+GEMM of the previous entry point run by all W ranks in one call
+ * ("Triton-distributed 语义", 内核设计模式 "AllGather + GEMM 重叠", every PE;
+ * paper summary, 方法: intra-node AllGather on the copy engine), W times the
+ * work of one rank's call.
+ *
+ * Shard A_r (Ms x K bf16) at region(r) + a_off; rank r's gathered M x K
+ * buffer (M = W*Ms) at region(r) + g_off, shard s at rows [s*Ms, (s+1)*Ms);
+ * B_r (K x N with TDG_B_KN, N x K with TDG_B_NK) at region(r) + b_off; C_r
+ * (M x N bf16) at region(r) + c_off.  Rank r's flag words g = row /
+ * signal_rows of its gathered rows are set to the call's epoch.
+ * CE mode: one persistent GEMM launch on `stream` runs every rank's tiles,
+ * rank after rank, each rank's m tiles in the swizzled order (its own shard
+ * first, read in place when Ms is a whole number of tiles) and waits (bounded)
+ * on the flags of the rows it reads; the W x W shard copies run on
+ * `side_stream` (cudaMemcpyAsync, then a stream-ordered flag write), rank by
+ * rank.  SERIAL mode: the copies, then the GEMM, on `stream`.
+ * Requirements: 1 <= world <= 64; K % 8 == 0; N % 8 == 0; offsets 16-byte
+ * aligned; every buffer inside its region (else TDG_ERR_NOMEM); the gathered
+ * buffers and C_r overlapping no other buffer (else TDG_ERR_INVALID);
+ * signal_rows dividing Ms; M / signal_rows <= signals_per_rank.  M == 0 or
+ * N == 0 is a no-op; K == 0 writes C_r = 0.
+ */
+typedef struct {
+    int world;
+    int64_t Ms, K, N;
+    size_t a_off, g_off, b_off, c_off;
+    int b_layout;        /* TDG_B_KN or TDG_B_NK                              */
+    int mode;            /* TDG_MODE_CE or TDG_MODE_SERIAL                    */
+    int64_t signal_rows; /* rows per signal; 0 = Ms (one per shard)           */
+    uint64_t timeout_ns; /* bound of every device wait; 0 = 2 s               */
+    uint64_t test_skip_notify; /* tests only: rank 0's flag of signal group g
+                                  is not written when bit (g % 64) is set     */
+} tdg_ag_gemm_all_args;
+
+TDG_API int tdg_ag_gemm_all_ranks(tdg_symm *h, const tdg_ag_gemm_all_args *args, void *stream,
+                                  void *side_stream);
+
 /* ---- GEMM + ReduceScatter -------------------------------------------------- */
 /*
  * out_o = rows [o*Mo, (o+1)*Mo) of sum_r A_r @ B_r, Mo = M / W, for every

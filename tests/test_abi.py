@@ -56,6 +56,8 @@ int main(void) {
   F(tdg_ag_gemm_args, test_skip_notify);
   F(tdg_gemm_rs_args, out_off); F(tdg_gemm_rs_args, timeout_ns); F(tdg_gemm_rs_args, partial_f32);
   printf("tdg_allreduce_args %zu\n", sizeof(tdg_allreduce_args));
+  printf("tdg_ag_gemm_all_args %zu\n", sizeof(tdg_ag_gemm_all_args));
+  F(tdg_ag_gemm_all_args, c_off); F(tdg_ag_gemm_all_args, signal_rows); F(tdg_ag_gemm_all_args, test_skip_notify);
   printf("tdg_flash_decode_args %zu\n", sizeof(tdg_flash_decode_args));
   F(tdg_allreduce_args, timeout_ns); F(tdg_allreduce_args, test_skip_signal); F(tdg_flash_decode_args, out); F(tdg_flash_decode_args, scale);
   F(tdg_moe_args, recv); F(tdg_moe_args, workspace_bytes); F(tdg_moe_args, phases);
@@ -73,12 +75,14 @@ int main(void) {
     assert int(got["tdg_fault"]) == ctypes.sizeof(tdg.TdgFault)
     assert int(got["tdg_allreduce_args"]) == ctypes.sizeof(tdg.AllReduceArgs)
     assert int(got["tdg_flash_decode_args"]) == ctypes.sizeof(tdg.FlashDecodeArgs)
+    assert int(got["tdg_ag_gemm_all_args"]) == ctypes.sizeof(tdg.AgGemmAllArgs)
     for key, val in got.items():
         if "." in key:
             s, f = key.split(".")
             cls = {"tdg_ag_gemm_args": tdg.AgGemmArgs, "tdg_gemm_rs_args": tdg.GemmRsArgs,
                    "tdg_moe_args": tdg.MoeArgs, "tdg_allreduce_args": tdg.AllReduceArgs,
-                   "tdg_flash_decode_args": tdg.FlashDecodeArgs}[s]
+                   "tdg_flash_decode_args": tdg.FlashDecodeArgs,
+                   "tdg_ag_gemm_all_args": tdg.AgGemmAllArgs}[s]
             assert getattr(cls, f).offset == int(val), key
 
 

@@ -145,3 +145,28 @@ def test_binding_refuses_tensors_it_cannot_describe():
     got, _ = c.run(rank=0, mode="sm")                                  # nothing was launched
     import oracle
     assert np.array_equal(got, oracle.ag_gemm(inp.shards, inp.B)[1])
+
+
+def test_ag_gemm_all_ranks_rejections():
+    from test_gpu_ag_all import AGAllCase
+    inp = synth.ag_all_inputs(2, 128, 64, 256, "int2", seed=7)
+    c = AGAllCase(inp)
+
+    def rc(side=None, **kw):
+        a = tdg.AgGemmAllArgs(world=2, Ms=128, K=64, N=256, a_off=c.a_off, g_off=c.g_off,
+                              b_off=c.b_off, c_off=c.c_off, b_layout=tdg.B_KN, mode=tdg.MODE_SERIAL)
+        for key, v in kw.items():
+            setattr(a, key, v)
+        cur = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        return tdg.lib().tdg_ag_gemm_all_ranks(c.symm.h, ctypes.byref(a), cur, ctypes.c_void_p(side))
+    assert rc(mode=tdg.MODE_SM) == tdg.TDG_ERR_INVALID                # CE or SERIAL only
+    assert rc(mode=tdg.MODE_CE) == tdg.TDG_ERR_INVALID                # CE needs a side stream
+    assert rc(N=250) == tdg.TDG_ERR_INVALID
+    assert rc(b_off=8) == tdg.TDG_ERR_INVALID                         # misaligned
+    assert rc(c_off=c.b_off) == tdg.TDG_ERR_INVALID                   # C overlaps B
+    assert rc(g_off=c.a_off) == tdg.TDG_ERR_INVALID                   # gathered overlaps the shard
+    assert rc(signal_rows=48) == tdg.TDG_ERR_INVALID                  # does not divide Ms
+    assert rc(world=3) == tdg.TDG_ERR_INVALID
+    assert rc(Ms=1 << 20) == tdg.TDG_ERR_NOMEM
+    torch.cuda.synchronize()
+    assert c.symm.status()["code"] == 0

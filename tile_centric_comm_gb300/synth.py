@@ -81,6 +81,26 @@ def ag_inputs(W: int, Ms: int, K: int, N: int, dist: str = "normal",
     return AGInputs(shards, B, W, Ms, K, N)
 
 
+@dataclass
+class AGAllInputs:
+    shards: list          # W arrays (Ms, K)
+    Bs: list              # W arrays (K, N): rank r's weight shard
+    W: int
+    Ms: int
+    K: int
+    N: int
+
+
+def ag_all_inputs(W: int, Ms: int, K: int, N: int, dist: str = "normal",
+                  seed: int = 0, b_std: float = 0.02) -> AGAllInputs:
+    """Inputs of the AllGather+GEMM of every rank: the W shards, then W weight
+    shards B_r, drawn in that order."""
+    g = rng(seed)
+    shards = [draw(g, (Ms, K), dist) for _ in range(W)]
+    Bs = [draw(g, (K, N), dist, 1.0 if dist == "int2" else b_std) for _ in range(W)]
+    return AGAllInputs(shards, Bs, W, Ms, K, N)
+
+
 # ------------------------------------------------------------------ RS ----
 @dataclass
 class RSInputs:

@@ -33,7 +33,7 @@ WHERE = {1: "ag_flag", 2: "pipe", 3: "ll", 4: "moe_expert", 5: "ring", 6: "rs_si
 EXPORTS = [
     "tdg_symm_bytes", "tdg_symm_alloc", "tdg_symm_free", "tdg_symm_region", "tdg_symm_at",
     "tdg_symm_flags", "tdg_symm_counters", "tdg_symm_epoch", "tdg_status", "tdg_strerror",
-    "tdg_device_info", "tdg_ag_gemm", "tdg_gemm_rs_stage_bytes", "tdg_gemm_rs",
+    "tdg_device_info", "tdg_ag_gemm", "tdg_ag_gemm_all_ranks", "tdg_gemm_rs_stage_bytes", "tdg_gemm_rs",
     "tdg_moe_workspace_bytes", "tdg_moe_dispatch_combine", "tdg_moe_dispatch_combine_noalloc",
     "tdg_allreduce_recv_bytes", "tdg_allreduce", "tdg_flash_decode_part_bytes", "tdg_flash_decode",
 ]
@@ -53,6 +53,13 @@ class AgGemmArgs(ctypes.Structure):
                 ("b_layout", ctypes.c_int), ("mode", ctypes.c_int), ("producers", ctypes.c_int),
                 ("signal_rows", _i64), ("swizzle", ctypes.c_int), ("timeout_ns", _u64),
                 ("ll_off", _sz), ("test_skip_notify", _u64), ("source_order", ctypes.c_int)]
+
+
+class AgGemmAllArgs(ctypes.Structure):
+    _fields_ = [("world", ctypes.c_int), ("Ms", _i64), ("K", _i64), ("N", _i64), ("a_off", _sz),
+                ("g_off", _sz), ("b_off", _sz), ("c_off", _sz), ("b_layout", ctypes.c_int),
+                ("mode", ctypes.c_int), ("signal_rows", _i64), ("timeout_ns", _u64),
+                ("test_skip_notify", _u64)]
 
 
 class GemmRsArgs(ctypes.Structure):
@@ -124,6 +131,8 @@ def lib():
             L.tdg_device_info.argtypes = [ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]
             L.tdg_ag_gemm.restype = ctypes.c_int
             L.tdg_ag_gemm.argtypes = [_vp, ctypes.POINTER(AgGemmArgs), _vp, _vp]
+            L.tdg_ag_gemm_all_ranks.restype = ctypes.c_int
+            L.tdg_ag_gemm_all_ranks.argtypes = [_vp, ctypes.POINTER(AgGemmAllArgs), _vp, _vp]
             L.tdg_gemm_rs_stage_bytes.restype = _sz
             L.tdg_gemm_rs_stage_bytes.argtypes = [ctypes.c_int, _i64, _i64]
             L.tdg_gemm_rs.restype = ctypes.c_int
@@ -284,6 +293,19 @@ def ag_gemm(symm: Symm, rank: int, Ms: int, K: int, N: int, a_off: int, g_off: i
                    source_order=source_order)
     side = _vp(side_stream.cuda_stream) if side_stream is not None else _vp(None)
     _check(lib().tdg_ag_gemm(symm.h, ctypes.byref(a), _stream(stream), side), "tdg_ag_gemm")
+
+
+def ag_gemm_all_ranks(symm: Symm, Ms: int, K: int, N: int, a_off: int, g_off: int, b_off: int,
+                      c_off: int, mode="ce", b_layout=B_KN, signal_rows=0, timeout_ns=0,
+                      test_skip_notify=0, stream=None, side_stream=None):
+    """AllGather+GEMM of every rank in one call: C_r = concat(A_0..A_{W-1}) @ B_r,
+    with A_r, the gathered buffers, B_r and C_r all in the heap (offsets)."""
+    a = AgGemmAllArgs(world=symm.world, Ms=Ms, K=K, N=N, a_off=a_off, g_off=g_off, b_off=b_off,
+                      c_off=c_off, b_layout=b_layout, mode=MODES[mode], signal_rows=signal_rows,
+                      timeout_ns=timeout_ns, test_skip_notify=test_skip_notify)
+    side = _vp(side_stream.cuda_stream) if side_stream is not None else _vp(None)
+    _check(lib().tdg_ag_gemm_all_ranks(symm.h, ctypes.byref(a), _stream(stream), side),
+           "tdg_ag_gemm_all_ranks")
 
 
 def gemm_rs_stage_bytes(world: int, M: int, N: int) -> int:
