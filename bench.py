@@ -513,6 +513,41 @@ def leg_moe(torch, tdg, synth, args, flush, pk):
     return extras["moe_dispatch_combine"]
 
 
+def leg_ag_all(torch, tdg, args, flush, pk):
+    """The AG-GEMM of the step for every logical rank in one call (W x the
+    work: each rank gathers all shards and multiplies by its own B_r), CE mode
+    against its serial twin, timed in interleaved rounds."""
+    W, Ms, K, N = AG["W"], AG["Ms"], AG["K"], AG["N"]
+    M = W * Ms
+    a_off, g_off = 0, _align(Ms * K * 2)
+    b_off = _align(g_off + M * K * 2)
+    c_off = _align(b_off + K * N * 2)
+    sym = tdg.Symm(W, _align(c_off + M * N * 2 + 1024), 65536)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(0)
+    for r in range(W):
+        sym.view(r, a_off, (Ms, K), torch.bfloat16).copy_(torch.randn(Ms, K, device="cuda", generator=g))
+        sym.view(r, b_off, (K, N), torch.bfloat16).copy_(torch.randn(K, N, device="cuda", generator=g) * 0.02)
+    side = torch.cuda.Stream()
+    call = lambda mode: (lambda: tdg.ag_gemm_all_ranks(sym, Ms, K, N, a_off, g_off, b_off, c_off, mode=mode,
+                                                       side_stream=side if mode == "ce" else None))
+    iv = interleaved_steps(torch, {"ce": [call("ce")], "serial": [call("serial")]}, 3,
+                           max(4, args.steps // 5), flush)
+    st = sym.status()
+    if st["code"] != 0:
+        raise RuntimeError(f"device fault in the all-ranks AG-GEMM: {st}")
+    del sym
+    torch.cuda.empty_cache()
+    flop = W * AG_FLOP
+    return {"workload": "AG-GEMM Qwen-32B up for all 8 logical ranks in one call (8 x 8192x3200x5120, "
+                        "56 remote shard copies)",
+            "ce_ms": iv["ce"][0], "ce_tflops": flop / iv["ce"][0] / 1e9,
+            "ce_frac_of_bf16_peak": flop / iv["ce"][0] / 1e9 / pk["bf16"],
+            "serial_ms": iv["serial"][0], "serial_tflops": flop / iv["serial"][0] / 1e9,
+            "ce_overlap_gain_vs_serial": iv["serial"][0] / iv["ce"][0],
+            "note": "synthetic N(0,1) shards, 0.02*N(0,1) B_r generated on the device; modes in 3 interleaved rounds"}
+
+
 def leg_rs_f32(torch, tdg, args, flush, pk):
     """The GEMM-RS of the step with fp32 partials (one rounding, twice the
     staging bytes), overlapped and serial, timed in interleaved rounds."""
@@ -800,6 +835,7 @@ def main():
         extras["ag_tiny"] = leg_ag_config(
             torch, tdg, synth, args, flush, pk, 2, 64, 256, 128, "int2",
             "AG-GEMM tiny: W=2, A_r 64x256, B 256x128, integers (latency bound)", modes=("ce", "sm", "ll"))
+        extras["ag_all_ranks_qwen32b_up"] = leg_ag_all(torch, tdg, args, flush, pk)
         extras["gemm_rs_f32_partials"] = leg_rs_f32(torch, tdg, args, flush, pk)
         extras["moe_dispatch_combine"] = leg_moe(torch, tdg, synth, args, flush, pk)
         extras["ring_allreduce"] = leg_ring(torch, tdg, synth, args, flush, pk)
