@@ -74,8 +74,8 @@ def parse():
     ap.add_argument("--no-extras", action="store_true", help="skip serial/e2e/MoE/CPU legs")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--only", default="", help="measure one operation alone, not the bench line: "
-                    "ag, rs, moe, ring or flash; 'library' times torch.matmul (cuBLAS) on the AG "
-                    "GEMM shape as context")
+                    "ag, rs, moe, ring, flash or ag_all (the AG-GEMM of all ranks in one call); "
+                    "'library' times torch.matmul (cuBLAS) on the AG GEMM shape as context")
     ap.add_argument("--ag-shape", default="", help="W,Ms,K,N for --only ag|library, e.g. 8,2048,8192,7168 "
                     "(the Llama-3-70B gate+up shape)")
     return ap.parse_args()
@@ -531,21 +531,29 @@ def leg_ag_all(torch, tdg, args, flush, pk):
     side = torch.cuda.Stream()
     call = lambda mode: (lambda: tdg.ag_gemm_all_ranks(sym, Ms, K, N, a_off, g_off, b_off, c_off, mode=mode,
                                                        side_stream=side if mode == "ce" else None))
-    iv = interleaved_steps(torch, {"ce": [call("ce")], "serial": [call("serial")]}, 3,
-                           max(4, args.steps // 5), flush)
+    flop = W * AG_FLOP
+    res = {"workload": "AG-GEMM Qwen-32B up for all 8 logical ranks in one call (8 x 8192x3200x5120, "
+                       "56 remote shard copies)",
+           "note": "synthetic N(0,1) shards, 0.02*N(0,1) B_r generated on the device"}
+    if args.only == "ag_all" and args.mode == "serial":
+        # the serial twin alone (no flag waits: the form an ncu capture can replay)
+        ms = statistics.mean(timed_steps(torch, [call("serial")], args.steps, args.warmup, flush)[0])
+        res.update({"serial_ms": ms, "serial_tflops": flop / ms / 1e9,
+                    "serial_frac_of_bf16_peak": flop / ms / 1e9 / pk["bf16"]})
+    else:
+        iv = interleaved_steps(torch, {"ce": [call("ce")], "serial": [call("serial")]}, 3,
+                               max(4, args.steps // 5), flush)
+        res.update({"ce_ms": iv["ce"][0], "ce_tflops": flop / iv["ce"][0] / 1e9,
+                    "ce_frac_of_bf16_peak": flop / iv["ce"][0] / 1e9 / pk["bf16"],
+                    "serial_ms": iv["serial"][0], "serial_tflops": flop / iv["serial"][0] / 1e9,
+                    "ce_overlap_gain_vs_serial": iv["serial"][0] / iv["ce"][0]})
+        res["note"] += "; modes in 3 interleaved rounds"
     st = sym.status()
     if st["code"] != 0:
         raise RuntimeError(f"device fault in the all-ranks AG-GEMM: {st}")
     del sym
     torch.cuda.empty_cache()
-    flop = W * AG_FLOP
-    return {"workload": "AG-GEMM Qwen-32B up for all 8 logical ranks in one call (8 x 8192x3200x5120, "
-                        "56 remote shard copies)",
-            "ce_ms": iv["ce"][0], "ce_tflops": flop / iv["ce"][0] / 1e9,
-            "ce_frac_of_bf16_peak": flop / iv["ce"][0] / 1e9 / pk["bf16"],
-            "serial_ms": iv["serial"][0], "serial_tflops": flop / iv["serial"][0] / 1e9,
-            "ce_overlap_gain_vs_serial": iv["serial"][0] / iv["ce"][0],
-            "note": "synthetic N(0,1) shards, 0.02*N(0,1) B_r generated on the device; modes in 3 interleaved rounds"}
+    return res
 
 
 def leg_rs_f32(torch, tdg, args, flush, pk):
@@ -707,6 +715,18 @@ def main():
             print(json.dumps({"metric": "library GEMM TFLOP/s (context)", "value": 2 * M * K * N / ms / 1e9,
                               "unit": "TFLOP/s", "ms": ms, "shape": [M, K, N], "steps": args.steps,
                               "warmup": args.warmup, "clocks": clk.summary()}), flush=True)
+        return
+    if args.only == "ag_all":
+        with Clocks(local) as clk:
+            res = leg_ag_all(torch, tdg, args, flush, pk)
+        if rank == 0:
+            key = "serial" if "ce_tflops" not in res else "ce"
+            print(json.dumps({"metric": f"all-ranks AG-GEMM TFLOP/s ({key})", "value": res[f"{key}_tflops"],
+                              "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                              "higher_is_better": True, "dtype": "bf16",
+                              "roofline": {"bound": "tensor", "achieved": res[f"{key}_tflops"], "peak": pk["bf16"],
+                                           "unit": "TFLOP/s", "frac": res[f"{key}_tflops"] / pk["bf16"]},
+                              "clocks": clk.summary(), "detail": res}), flush=True)
         return
     if args.only in ("moe", "ring", "flash"):
         leg = {"moe": leg_moe, "ring": leg_ring, "flash": leg_flash}[args.only]
