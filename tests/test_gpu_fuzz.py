@@ -27,6 +27,34 @@ def _ag_cases(n=16, seed=2024):
     return out
 
 
+def _ag_all_cases(n=8, seed=2028):
+    g = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        W = int(g.choice([1, 2, 3, 4, 8]))
+        Ms = int(g.choice([64, 128, 192, 256, 512]))
+        while W * Ms > 2048:
+            Ms //= 2
+        K = int(g.choice([8, 64, 136, 256]))
+        N = int(g.choice([8, 72, 264, 520]))
+        lay = int(g.integers(0, 2))
+        out.append((W, Ms, K, N, lay, 4000 + i))
+    return out
+
+
+@pytest.mark.parametrize("W,Ms,K,N,lay,seed", _ag_all_cases())
+def test_ag_all_ranks_random_shapes_bit_exact(W, Ms, K, N, lay, seed):
+    from test_gpu_ag_all import AGAllCase
+    inp = synth.ag_all_inputs(W, Ms, K, N, "int2", seed=seed)
+    case = AGAllCase(inp, b_layout=tdg.B_KN if lay == 0 else tdg.B_NK)
+    want = [oracle.ag_gemm(inp.shards, inp.Bs[r])[1] for r in range(W)]
+    for mode in ("ce", "serial"):
+        got, _ = case.run(mode=mode)
+        for r in range(W):
+            assert np.array_equal(got[r], want[r]), (mode, r)
+            assert np.array_equal(to_bits(case.gathered(r)), np.concatenate(inp.shards)), (mode, r)
+
+
 def _rs_cases(n=12, seed=2025):
     g = np.random.default_rng(seed)
     out = []
