@@ -556,6 +556,48 @@ def leg_ag_all(torch, tdg, args, flush, pk):
     return res
 
 
+def leg_tp_mlp_all(torch, tdg, args, flush, pk):
+    """The Qwen-32B tensor-parallel MLP forward (without the activation) for
+    all 8 logical ranks: the all-ranks AG-GEMM writes every C_r into the heap
+    and the GEMM-RS reads it there as its A_r (no copy between the two).
+    Overlapped (CE + fused RS) against the serial twins, interleaved rounds."""
+    W, Ms, H, F = AG["W"], AG["Ms"], AG["K"], AG["N"]     # hidden 5120, ffn shard 3200
+    M = W * Ms
+    a_off, g_off = 0, _align(Ms * H * 2)
+    bu_off = _align(g_off + M * H * 2)
+    c_off = _align(bu_off + H * F * 2)
+    bd_off = _align(c_off + M * F * 2)
+    s_off = _align(bd_off + F * H * 2)
+    o_off = _align(s_off + tdg.gemm_rs_stage_bytes(W, M, H))
+    sym = tdg.Symm(W, _align(o_off + Ms * H * 2 + 1024), 65536)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(0)
+    for r in range(W):
+        sym.view(r, a_off, (Ms, H), torch.bfloat16).copy_(torch.randn(Ms, H, device="cuda", generator=g))
+        sym.view(r, bu_off, (H, F), torch.bfloat16).copy_(torch.randn(H, F, device="cuda", generator=g) * 0.02)
+        sym.view(r, bd_off, (F, H), torch.bfloat16).copy_(torch.randn(F, H, device="cuda", generator=g) * 0.02)
+    side = torch.cuda.Stream()
+    over = [lambda: tdg.ag_gemm_all_ranks(sym, Ms, H, F, a_off, g_off, bu_off, c_off, mode="ce", side_stream=side),
+            lambda: tdg.gemm_rs(sym, M, F, H, c_off, bd_off, s_off, o_off, mode="sm")]
+    ser = [lambda: tdg.ag_gemm_all_ranks(sym, Ms, H, F, a_off, g_off, bu_off, c_off, mode="serial"),
+           lambda: tdg.gemm_rs(sym, M, F, H, c_off, bd_off, s_off, o_off, mode="serial")]
+    iv = interleaved_steps(torch, {"overlapped": over, "serial": ser}, 3, max(4, args.steps // 5), flush)
+    st = sym.status()
+    if st["code"] != 0:
+        raise RuntimeError(f"device fault in the all-ranks MLP: {st}")
+    del sym
+    torch.cuda.empty_cache()
+    o_ms, s_ms = sum(iv["overlapped"]), sum(iv["serial"])
+    flop = W * AG_FLOP + RS_FLOP
+    return {"workload": "Qwen-32B TP MLP forward for all 8 logical ranks: all-ranks AG-GEMM up "
+                        "(8 x 8192x3200x5120) into the heap, then GEMM-RS down reading it (8 x 8192x5120x3200)",
+            "tflop_per_step": flop / 1e12, "ms": o_ms, "tflops": flop / o_ms / 1e9,
+            "frac_of_bf16_peak": flop / o_ms / 1e9 / pk["bf16"], "ag_ms": iv["overlapped"][0],
+            "rs_ms": iv["overlapped"][1], "serial_ms": s_ms, "serial_tflops": flop / s_ms / 1e9,
+            "overlap_gain_vs_serial": s_ms / o_ms,
+            "note": "synthetic N(0,1) x, 0.02*N(0,1) weights generated on the device; 3 interleaved rounds"}
+
+
 def leg_rs_f32(torch, tdg, args, flush, pk):
     """The GEMM-RS of the step with fp32 partials (one rounding, twice the
     staging bytes), overlapped and serial, timed in interleaved rounds."""
@@ -856,6 +898,7 @@ def main():
             torch, tdg, synth, args, flush, pk, 2, 64, 256, 128, "int2",
             "AG-GEMM tiny: W=2, A_r 64x256, B 256x128, integers (latency bound)", modes=("ce", "sm", "ll"))
         extras["ag_all_ranks_qwen32b_up"] = leg_ag_all(torch, tdg, args, flush, pk)
+        extras["tp_mlp_all_ranks_qwen32b"] = leg_tp_mlp_all(torch, tdg, args, flush, pk)
         extras["gemm_rs_f32_partials"] = leg_rs_f32(torch, tdg, args, flush, pk)
         extras["moe_dispatch_combine"] = leg_moe(torch, tdg, synth, args, flush, pk)
         extras["ring_allreduce"] = leg_ring(torch, tdg, synth, args, flush, pk)
