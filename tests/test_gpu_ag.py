@@ -215,3 +215,19 @@ def test_ll_second_heap_on_the_same_memory():
         assert np.array_equal(got, C2)
     got, _ = again.run(rank=1, mode="ll", ll_off=again.ll_off)
     assert np.array_equal(got, C2)
+
+
+@pytest.mark.parametrize("rounds", ["0", "1", "-1"])
+def test_sm_mode_producers_take_the_last_items(rounds, monkeypatch):
+    # 36 two-pair-cluster tiles (M 6144, 3 n tiles); 16 producer CTAs are 4
+    # clusters.  With TDG_AG_PROD_ROUNDS=0 the producer clusters take the last
+    # 4 items after their copies (the 32 GEMM clusters then need one round,
+    # not two); with 1 or -1 they take none.  Every split gives the oracle's bits.
+    monkeypatch.setenv("TDG_AG_PROD_ROUNDS", rounds)
+    inp = synth.ag_inputs(4, 1536, 128, 520, "int2", seed=17)
+    _, C16 = oracle.ag_gemm(inp.shards, inp.B)
+    case = AGCase(inp)
+    for rank in (0, 3):
+        got, _ = case.run(rank=rank, mode="sm", producers=16)
+        assert np.array_equal(got, C16), rank
+        _gathered_ok(case, rank)

@@ -71,6 +71,7 @@ struct AgParams {
     int split; // tiles of the last, partial wave split in two 128-column halves
     int mesh;  // 1: producers take all sources at once (round robin over sources)
     int group_m; // m rows per raster group
+    int64_t tail_lo; // SM mode: items [tail_lo, T) go to the producer clusters once their copies are done
     // LL mode: producer CTAs [0, n_send) send, [n_send, n_prod) receive
     int ll;
     int n_send;
@@ -293,7 +294,7 @@ __device__ void ag_producer(const AgParams &p, uint8_t *smem)
         uint8_t *dst = p.gathered + (uint64_t)grow * row_bytes;
         if (!ring_copy(dst, src, (uint64_t)rows * row_bytes, ring, bar, phases, p.timeout_ns)) {
             report_fault(p.status, TDG_ERR_TIMEOUT, TDG_WHERE_PIPE, (uint32_t)u, p.epoch);
-            return;
+            break;
         }
         bulk_wait<0>();             // the group's writes are complete ...
         fence_proxy_async_global(); // ... and ordered before the generic release
@@ -303,6 +304,9 @@ __device__ void ag_producer(const AgParams &p, uint8_t *smem)
                 st_release_gpu(p.flags_w + g, p.epoch); // notify
         }
     }
+    // the ring's shared memory may serve another role next
+    for (int i = 0; i < PSLOTS; ++i)
+        mbar_inval(&bar[i]);
 }
 
 // LL sender (paper summary, 方法: the low-latency protocol stores data and
@@ -422,18 +426,25 @@ __global__ void __launch_bounds__(gm::NUM_THREADS, 1) ag_gemm_kernel(const __gri
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
+    const int64_t T = (int64_t)p.m_tiles * p.n_tiles + p.split;
     if ((int)blockIdx.x < p.n_prod) {
-        // producer CTAs fill whole clusters and take no part in the GEMM
-        if (!p.ll)
+        // producer CTAs fill whole clusters; in SM mode, once a cluster's copies
+        // are done, it takes the last items of the GEMM (whose shards arrive last)
+        if (!p.ll) {
             ag_producer(p, smem);
-        else if ((int)blockIdx.x < p.n_send)
+            if (p.tail_lo < T) {
+                __syncthreads(); // every copy worker of this CTA is done with the ring
+                gemm_consumer<AgPolicy<BMN>, CL>(p, smem, (int)blockIdx.x / CL, p.n_prod / CL, p.tail_lo, T);
+            }
+        } else if ((int)blockIdx.x < p.n_send) {
             ll_sender(p, blockIdx.x, p.n_send);
-        else
+        } else {
             ll_receiver(p, blockIdx.x - p.n_send, p.n_prod - p.n_send);
+        }
         return;
     }
     const int c = (int)blockIdx.x - p.n_prod, nc = (int)gridDim.x - p.n_prod;
-    gemm_consumer<AgPolicy<BMN>, CL>(p, smem, c / CL, nc / CL);
+    gemm_consumer<AgPolicy<BMN>, CL>(p, smem, c / CL, nc / CL, 0, p.tail_lo < T ? p.tail_lo : T);
 }
 
 } // namespace tdg
@@ -472,6 +483,43 @@ int ag_grid(const AgParams &p, int b_layout, int sms)
     return p.cl * n;
 }
 
+// SM mode: once a producer cluster has copied its share of the shards it
+// takes GEMM items from the end of the order (rows that arrive last).  The
+// split balances the rounds of tiles: GEMM clusters run ceil(T_c / n_cc)
+// rounds, producer clusters c rounds' worth of copying and then
+// ceil((T - T_c) / n_pc) rounds.  c is estimated from the bytes each producer
+// CTA moves (about 45 GB/s each, measured: 16 CTAs copy the Qwen-32B shards
+// in about 115 us) against the time of one tile (about 12 TFLOP/s per SM);
+// TDG_AG_PROD_ROUNDS overrides it (-1: producers take no items).
+int64_t producer_tail_lo(const AgParams &p, int grid, int TM)
+{
+    const int64_t T = (int64_t)p.m_tiles * p.n_tiles;
+    const int n_pc = p.n_prod / p.cl, n_cc = (grid - p.n_prod) / p.cl;
+    if (n_pc <= 0 || n_cc <= 0)
+        return T;
+    int64_t c;
+    if (const char *e = getenv("TDG_AG_PROD_ROUNDS")) {
+        c = atoi(e);
+        if (c < 0)
+            return T;
+    } else {
+        const double copy_s = (double)p.W * p.Ms * p.K * 2.0 / p.n_prod / 45e9;
+        const double tile_s = 2.0 * TM * gm::BN * p.K / (p.cl * 12e12);
+        c = (int64_t)ceil(copy_s / tile_s);
+    }
+    int64_t best_t = 0, best_r = (T + n_cc - 1) / n_cc;
+    for (int64_t t = 1; t <= T; ++t) {
+        const int64_t rc = (T - t + n_cc - 1) / n_cc;
+        const int64_t rp = c + (t + n_pc - 1) / n_pc;
+        const int64_t r = rc > rp ? rc : rp;
+        if (r < best_r) {
+            best_r = r;
+            best_t = t;
+        }
+    }
+    return T - best_t;
+}
+
 int launch_ag(const AgParams &p, int b_layout, int grid, bool coop, cudaStream_t s)
 {
     const void *fn = ag_kernel_fn(b_layout, p.cl);
@@ -491,10 +539,14 @@ int launch_ag(const AgParams &p, int b_layout, int grid, bool coop, cudaStream_t
     q.split = 0;
     // opt-in (TDG_SPLIT_TAIL=1): measured slower at the Qwen-32B up-projection
     // shape, where the half-width tiles move more operand bytes per FLOP and the
-    // tail tiles wait on the shard that arrives last anyway
+    // tail tiles wait on the shard that arrives last anyway.  Not combined with
+    // producer clusters that take the last items.
     const char *st = getenv("TDG_SPLIT_TAIL");
-    if (st && st[0] == '1' && units > 0 && T > units && (T % units) > 0 && 2 * (T % units) <= units)
+    if (st && st[0] == '1' && p.tail_lo >= T && units > 0 && T > units && (T % units) > 0 &&
+        2 * (T % units) <= units)
         q.split = (int)(T % units);
+    if (q.tail_lo >= T)
+        q.tail_lo = T + q.split; // every item goes to the GEMM CTAs
     void *args[] = {&q};
     cudaError_t e = launch(fn, dim3(grid), dim3(gm::NUM_THREADS), gm::SMEM_BYTES, s, args, coop, p.cl);
     if (e != cudaSuccess && coop && p.cl > 1) {
@@ -597,6 +649,7 @@ extern "C" int tdg_ag_gemm(tdg_symm *h, const tdg_ag_gemm_args *a, void *stream,
     // otherwise m-major
     p.group_m = ((uint64_t)K * N * 2 > (64ull << 20)) ? 8 : 0;
     p.n_tiles = (int)((N + gm::BN - 1) / gm::BN);
+    p.tail_lo = (int64_t)p.m_tiles * p.n_tiles; // no items for the producer CTAs
     p.swz = a->swizzle ? (int)(((int64_t)rank * Ms / TM) % p.m_tiles) : 0;
     p.local_inplace = inplace ? 1 : 0;
     p.local_lo = inplace ? (int)(rank * Ms / TM) : 0;
@@ -649,6 +702,7 @@ extern "C" int tdg_ag_gemm(tdg_symm *h, const tdg_ag_gemm_args *a, void *stream,
         p.unit_rows = sig_rows;
         p.units_per_shard = Ms / sig_rows;
         p.n_units = (int64_t)W * p.units_per_shard;
+        p.tail_lo = producer_tail_lo(p, ggrid, TM);
         return launch_ag(p, a->b_layout, ggrid, true, s);
     }
     if (a->mode == TDG_MODE_SERIAL) {

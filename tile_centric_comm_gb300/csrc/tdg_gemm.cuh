@@ -128,8 +128,11 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p)
 // The load hooks receive the mbarrier as a shared::cluster address (the pair
 // leader's barrier when CL >= 2) and issue pair TMA when CL >= 2.  All
 // tcgen05 and TMA instructions of one kernel use a single cta_group.
+// Items [item_lo, item_hi) (item_hi < 0: all of P::num_items) are dealt to
+// `nunits` scheduling units round robin; this CTA's unit is `unit`.
 template <class P, int CL>
-__device__ void gemm_consumer(const typename P::Params &p, uint8_t *smem, int unit, int nunits)
+__device__ void gemm_consumer(const typename P::Params &p, uint8_t *smem, int unit, int nunits,
+                              int64_t item_lo = 0, int64_t item_hi = -1)
 {
     using namespace gm;
     constexpr int PAIR = CL >= 2 ? 1 : 0;
@@ -177,7 +180,8 @@ __device__ void gemm_consumer(const typename P::Params &p, uint8_t *smem, int un
         cluster_sync(); // the peer's barriers are initialised before any remote use
     tc_fence_after();
     const uint32_t tmem_base = ps->tmem_base;
-    const int64_t items = P::num_items(p);
+    // this launch's share of the items: [item_lo, items), unit by unit
+    const int64_t items = item_hi >= 0 ? item_hi : P::num_items(p);
     const uint64_t tmo = p.pipe_timeout_ns;
     // the barrier a load completes on / an epilogue releases: the pair leader's
     const uint32_t full0 = PAIR ? mapa_shared(smem_u32(&ps->full[0]), lead_rank) : smem_u32(&ps->full[0]);
@@ -190,7 +194,7 @@ __device__ void gemm_consumer(const typename P::Params &p, uint8_t *smem, int un
             uint32_t phase = 0;
             bool gave_up = false;
             uint32_t issued = 0; // kept in a register; published once for the abort drain
-            for (int64_t it = unit; it < items && !ps->abort; it += nunits) {
+            for (int64_t it = item_lo + unit; it < items && !ps->abort; it += nunits) {
                 TileInfo ti;
                 P::tile(p, it, ti, crank);
                 if (ti.n_valid <= 0)
@@ -230,7 +234,7 @@ __device__ void gemm_consumer(const typename P::Params &p, uint8_t *smem, int un
             uint32_t acc_phase = 0;
             uint32_t consumed = 0; // kept in a register; published once for the abort drain
             const uint32_t sbase = smem_u32(smem);
-            for (int64_t it = unit; it < items && !ps->abort; it += nunits) {
+            for (int64_t it = item_lo + unit; it < items && !ps->abort; it += nunits) {
                 TileInfo ti;
                 P::tile(p, it, ti, crank);
                 if (ti.n_valid <= 0)
@@ -312,7 +316,7 @@ __device__ void gemm_consumer(const typename P::Params &p, uint8_t *smem, int un
         typename P::EpiState est{};
         // after the last tile, one more pass with no tile (tail = true) lets
         // the policy finish work it deferred
-        for (int64_t it = unit;; it += nunits) {
+        for (int64_t it = item_lo + unit;; it += nunits) {
             TileInfo ti;
             if (it >= items) {
                 if (!ps->abort)
