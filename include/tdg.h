@@ -261,10 +261,11 @@ TDG_API int tdg_ag_gemm_all_ranks(tdg_symm *h, const tdg_ag_gemm_all_args *args,
  * the final one of the fp32 sum to bf16 (the pages leave the partial type
  * open; bf16 is the default).
  * Requirements: M % W == 0, (M/W) % 128 == 0, K % 8 == 0, N % 8 == 0, the
- * offsets 16-byte aligned, W*(M/W/128)*ceil(N/256) <= signals_per_rank,
+ * offsets 16-byte aligned, 4*(M/W/128)*ceil(N/256) <= signals_per_rank
+ * (one counter word per 32-row quarter of each of an owner's tiles),
  * partial_f32 0 or 1, and the staging area and out_o overlapping neither
- * each other nor A_r / B_r (TDG_ERR_INVALID otherwise; TDG_ERR_NOMEM when a
- * buffer runs past its region).
+ * each other nor A_r / B_r.  TDG_ERR_NOMEM when a buffer runs past its
+ * region or the counter words are too few; TDG_ERR_INVALID for the rest.
  */
 typedef struct {
     int world;
