@@ -166,10 +166,15 @@ TDG_API int tdg_device_info(int *sm_count, int *supported);
  *
  * B: K x N (TDG_B_KN) or N x K (TDG_B_NK) bf16, device pointer.
  * C: M x N bf16 output, device pointer.
- * Requirements: 1 <= world <= 64; K % 8 == 0; N % 8 == 0; a_off, g_off, B, C
- * 16-byte aligned; g_off + M*K*2 <= region_bytes; a_off + Ms*K*2 <=
- * region_bytes; M / signal_rows <= signals_per_rank.  M == 0 or N == 0 is a
- * no-op; K == 0 writes C = 0.
+ * Requirements: 1 <= world <= 64; 0 <= rank < world; K % 8 == 0; N % 8 ==
+ * 0; a_off, g_off, B, C 16-byte aligned; the gathered buffer not overlapping
+ * the shard; signal_rows dividing Ms; source_order 0 or 1; CE mode needs a
+ * side_stream other than stream; LL mode an aligned LL buffer that overlaps
+ * neither the shard nor the gathered buffer; SM / LL producer CTAs fewer than
+ * the GEMM's grid (TDG_ERR_INVALID otherwise).  g_off + M*K*2, a_off + Ms*K*2
+ * (and ll_off + M*K*4) <= region_bytes and M / signal_rows <=
+ * signals_per_rank (TDG_ERR_NOMEM otherwise).  M == 0 or N == 0 is a no-op;
+ * K == 0 writes C = 0.
  */
 typedef struct {
     int world, rank;
