@@ -307,8 +307,11 @@ TDG_API int tdg_gemm_rs(tdg_symm *h, const tdg_gemm_rs_args *args, void *stream)
  * (tdg_allreduce_recv_bytes).  Signals: rank r's flag words
  * [0, (2W-2) * tiles_per_chunk).
  * Requirements: count % (4 * world) == 0, tile_elems % 4 == 0 (0 = default),
- * offsets 16-byte aligned, (2W-2) * ceil(count/W / tile_elems) <=
- * signals_per_rank.  count == 0 or world == 1 is a no-op.
+ * offsets 16-byte aligned, the receive slots not overlapping x, and no more
+ * CTAs than can be resident at once (TDG_ERR_INVALID otherwise); x and the
+ * receive slots inside their region and (2W-2) * ceil(count/W / tile_elems)
+ * <= signals_per_rank (TDG_ERR_NOMEM otherwise).  count == 0 or world == 1
+ * is a no-op.
  */
 typedef struct {
     int world;
@@ -379,9 +382,15 @@ TDG_API int tdg_flash_decode(tdg_symm *h, const tdg_flash_decode_args *args, voi
  * y[slot(src,t,kk)]) with an fp32 sum in kk order, written to region(src) +
  * out_off.  y has the receive layout; y == NULL means y = recv.
  * workspace: device scratch of tdg_moe_workspace_bytes() bytes.
- * Requirements: E % W == 0, 1 <= k <= 32, k <= E, H % 8 == 0, offsets and
- * pointers 16-byte aligned.  An expert id outside [0, E) is reported as
- * TDG_ERR_DEVICE by tdg_status and that (t, kk) gets slot -1.
+ * Requirements: E % W == 0, E <= 4096, 1 <= k <= 32, k <= E, H % 8 == 0,
+ * W*T*k < 2^31, phases a nonzero OR of the bits; x_off, out_off, recv and y
+ * 16-byte aligned, topk_off and gate_off 4-byte aligned; slot always, counts
+ * and base when routing, recv when dispatching (or combining with y NULL);
+ * row_src / row_tok / row_k all or none (TDG_ERR_INVALID otherwise).  The
+ * per-rank inputs inside their region and, when routing, a workspace of
+ * tdg_moe_workspace_bytes() (TDG_ERR_NOMEM otherwise).  T == 0 is a no-op.
+ * An expert id outside [0, E) is reported as TDG_ERR_DEVICE by tdg_status
+ * and that (t, kk) gets slot -1.
  */
 #define TDG_MOE_ROUTE 1
 #define TDG_MOE_DISPATCH 2
