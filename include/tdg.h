@@ -341,9 +341,12 @@ TDG_API int tdg_allreduce(tdg_symm *h, const tdg_allreduce_args *args, void *str
  * + part_off; a second, stream-ordered launch on the root merges all partials
  * by log-sum-exp and writes out (bf16).
  * q, out: B x Hq x D bf16 device pointers.  Requirements: D == 128,
- * Hq % Hkv == 0, Hq/Hkv <= 16, S % world == 0, S > 0, chunk % 64 == 0
- * (0 = 2048 tokens), world * ceil(S/world/chunk) <= 12000, offsets and
- * pointers 16-byte aligned.
+ * Hq % Hkv == 0, Hq/Hkv <= 16, B*Hkv <= 65535, S % world == 0, S > 0,
+ * 0 <= root < world, chunk % 64 == 0 (0 = 2048 tokens), world *
+ * ceil(S/world/chunk) <= 12000, offsets and pointers 16-byte aligned, the
+ * partials overlapping neither K nor V (TDG_ERR_INVALID otherwise); K, V and
+ * the partials (tdg_flash_decode_part_bytes) inside their regions
+ * (TDG_ERR_NOMEM otherwise).
  */
 typedef struct {
     int world, root;

@@ -117,6 +117,7 @@ def test_flash_decode_rejections():
     assert rc(Hq=32, Hkv=1) == tdg.TDG_ERR_INVALID                    # more than 16 heads per kv head
     assert rc(chunk=96) == tdg.TDG_ERR_INVALID                        # chunk not a multiple of 64
     assert rc(root=2) == tdg.TDG_ERR_INVALID
+    assert rc(part_off=c.v_off) == tdg.TDG_ERR_INVALID                # partials overlap V
     assert rc(S=1 << 24) == tdg.TDG_ERR_NOMEM
     torch.cuda.synchronize()
     assert c.symm.status()["code"] == 0

@@ -352,6 +352,10 @@ extern "C" int tdg_flash_decode(tdg_symm *h, const tdg_flash_decode_args *a, voi
     const uint64_t R = h->region_bytes;
     if (a->k_off + kv_bytes > R || a->v_off + kv_bytes > R || a->part_off + part > R)
         return TDG_ERR_NOMEM;
+    // the partials (written) overlap neither K nor V
+    if ((a->part_off < a->k_off + kv_bytes && a->k_off < a->part_off + part) ||
+        (a->part_off < a->v_off + kv_bytes && a->v_off < a->part_off + part))
+        return TDG_ERR_INVALID;
     if (a->B * a->Hkv > 65535 || (int64_t)W * splits * 4 + 128 > 48 * 1024)
         return TDG_ERR_INVALID;
     FlashParams p;
