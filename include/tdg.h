@@ -389,7 +389,8 @@ TDG_API int tdg_flash_decode(tdg_symm *h, const tdg_flash_decode_args *args, voi
  * W*T*k < 2^31, phases a nonzero OR of the bits; x_off, out_off, recv and y
  * 16-byte aligned, topk_off and gate_off 4-byte aligned; slot always, counts
  * and base when routing, recv when dispatching (or combining with y NULL);
- * row_src / row_tok / row_k all or none (TDG_ERR_INVALID otherwise).  The
+ * row_src / row_tok / row_k all or none; when combining, out not
+ * overlapping the gates (TDG_ERR_INVALID otherwise).  The
  * per-rank inputs inside their region and, when routing, a workspace of
  * tdg_moe_workspace_bytes() (TDG_ERR_NOMEM otherwise).  T == 0 is a no-op.
  * An expert id outside [0, E) is reported as TDG_ERR_DEVICE by tdg_status

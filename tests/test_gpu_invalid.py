@@ -80,10 +80,11 @@ def test_moe_rejections_and_empty():
     inp = synth.moe_inputs(2, 64, 128, 16, 4, seed=3)
     c = MoECase(inp)
 
-    def rc(T=64, H=128, E=16, k=4, phases=tdg.MOE_ALL, ws=None):
+    def rc(T=64, H=128, E=16, k=4, phases=tdg.MOE_ALL, ws=None, out_off=None):
         ws = c.ws if ws is None else ws
         a = tdg.MoeArgs(world=2, T=T, H=H, E=E, k=k, x_off=c.x_off, topk_off=c.topk_off,
-                        gate_off=c.gate_off, out_off=c.out_off, recv=c.recv.data_ptr(),
+                        gate_off=c.gate_off, out_off=c.out_off if out_off is None else out_off,
+                        recv=c.recv.data_ptr(),
                         counts=c.counts.data_ptr(), base=c.base.data_ptr(), slot=c.slot.data_ptr(),
                         workspace=ws.data_ptr(), workspace_bytes=ws.numel(), phases=phases)
         cur = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
@@ -92,6 +93,7 @@ def test_moe_rejections_and_empty():
     assert rc(k=17) == tdg.TDG_ERR_INVALID                            # k > E
     assert rc(H=100) == tdg.TDG_ERR_INVALID                           # H not a multiple of 8
     assert rc(phases=0) == tdg.TDG_ERR_INVALID
+    assert rc(out_off=c.gate_off) == tdg.TDG_ERR_INVALID                  # out over the gates, combining
     small = torch.empty(16, dtype=torch.uint8, device="cuda")
     assert rc(ws=small) == tdg.TDG_ERR_NOMEM                          # workspace too small
     assert rc(T=0) == tdg.TDG_OK                                      # no tokens: a no-op

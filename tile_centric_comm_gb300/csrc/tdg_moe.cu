@@ -369,6 +369,9 @@ extern "C" int tdg_moe_dispatch_combine(tdg_symm *h, const tdg_moe_args *a, void
         return TDG_ERR_NOMEM;
     if (!a->slot || (route && (!a->counts || !a->base)))
         return TDG_ERR_INVALID;
+    // combine writes out while it reads the gates
+    if (comb && a->out_off < a->gate_off + (uint64_t)T * k * 4 && a->gate_off < a->out_off + (uint64_t)T * H * 2)
+        return TDG_ERR_INVALID;
     if ((disp || (comb && !a->y)) && (!a->recv || !aligned16(a->recv)))
         return TDG_ERR_INVALID;
     if (a->y && !aligned16(a->y))
