@@ -598,6 +598,85 @@ def leg_tp_mlp_all(torch, tdg, args, flush, pk):
             "note": "synthetic N(0,1) x, 0.02*N(0,1) weights generated on the device; 3 interleaved rounds"}
 
 
+def leg_tp_mlp_e2e(torch, tdg, args, pk):
+    """The all-ranks TP MLP end to end through the public API with host
+    buffers: every step uploads the 8 ranks' activations x_r from pinned host
+    memory and downloads the 8 outputs; the weights stay resident (uploaded
+    once, as in serving).  Consecutive steps overlap over two heaps (upload,
+    compute and download streams)."""
+    W, Ms, H, F = AG["W"], AG["Ms"], AG["K"], AG["N"]
+    M = W * Ms
+    a_off, g_off = 0, _align(Ms * H * 2)
+    bu_off = _align(g_off + M * H * 2)
+    c_off = _align(bu_off + H * F * 2)
+    bd_off = _align(c_off + M * F * 2)
+    s_off = _align(bd_off + F * H * 2)
+    o_off = _align(s_off + tdg.gemm_rs_stage_bytes(W, M, H))
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(0)
+    sets = []
+    for _ in range(2):
+        sym = tdg.Symm(W, _align(o_off + Ms * H * 2 + 1024), 65536)
+        for r in range(W):
+            sym.view(r, bu_off, (H, F), torch.bfloat16).copy_(torch.randn(H, F, device="cuda", generator=gen) * 0.02)
+            sym.view(r, bd_off, (F, H), torch.bfloat16).copy_(torch.randn(F, H, device="cuda", generator=gen) * 0.02)
+        sets.append(sym)
+    cpu_gen = torch.Generator()
+    cpu_gen.manual_seed(0)
+    x_host = [torch.randn(Ms, H, generator=cpu_gen).to(torch.bfloat16).pin_memory() for _ in range(W)]
+    out_host = [torch.empty(Ms, H, dtype=torch.bfloat16).pin_memory() for _ in range(W)]
+    comp = torch.cuda.current_stream()
+    up, down, side = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    free = [torch.cuda.Event() for _ in sets]
+    for e in free:
+        e.record(comp)
+
+    def step(i):
+        sym = sets[i % 2]
+        x_in, done = torch.cuda.Event(), torch.cuda.Event()
+        up.wait_event(free[i % 2])
+        with torch.cuda.stream(up):
+            for r in range(W):
+                sym.view(r, a_off, (Ms, H), torch.bfloat16).copy_(x_host[r], non_blocking=True)
+            x_in.record(up)
+        comp.wait_event(x_in)
+        tdg.ag_gemm_all_ranks(sym, Ms, H, F, a_off, g_off, bu_off, c_off, mode="ce", side_stream=side)
+        tdg.gemm_rs(sym, M, F, H, c_off, bd_off, s_off, o_off, mode="sm")
+        done.record(comp)
+        down.wait_event(done)
+        with torch.cuda.stream(down):
+            for o in range(W):
+                out_host[o].copy_(sym.view(o, o_off, (Ms, H), torch.bfloat16), non_blocking=True)
+            free[i % 2].record(down)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(comp)
+    up.wait_event(e0)
+    for i in range(args.warmup, args.warmup + args.steps):
+        step(i)
+    comp.wait_stream(up)
+    comp.wait_stream(down)
+    e1.record(comp)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    for sym in sets:
+        st = sym.status()
+        if st["code"] != 0:
+            raise RuntimeError(f"device fault in the all-ranks MLP end to end: {st}")
+    del sets
+    torch.cuda.empty_cache()
+    flop = W * AG_FLOP + RS_FLOP
+    return {"workload": "Qwen-32B TP MLP forward for all 8 logical ranks, end to end: x_r of every rank "
+                        "uploaded and every out_o downloaded each step, weights resident",
+            "value": flop / ms / 1e9, "unit": "TFLOP/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": W * Ms * H * 2, "d2h_bytes_per_step": W * Ms * H * 2,
+            "frac_of_bf16_peak": flop / ms / 1e9 / pk["bf16"],
+            "how": "two heaps, upload / compute / download streams; the AG-GEMM's copies on a side stream"}
+
+
 def leg_rs_f32(torch, tdg, args, flush, pk):
     """The GEMM-RS of the step with fp32 partials (one rounding, twice the
     staging bytes), overlapped and serial, timed in interleaved rounds."""
@@ -899,6 +978,7 @@ def main():
             "AG-GEMM tiny: W=2, A_r 64x256, B 256x128, integers (latency bound)", modes=("ce", "sm", "ll"))
         extras["ag_all_ranks_qwen32b_up"] = leg_ag_all(torch, tdg, args, flush, pk)
         extras["tp_mlp_all_ranks_qwen32b"] = leg_tp_mlp_all(torch, tdg, args, flush, pk)
+        extras["tp_mlp_all_ranks_qwen32b"]["e2e"] = leg_tp_mlp_e2e(torch, tdg, args, pk)
         extras["gemm_rs_f32_partials"] = leg_rs_f32(torch, tdg, args, flush, pk)
         extras["moe_dispatch_combine"] = leg_moe(torch, tdg, synth, args, flush, pk)
         extras["ring_allreduce"] = leg_ring(torch, tdg, synth, args, flush, pk)
