@@ -221,7 +221,10 @@ TDG_API int tdg_ag_gemm(tdg_symm *h, const tdg_ag_gemm_args *args, void *stream,
  * first, read in place when Ms is a whole number of tiles) and waits (bounded)
  * on the flags of the rows it reads; the W x W shard copies run on
  * `side_stream` (cudaMemcpyAsync, then a stream-ordered flag write), rank by
- * rank.  SERIAL mode: the copies, then the GEMM, on `stream`.
+ * rank.  The GEMM is queued first, so that the tiles of each rank's own
+ * shard start at once; its flag waits are bounded by timeout_ns, within
+ * which this call queues the copies behind it.  SERIAL mode: the copies,
+ * then the GEMM, on `stream`.
  * Requirements: 1 <= world <= 64; K % 8 == 0; N % 8 == 0; offsets 16-byte
  * aligned; every buffer inside its region (else TDG_ERR_NOMEM); the gathered
  * buffers and C_r overlapping no other buffer (else TDG_ERR_INVALID);
