@@ -29,7 +29,8 @@
  *     used from different threads.
  *   - Every operation runs on the device the heap was allocated on
  *     (tdg_symm_alloc records the current device); calling it while another
- *     device is current returns TDG_ERR_INVALID.
+ *     device is current returns TDG_ERR_INVALID.  Any host thread may call:
+ *     the call makes that device's context current in the calling thread.
  */
 #ifndef TDG_H_
 #define TDG_H_

@@ -133,7 +133,12 @@ int check_device(const tdg_symm *h)
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess)
         return TDG_ERR_CUDA;
-    return dev == h->device ? TDG_OK : TDG_ERR_INVALID;
+    if (dev != h->device)
+        return TDG_ERR_INVALID;
+    // The driver calls that follow (tensor-map encoding, stream memory
+    // operations) need the device's context current in this thread; a thread
+    // whose first CUDA call this is may not have it yet.
+    return cudaSetDevice(dev) == cudaSuccess ? TDG_OK : TDG_ERR_CUDA;
 }
 
 cudaError_t launch(const void *fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s,

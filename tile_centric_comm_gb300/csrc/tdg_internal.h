@@ -67,8 +67,9 @@ bool stream_write_u32(cudaStream_t s, uint32_t *dev_addr, uint32_t value);
 // several host threads.
 cudaError_t set_smem(const void *fn, int bytes);
 
-// TDG_OK when the current device is the one the heap was allocated on,
-// TDG_ERR_INVALID when it is another, TDG_ERR_CUDA when it cannot be read.
+// TDG_OK when the current device is the one the heap was allocated on (its
+// context is then current in the calling thread), TDG_ERR_INVALID when it is
+// another, TDG_ERR_CUDA when it cannot be read or made current.
 int check_device(const tdg_symm *h);
 
 // Launch with the cooperative attribute (all CTAs co-resident, which the
