@@ -183,8 +183,6 @@ uint32_t next_epoch(tdg_symm *h)
 
 uint32_t peek_epoch() { return epoch_after(g_epoch.load(std::memory_order_relaxed)); }
 
-int max_pairs(const void *fn, int block, int smem) { return max_clusters(fn, block, smem, 2); }
-
 int max_clusters(const void *fn, int block, int smem, int cl)
 {
     cudaLaunchConfig_t cfg = {};
@@ -202,14 +200,6 @@ int max_clusters(const void *fn, int block, int smem, int cl)
     if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess)
         return 0;
     return n;
-}
-
-int occupancy_ok(const void *fn, int block, int smem, int grid, int sm_count)
-{
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, block, smem) != cudaSuccess)
-        return 0;
-    return per_sm * sm_count >= grid;
 }
 
 } // namespace tdg_host

@@ -77,8 +77,6 @@ int check_device(const tdg_symm *h);
 cudaError_t launch(const void *fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s,
                    void **args, bool cooperative, int cluster = 1);
 
-// Number of 2-CTA clusters of `fn` that can be resident at once (0 on error).
-int max_pairs(const void *fn, int block, int smem);
 // Number of `cl`-CTA clusters of `fn` that can be resident at once (0 on error).
 int max_clusters(const void *fn, int block, int smem, int cl);
 
@@ -95,8 +93,6 @@ inline bool quads_enabled()
     const char *e = getenv("TDG_QUAD");
     return !(e && e[0] == '0');
 }
-
-int occupancy_ok(const void *fn, int block, int smem, int grid, int sm_count);
 
 inline int cuda_err(cudaError_t e, const char *what)
 {
