@@ -7,8 +7,8 @@
 // are (owner block, rank r, owner o in the block, m tile inside o, n tile):
 // all ranks' items of one block of two owners run back to back, so every
 // output tile gathers its W partials close together in time while each B_r
-// is streamed once per block.  The epilogue pushes each bf16
-// partial tile (tile-contiguous, 128 x 256) into owner o's staging area
+// is streamed once per block.  The epilogue pushes each partial tile (bf16,
+// or fp32 when asked; tile-contiguous, 128 x 256) into owner o's staging area
 // (region o) with TMA, waits for the write to complete, fences the async
 // proxy, and increments the owner's per-(tile, row-quarter) arrival counter
 // with acq_rel semantics (the pages' "increment" signal; the counter word is
