@@ -11,6 +11,8 @@
 // call's epoch.  CTAs [P, grid) are the persistent tcgen05 GEMM; its loader
 // waits on the groups of each A tile with a bounded ld.acquire spin, then
 // fences the async proxy and issues TMA.  The local shard is read in place.
+// Once its copies are done, a producer cluster takes GEMM items from the end
+// of the order (the host balances that split from the copy and tile times).
 // CE mode: cudaMemcpyAsync per group on the side stream, each followed by a
 // stream-ordered cuStreamWriteValue32 of the flag; the GEMM-only launch on
 // the main stream waits on the flags.
