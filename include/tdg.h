@@ -197,7 +197,7 @@ typedef struct {
     uint64_t test_skip_notify; /* tests only: producers skip the notify of
                                   signal groups whose bit (g % 64) is set   */
     int source_order;    /* 0: one source at a time, rank+1, rank+2, ... (the
-                            pages' NVSwitch swizzle); 1: all sources at once,
+                            published NVSwitch swizzle); 1: all sources at once,
                             round robin over sources (their full-mesh order) */
 } tdg_ag_gemm_args;
 
@@ -267,8 +267,8 @@ TDG_API int tdg_ag_gemm_all_ranks(tdg_symm *h, const tdg_ag_gemm_all_args *args,
  * and the reduction after it.
  * partial_f32 = 1 pushes the partial tiles as fp32 instead of bf16: the
  * staging area is twice tdg_gemm_rs_stage_bytes(), and the only rounding is
- * the final one of the fp32 sum to bf16 (the pages leave the partial type
- * open; bf16 is the default).
+ * the final one of the fp32 sum to bf16 (the published design leaves the
+ * partial type open; bf16 is the default).
  * Requirements: M % W == 0, (M/W) % 128 == 0, K % 8 == 0, N % 8 == 0, the
  * offsets 16-byte aligned, 4*(M/W/128)*ceil(N/256) <= signals_per_rank
  * (one counter word per 32-row quarter of each of an owner's tiles),
@@ -305,7 +305,7 @@ TDG_API int tdg_gemm_rs(tdg_symm *h, const tdg_gemm_rs_args *args, void *stream)
  * every rank holds sum_r x_r.  Each buffer is split into W chunks of count/W;
  * at reduce-scatter step s rank r sends chunk (r - s) mod W to rank r+1, which
  * adds its own copy (local + incoming, float32) -- the textbook ring, since
- * the tile indices printed in the pages' example are inconsistent -- and at
+ * the tile indices printed in the published example are inconsistent -- and at
  * all-gather step s rank r forwards chunk (r + 1 - s) mod W.
  * recv_r at region(r) + recv_off holds W-1 chunk-sized float32 slots
  * (tdg_allreduce_recv_bytes).  Signals: rank r's flag words
@@ -425,8 +425,8 @@ TDG_API size_t tdg_moe_workspace_bytes(int world, int64_t T, int E);
 TDG_API int tdg_moe_dispatch_combine(tdg_symm *h, const tdg_moe_args *args, void *stream);
 
 /*
- * Allocation-free variant of tdg_moe_dispatch_combine.  The pages have no
- * counterpart: this entry point exists for callers that cannot allocate
+ * Allocation-free variant of tdg_moe_dispatch_combine.  The published design
+ * has no counterpart: this entry point exists for callers that cannot allocate
  * device memory at the moment they call -- for example code running inside
  * a memory-budgeted runtime or a pool that forbids cudaMalloc after start-up,
  * or a caller with no allocator of its own -- and so cannot hand over the

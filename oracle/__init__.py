@@ -6,7 +6,7 @@ package.  The product library under ``tile_centric_comm_gb300/`` never imports
 it and shares no code with it.
 
 The arithmetic lives in ``tdg_oracle.c`` (plain C, double precision, explicit
-loops, each function citing the passage of the pages it writes out).  This
+loops, each function citing the published passage it writes out).  This
 module only compiles it with gcc and marshals numpy arrays through ctypes.
 
 bf16 values travel as numpy ``uint16`` bit patterns.

@@ -26,7 +26,7 @@
  *                section "DITRON 加入三级分块": per-expert token counts are
  *                only known at run time.
  *
- * Readings where the pages are silent (each one is listed with its reason in
+ * Readings where the cited pages are silent (each one is listed with its reason in
  * the design notes of this repository):
  *   - bf16 is IEEE-754 binary16-brain (1 sign, 8 exponent, 7 fraction bits);
  *     outputs are rounded once, from the exact double-precision sum, to the

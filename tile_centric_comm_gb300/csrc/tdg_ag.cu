@@ -6,8 +6,8 @@
 // their copy workers (one thread per warp, 1-D TMA bulk copies through a
 // shared-memory ring) pull shard tiles from the peer regions into the
 // gathered buffer, one signal group at a time, in source order
-// (rank+1, rank+2, ..., rank) -- one source at a time, the NVSwitch order the
-// pages describe -- and publish each finished group with st.release of the
+// (rank+1, rank+2, ..., rank) -- one source at a time, the NVSwitch order of
+// Triton-distributed -- and publish each finished group with st.release of the
 // call's epoch.  CTAs [P, grid) are the persistent tcgen05 GEMM; its loader
 // waits on the groups of each A tile with a bounded ld.acquire spin, then
 // fences the async proxy and issues TMA.  The local shard is read in place.
@@ -22,7 +22,7 @@
 // waits on those flags as in SM mode.
 // SERIAL mode: a copy-only launch (all SMs), then a GEMM-only launch that does
 // not wait; the two are ordered by the stream.
-// Tile order: the pages' rank swizzle over m tiles; m-major while B fits in
+// Tile order: Triton-distributed's rank swizzle over m tiles; m-major while B fits in
 // about half of L2, else groups of 8 m tiles with n outer inside a group.
 #include "tdg_gemm.cuh"
 #include "tdg_internal.h"
@@ -120,7 +120,7 @@ template <int BMN> struct AgPolicy {
             t.pn = (int)(in / rows);
             pm0 = grp * GM + (int)(in % rows);
         }
-        // the pages' swizzle: pid_m = (pid_m + rank * tiles_per_pe) % total
+        // Triton-distributed's swizzle: pid_m = (pid_m + rank * tiles_per_pe) % total
         const int pm = (pm0 + p.swz) % p.m_tiles;
         t.m0 = pm * tm + sub * gm::BM;
         t.n0 = t.pn * gm::BN;

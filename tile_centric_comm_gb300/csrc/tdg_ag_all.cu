@@ -12,7 +12,7 @@
 // by a stream-ordered write of rank r's flag for that signal group.  One
 // persistent tcgen05 GEMM launch on the main stream runs every rank's tiles,
 // rank by rank (each rank's B_r stays in L2 while its tiles run), each rank's
-// m tiles in the pages' swizzled order (its own shard first, read in place);
+// m tiles in Triton-distributed's swizzled order (its own shard first, read in place);
 // a tile's loader waits on the groups of its A rows with a bounded
 // ld.acquire spin before its TMA loads.
 // SERIAL mode: the same copies on the main stream, then the GEMM launch,
@@ -75,7 +75,7 @@ template <int BMN> struct AgAllPolicy {
             t.pn = (int)(in / rows);
             pm0 = grp * GM + (int)(in % rows);
         }
-        // the pages' swizzle: pid_m = (pid_m + rank * tiles_per_pe) % total
+        // Triton-distributed's swizzle: pid_m = (pid_m + rank * tiles_per_pe) % total
         const int pm = (pm0 + (int)(((int64_t)r * p.Ms / tm) % p.m_tiles)) % p.m_tiles;
         t.m0 = pm * tm + sub * gm::BM;
         t.n0 = t.pn * gm::BN;

@@ -2,7 +2,7 @@
 // status block carved out of one caller allocation), the device status, and
 // the host helpers every operation shares.
 //
-// The heap realises the pages' symmetric memory ("Triton-distributed 语义",
+// The heap realises Triton-distributed's symmetric memory ("Triton-distributed 语义",
 // 对称内存模型: every PE allocates at the same virtual address; symm_at maps a
 // local pointer to the peer's) on one GPU: region r stands for rank r's heap,
 // and symm_at is pointer arithmetic between regions.

@@ -6,7 +6,7 @@
 //
 // Each CTA runs 6 warps:
 //   warp 0      TMA loader: per tile it first runs the policy's signal wait
-//               (the wait / consume_token pair of the pages), then streams
+//               (Triton-distributed's wait / consume_token), then streams
 //               BK-wide slices of A and B into a shared-memory ring.
 //   warp 1      MMA issuer: one thread issues tcgen05.mma (K=16 per
 //               instruction) into one of two TMEM accumulators (2 x 256 fp32

@@ -1,6 +1,6 @@
 // tdg_ptx.cuh -- hand-written PTX wrappers for sm_103a: mbarrier, TMA (tensor
 // and 1-D bulk copies), tcgen05 (TMEM allocation, MMA, loads), memory-model
-// fences, and the bounded signal waits that realise the pages' notify / wait /
+// fences, and the bounded signal waits that realise Triton-distributed's notify / wait /
 // consume_token primitives ("Triton-distributed 语义", sections
 // 基于信号的同步 and 基于令牌的数据依赖) on one GPU.
 #pragma once
@@ -169,8 +169,8 @@ __device__ __forceinline__ bool epoch_reached(uint32_t flag, uint32_t epoch)
 }
 
 // wait: bounded acquire spin until flag >= epoch.  The acquire load plus the
-// "memory" clobber keep every later load below the wait (the role the pages
-// give consume_token); a caller that then reads through TMA adds
+// "memory" clobber keep every later load below the wait (the role
+// Triton-distributed gives consume_token); a caller that then reads through TMA adds
 // fence_proxy_async_global().  Returns false when the bound ran out.
 __device__ __forceinline__ bool wait_flag(const uint32_t *p, uint32_t epoch, uint64_t timeout_ns)
 {

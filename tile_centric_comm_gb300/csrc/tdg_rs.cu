@@ -11,7 +11,7 @@
 // or fp32 when asked; tile-contiguous, 128 x 256) into owner o's staging area
 // (region o) with TMA, waits for the write to complete, fences the async
 // proxy, and increments the owner's per-(tile, row-quarter) arrival counter
-// with acq_rel semantics (the pages' "increment" signal; the counter word is
+// with acq_rel semantics (Triton-distributed's "increment" signal; the counter word is
 // tagged with the call's epoch).  The epilogue warp whose increment completes
 // the count of W acquires the other W-1 pushes and owes the reduction of its
 // 32 rows: summing the W partials in fixed rank order (fp32, 16-byte
