@@ -360,6 +360,22 @@ class MLP:
                 raise RuntimeError(f"device fault during the bench: {st}")
 
 
+def max_over_ranks(x, pg, torch, device):
+    """The slowest rank's value: the job's steps end when its last rank's do.
+    `pg` is torch.distributed (or None for one process)."""
+    if not pg:
+        return x
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(world, flop_per_rank_step, steps, max_total_ms):
+    """Whole-job throughput: every rank's work (weak scaling: the same work
+    on each rank) over the slowest rank's time."""
+    return world * flop_per_rank_step * steps / (max_total_ms * 1e-3) / 1e12
+
+
 def timed_steps(torch, fns, steps, warmup, flush):
     """Run `fns` (one callable per part) once per step, flushing L2 before every
     step (outside the events); return per-part lists of device times (ms) of the
@@ -886,14 +902,11 @@ def main():
     clocks = clk.summary()
     step_ms = [sum(p[i] for p in parts) for i in range(args.steps)]
     total_ms = sum(step_ms)
-    if pg:
-        t = torch.tensor([total_ms], device="cuda")
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, pg, torch, "cuda")
     ms_per_step = total_ms / args.steps
     ag_flop = 2 * AG["W"] * AG["Ms"] * AG["K"] * AG["N"]
     flop = (ag_flop if args.only != "rs" else 0) + (RS_FLOP if args.only != "ag" else 0)
-    value = world * flop * args.steps / (total_ms * 1e-3) / 1e12
+    value = job_tflops(world, flop, args.steps, total_ms)
     launches = 2 * args.steps if not args.only else args.steps
     ag_ms = statistics.mean(parts[0]) if args.only != "rs" else None
     rs_ms = statistics.mean(parts[-1]) if args.only != "ag" else None
@@ -931,6 +944,7 @@ def main():
         mlp.check_status()
         # end to end through the public API with host buffers: one step at a
         # time, then consecutive steps overlapped over two buffer sets
+        barrier()
         eparts = timed_steps(torch, [mlp.e2e_step], args.steps, args.warmup, flush)
         e_one = statistics.mean(eparts[0])
         mlp2 = mlp.twin()
@@ -944,14 +958,16 @@ def main():
         e_w = mlp.e2e_pipelined([mlp, mlp2], args.steps, args.warmup, weights=False)
         mlp2.check_status()
         del mlp2
-        e2e = {"value": STEP_FLOP / e_ms / 1e9, "unit": "TFLOP/s",
-               "h2d_bytes_per_step": mlp.h2d_bytes, "d2h_bytes_per_step": mlp.d2h_bytes,
+        # whole job, as for `value`: every rank's steps over the slowest rank's time
+        e_ms, e_one, e_w = (max_over_ranks(x, pg, torch, "cuda") for x in (e_ms, e_one, e_w))
+        e2e = {"value": world * STEP_FLOP / e_ms / 1e9, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": world * mlp.h2d_bytes, "d2h_bytes_per_step": world * mlp.d2h_bytes,
                "ms_per_step": e_ms,
                "how": "consecutive steps overlapped over two device buffer sets (upload, compute and "
                       "download streams); every step copies all its inputs H2D and both outputs D2H",
-               "one_step_at_a_time": {"value": STEP_FLOP / e_one / 1e9, "ms_per_step": e_one},
-               "weights_resident": {"value": STEP_FLOP / e_w / 1e9, "ms_per_step": e_w,
-                                    "h2d_bytes_per_step": mlp.h2d_act_bytes,
+               "one_step_at_a_time": {"value": world * STEP_FLOP / e_one / 1e9, "ms_per_step": e_one},
+               "weights_resident": {"value": world * STEP_FLOP / e_w / 1e9, "ms_per_step": e_w,
+                                    "h2d_bytes_per_step": world * mlp.h2d_act_bytes,
                                     "what": "activations (AG shards, RS A_r) H2D every step, outputs D2H; "
                                             "B and B_r uploaded once before the timed steps"}}
         mlp.check_status()

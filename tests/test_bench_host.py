@@ -1,6 +1,7 @@
 """bench.py's host logic on CPU: the reference arm's JSON line (the oracle on a
-bounded sample), the silent exit of ranks other than 0, and the summary of the
-clock samples taken during a timed region."""
+bounded sample), the silent exit of ranks other than 0, the summary of the
+clock samples taken during a timed region, and, with two gloo ranks, the
+slowest-rank time and whole-job throughput that several replicas report."""
 import json
 import os
 import subprocess
@@ -83,3 +84,44 @@ def test_peaks_read_the_measured_file():
         assert pk["src"] == "measured" and pk["hbm"] == d["hbm_gbs"] and pk["bf16"] == d["bf16_tflops"]
     else:
         pytest.skip("no measured peaks in this checkout")
+
+
+def _rank_worker(rank, world, port, q):
+    import torch
+    import torch.distributed as dist
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        local_ms = [70.0, 75.5][rank]           # rank 1 is the slower one
+        worst = bench.max_over_ranks(local_ms, dist, torch, "cpu")
+        q.put((rank, worst, bench.job_tflops(world, 4.0e12, 50, worst)))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_report_the_slowest_rank_and_the_whole_job():
+    import socket
+    import torch.multiprocessing as mp
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    ps = [ctx.Process(target=_rank_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in ps:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in range(2))
+    for p in ps:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, worst, tflops in res:
+        assert worst == 75.5
+        # both ranks' 50 steps of 4 TFLOP over the slowest rank's 75.5 ms
+        assert tflops == pytest.approx(2 * 4.0e12 * 50 / 75.5e-3 / 1e12)
+
+
+def test_one_process_needs_no_group():
+    assert bench.max_over_ranks(12.5, None, None, "cpu") == 12.5
+    assert bench.job_tflops(1, 1e12, 10, 1000.0) == pytest.approx(10.0)
