@@ -166,10 +166,12 @@ TDG_API int tdg_device_info(int *sm_count, int *supported);
  * place, with no wait.
  *
  * B: K x N (TDG_B_KN) or N x K (TDG_B_NK) bf16, device pointer.
- * C: M x N bf16 output, device pointer.
+ * C: M x N output, device pointer: bf16 (each fp32 accumulator rounded to
+ * nearest even), or with c_f32 = 1 float32 (the fp32 accumulator itself, no
+ * rounding; M*N*4 bytes).  The caller owns B and C.
  * Requirements: 1 <= world <= 64; 0 <= rank < world; K % 8 == 0; N % 8 ==
  * 0; a_off, g_off, B, C 16-byte aligned; the gathered buffer not overlapping
- * the shard; signal_rows dividing Ms; source_order 0 or 1; CE mode needs a
+ * the shard; signal_rows dividing Ms; source_order and c_f32 0 or 1; CE mode needs a
  * side_stream other than stream; LL mode an aligned LL buffer that overlaps
  * neither the shard nor the gathered buffer; SM / LL producer CTAs fewer than
  * the GEMM's grid (TDG_ERR_INVALID otherwise).  g_off + M*K*2, a_off + Ms*K*2
@@ -199,6 +201,7 @@ typedef struct {
     int source_order;    /* 0: one source at a time, rank+1, rank+2, ... (the
                             published NVSwitch swizzle); 1: all sources at once,
                             round robin over sources (their full-mesh order) */
+    int c_f32;           /* 1: C is float32; 0: bf16                         */
 } tdg_ag_gemm_args;
 
 TDG_API int tdg_ag_gemm(tdg_symm *h, const tdg_ag_gemm_args *args, void *stream,

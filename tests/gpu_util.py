@@ -41,8 +41,9 @@ def assert_close(got_bits, ref64, tol=1e-2):
 class AGCase:
     """Inputs of one AllGather+GEMM call laid out in a symmetric heap."""
 
-    def __init__(self, inp, b_layout=tdg.B_KN, device="cuda", ll=False):
+    def __init__(self, inp, b_layout=tdg.B_KN, device="cuda", ll=False, c_f32=False):
         self.inp = inp
+        self.c_f32 = c_f32
         W, Ms, K, N = inp.W, inp.Ms, inp.K, inp.N
         self.M = W * Ms
         self.a_off = 0
@@ -58,7 +59,7 @@ class AGCase:
             self.B = to_dev_bf16(inp.B)
         else:
             self.B = to_dev_bf16(np.ascontiguousarray(inp.B.T))
-        self.C = torch.empty((self.M, N), dtype=torch.bfloat16, device=device)
+        self.C = torch.empty((self.M, N), dtype=torch.float32 if c_f32 else torch.bfloat16, device=device)
 
     def gathered(self, rank):
         return self.symm.view(rank, self.g_off, (self.M, self.inp.K), torch.bfloat16)
@@ -69,15 +70,20 @@ class AGCase:
 
     def run(self, rank=0, mode="sm", check_status=True, **kw):
         inp = self.inp
-        self.C.view(torch.int16).fill_(POISON)
+        if self.c_f32:
+            self.C.view(torch.int32).fill_(0x7FC00001)   # a NaN float32 pattern
+        else:
+            self.C.view(torch.int16).fill_(POISON)
         self.gathered(rank).view(torch.int16).fill_(POISON)
         side = torch.cuda.Stream() if mode == "ce" else None
         tdg.ag_gemm(self.symm, rank, inp.Ms, inp.K, inp.N, self.a_off, self.g_off, self.B, self.C,
-                    mode=mode, b_layout=self.b_layout, side_stream=side, **kw)
+                    mode=mode, b_layout=self.b_layout, side_stream=side, c_f32=self.c_f32, **kw)
         torch.cuda.synchronize()
         st = self.symm.status()
         if check_status:
             assert st["code"] == 0, st
+        if self.c_f32:
+            return self.C.cpu().numpy(), st      # float32 values
         return to_bits(self.C), st
 
 

@@ -40,6 +40,7 @@ def test_ag_gemm_rejections():
     assert _ag_rc(c, source_order=2) == tdg.TDG_ERR_INVALID
     assert _ag_rc(c, mode=7) == tdg.TDG_ERR_INVALID
     assert _ag_rc(c, b_layout=2) == tdg.TDG_ERR_INVALID
+    assert _ag_rc(c, c_f32=2) == tdg.TDG_ERR_INVALID
     torch.cuda.synchronize()
     assert c.symm.status()["code"] == 0
     got, _ = c.run(rank=1, mode="sm")                                  # still usable

@@ -41,7 +41,7 @@ struct AgParams {
     CUtensorMap tmA_g; // gathered A: M x K
     CUtensorMap tmA_l; // local shard in place: Ms x K
     CUtensorMap tmB;   // KN: {N, K} box {64, 64}; NK: {K, N} box {64, 256}
-    CUtensorMap tmC;   // C: {N, M} box {64, 32}
+    CUtensorMap tmC;   // C: bf16 {N, M} box {64, 32}, or fp32 {N, M} box {32, 32}
     DevStatus *status;
     uint32_t epoch;
     uint64_t timeout_ns;      // bound of a cross-CTA signal wait
@@ -78,9 +78,10 @@ struct AgParams {
     int ll;
     int n_send;
     uint64_t *ll_buf; // M * K / 2 words in region(rank)
+    int c_f32;        // 1: C is fp32
 };
 
-template <int BMN> struct AgPolicy {
+template <int BMN, bool F32 = false> struct AgPolicy {
     using Params = AgParams;
     static constexpr int B_MN = BMN;
 
@@ -209,13 +210,25 @@ template <int BMN> struct AgPolicy {
         return BMN ? (uint32_t)(((cols + 63) >> 6) * 8192) : (uint32_t)((p.pair ? gm::BN / 2 : gm::BN) * gm::BK * 2);
     }
 
-    static constexpr bool F32_OUT = false; // C is always bf16
+    // C is bf16 (RNE of the fp32 accumulator), or with F32 the accumulator
+    // itself, stored as fp32 chunks of 32 columns
+    static constexpr bool F32_OUT = F32;
+    __device__ static bool out_f32(const Params &) { return true; }
 
     __device__ static void store_chunk(const Params &p, const TileInfo &t, const void *buf, int ch, int q)
     {
         const int row = t.m0 + 32 * q;
         if (row < p.M)
             tma_store_2d(&p.tmC, buf, t.n0 + 64 * ch, row);
+    }
+
+    // (the second 32-column half of a 64-column chunk may start past N: skipped)
+    __device__ static void store_chunk_f32(const Params &p, const TileInfo &t, const void *buf, int sub, int q)
+    {
+        const int row = t.m0 + 32 * q;
+        const int col = t.n0 + 32 * sub;
+        if (row < p.M && col < p.N)
+            tma_store_2d(&p.tmC, buf, col, row);
     }
 
     struct EpiState {};
@@ -423,7 +436,7 @@ __device__ void ll_receiver(const AgParams &p, int cta, int ncta)
     }
 }
 
-template <int BMN, int CL>
+template <int BMN, int CL, bool F32>
 __global__ void __launch_bounds__(gm::NUM_THREADS, 1) ag_gemm_kernel(const __grid_constant__ AgParams p)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -436,7 +449,7 @@ __global__ void __launch_bounds__(gm::NUM_THREADS, 1) ag_gemm_kernel(const __gri
             ag_producer(p, smem);
             if (p.tail_lo < T) {
                 __syncthreads(); // every copy worker of this CTA is done with the ring
-                gemm_consumer<AgPolicy<BMN>, CL>(p, smem, (int)blockIdx.x / CL, p.n_prod / CL, p.tail_lo, T);
+                gemm_consumer<AgPolicy<BMN, F32>, CL>(p, smem, (int)blockIdx.x / CL, p.n_prod / CL, p.tail_lo, T);
             }
         } else if ((int)blockIdx.x < p.n_send) {
             ll_sender(p, blockIdx.x, p.n_send);
@@ -446,7 +459,7 @@ __global__ void __launch_bounds__(gm::NUM_THREADS, 1) ag_gemm_kernel(const __gri
         return;
     }
     const int c = (int)blockIdx.x - p.n_prod, nc = (int)gridDim.x - p.n_prod;
-    gemm_consumer<AgPolicy<BMN>, CL>(p, smem, c / CL, nc / CL, 0, p.tail_lo < T ? p.tail_lo : T);
+    gemm_consumer<AgPolicy<BMN, F32>, CL>(p, smem, c / CL, nc / CL, 0, p.tail_lo < T ? p.tail_lo : T);
 }
 
 } // namespace tdg
@@ -456,15 +469,18 @@ using namespace tdg_host;
 
 namespace {
 
-const void *ag_kernel_fn(int b_layout, int cl)
+template <int BMN, bool F32> const void *ag_kernel_cl(int cl)
+{
+    return cl == 4   ? reinterpret_cast<const void *>(&ag_gemm_kernel<BMN, 4, F32>)
+           : cl == 2 ? reinterpret_cast<const void *>(&ag_gemm_kernel<BMN, 2, F32>)
+                     : reinterpret_cast<const void *>(&ag_gemm_kernel<BMN, 1, F32>);
+}
+
+const void *ag_kernel_fn(int b_layout, int cl, bool f32)
 {
     if (b_layout == TDG_B_KN)
-        return cl == 4   ? reinterpret_cast<const void *>(&ag_gemm_kernel<1, 4>)
-               : cl == 2 ? reinterpret_cast<const void *>(&ag_gemm_kernel<1, 2>)
-                         : reinterpret_cast<const void *>(&ag_gemm_kernel<1, 1>);
-    return cl == 4   ? reinterpret_cast<const void *>(&ag_gemm_kernel<0, 4>)
-           : cl == 2 ? reinterpret_cast<const void *>(&ag_gemm_kernel<0, 2>)
-                     : reinterpret_cast<const void *>(&ag_gemm_kernel<0, 1>);
+        return f32 ? ag_kernel_cl<1, true>(cl) : ag_kernel_cl<1, false>(cl);
+    return f32 ? ag_kernel_cl<0, true>(cl) : ag_kernel_cl<0, false>(cl);
 }
 
 int prepare(const void *fn)
@@ -478,9 +494,9 @@ int ag_grid(const AgParams &p, int b_layout, int sms)
 {
     if (p.cl == 1)
         return sms;
-    if (prepare(ag_kernel_fn(b_layout, p.cl)) != TDG_OK)
+    if (prepare(ag_kernel_fn(b_layout, p.cl, p.c_f32 != 0)) != TDG_OK)
         return 0;
-    const int mc = max_clusters(ag_kernel_fn(b_layout, p.cl), gm::NUM_THREADS, gm::SMEM_BYTES, p.cl);
+    const int mc = max_clusters(ag_kernel_fn(b_layout, p.cl, p.c_f32 != 0), gm::NUM_THREADS, gm::SMEM_BYTES, p.cl);
     const int n = mc > 0 ? (mc < sms / p.cl ? mc : sms / p.cl) : 0;
     return p.cl * n;
 }
@@ -524,7 +540,7 @@ int64_t producer_tail_lo(const AgParams &p, int grid, int TM)
 
 int launch_ag(const AgParams &p, int b_layout, int grid, bool coop, cudaStream_t s)
 {
-    const void *fn = ag_kernel_fn(b_layout, p.cl);
+    const void *fn = ag_kernel_fn(b_layout, p.cl, p.c_f32 != 0);
     int rc = prepare(fn);
     if (rc != TDG_OK)
         return rc;
@@ -576,7 +592,10 @@ extern "C" int tdg_ag_gemm(tdg_symm *h, const tdg_ag_gemm_args *a, void *stream,
         return TDG_ERR_INVALID;
     if (a->b_layout != TDG_B_KN && a->b_layout != TDG_B_NK)
         return TDG_ERR_INVALID;
+    if (a->c_f32 != 0 && a->c_f32 != 1)
+        return TDG_ERR_INVALID;
     const int64_t Ms = a->Ms, K = a->K, N = a->N, M = (int64_t)W * Ms;
+    const size_t c_elem = a->c_f32 ? 4 : 2;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (M == 0 || N == 0)
         return TDG_OK;
@@ -591,7 +610,7 @@ extern "C" int tdg_ag_gemm(tdg_symm *h, const tdg_ag_gemm_args *a, void *stream,
     if (a->g_off < a->a_off + shard_bytes && a->a_off < a->g_off + gath_bytes && K > 0)
         return TDG_ERR_INVALID; // the gathered buffer overlaps the shard
     if (K == 0)
-        return cuda_err(cudaMemsetAsync(a->C, 0, (size_t)M * N * 2, s), "ag K==0");
+        return cuda_err(cudaMemsetAsync(a->C, 0, (size_t)M * N * c_elem, s), "ag K==0");
     const bool ll = a->mode == TDG_MODE_LL;
     const uint64_t ll_bytes = (uint64_t)M * K * 4;
     if (ll) {
@@ -630,7 +649,7 @@ extern "C" int tdg_ag_gemm(tdg_symm *h, const tdg_ag_gemm_args *a, void *stream,
         ok = ok && map_bf16_2d(&p.tmB, a->B, N, K, N * 2, 64, 64);
     else
         ok = ok && map_bf16_2d(&p.tmB, a->B, K, N, K * 2, 64, cl == 4 ? 64 : (pair ? 128 : 256));
-    ok = ok && map_bf16_2d(&p.tmC, a->C, N, M, N * 2, 64, 32);
+    ok = ok && (a->c_f32 ? map_f32_2d(&p.tmC, a->C, N, M, N * 4, 32, 32) : map_bf16_2d(&p.tmC, a->C, N, M, N * 2, 64, 32));
     if (!ok)
         return TDG_ERR_CUDA;
 
@@ -652,6 +671,7 @@ extern "C" int tdg_ag_gemm(tdg_symm *h, const tdg_ag_gemm_args *a, void *stream,
     p.group_m = ((uint64_t)K * N * 2 > (64ull << 20)) ? 8 : 0;
     p.n_tiles = (int)((N + gm::BN - 1) / gm::BN);
     p.tail_lo = (int64_t)p.m_tiles * p.n_tiles; // no items for the producer CTAs
+    p.c_f32 = a->c_f32;
     p.swz = a->swizzle ? (int)(((int64_t)rank * Ms / TM) % p.m_tiles) : 0;
     p.local_inplace = inplace ? 1 : 0;
     p.local_lo = inplace ? (int)(rank * Ms / TM) : 0;

@@ -87,6 +87,16 @@ bool map_bf16_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uin
                         CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+bool map_f32_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer,
+                uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer)
+{
+    const uint64_t dims[2] = {inner, outer};
+    const uint64_t str[1] = {row_bytes};
+    const uint32_t box[2] = {box_inner, box_outer};
+    return encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, str, box,
+                        CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
 bool map_f32_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2,
                 uint64_t s1_bytes, uint64_t s2_bytes, uint32_t b0, uint32_t b1, uint32_t b2)
 {

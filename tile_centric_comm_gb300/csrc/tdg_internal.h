@@ -55,6 +55,8 @@ bool map_bf16_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t oute
 bool map_bf16_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2,
                  uint64_t s1_bytes, uint64_t s2_bytes, uint32_t b0, uint32_t b1, uint32_t b2);
 // The same for fp32 elements.
+bool map_f32_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer,
+                uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);
 bool map_f32_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2,
                 uint64_t s1_bytes, uint64_t s2_bytes, uint32_t b0, uint32_t b1, uint32_t b2);
 

@@ -52,7 +52,8 @@ class AgGemmArgs(ctypes.Structure):
                 ("N", _i64), ("a_off", _sz), ("g_off", _sz), ("B", _vp), ("C", _vp),
                 ("b_layout", ctypes.c_int), ("mode", ctypes.c_int), ("producers", ctypes.c_int),
                 ("signal_rows", _i64), ("swizzle", ctypes.c_int), ("timeout_ns", _u64),
-                ("ll_off", _sz), ("test_skip_notify", _u64), ("source_order", ctypes.c_int)]
+                ("ll_off", _sz), ("test_skip_notify", _u64), ("source_order", ctypes.c_int),
+                ("c_f32", ctypes.c_int)]
 
 
 class AgGemmAllArgs(ctypes.Structure):
@@ -281,16 +282,17 @@ class Symm:
 def ag_gemm(symm: Symm, rank: int, Ms: int, K: int, N: int, a_off: int, g_off: int, B, C,
             mode="sm", b_layout=B_KN, producers=0, signal_rows=0, swizzle=True,
             timeout_ns=0, ll_off=0, test_skip_notify=0, source_order=0, stream=None,
-            side_stream=None):
+            side_stream=None, c_f32=False):
+    """c_f32: C is float32 (the fp32 accumulator, unrounded) instead of bf16."""
     import torch
     dev = symm.buf.device
     a = AgGemmArgs(world=symm.world, rank=rank, Ms=Ms, K=K, N=N, a_off=a_off, g_off=g_off,
                    B=_tensor(B, "B", torch.bfloat16, K * N, dev),
-                   C=_tensor(C, "C", torch.bfloat16, symm.world * Ms * N, dev),
+                   C=_tensor(C, "C", torch.float32 if c_f32 else torch.bfloat16, symm.world * Ms * N, dev),
                    b_layout=b_layout, mode=MODES[mode],
                    producers=producers, signal_rows=signal_rows, swizzle=1 if swizzle else 0,
                    timeout_ns=timeout_ns, ll_off=ll_off, test_skip_notify=test_skip_notify,
-                   source_order=source_order)
+                   source_order=source_order, c_f32=1 if c_f32 else 0)
     side = _vp(side_stream.cuda_stream) if side_stream is not None else _vp(None)
     _check(lib().tdg_ag_gemm(symm.h, ctypes.byref(a), _stream(stream), side), "tdg_ag_gemm")
 
