@@ -31,6 +31,25 @@
  *     (tdg_symm_alloc records the current device); calling it while another
  *     device is current returns TDG_ERR_INVALID.  Any host thread may call:
  *     the call makes that device's context current in the calling thread.
+ *
+ * Environment variables (read at each call; each selects among schedules of
+ * the same computation, and the tests check every setting against the oracle):
+ *   TDG_PAIR=0            GEMMs on one CTA per 128-row tile instead of CTA
+ *                         pairs (cta_group::2, 256-row tiles).
+ *   TDG_QUAD=0            CTA pairs alone instead of clusters of two pairs
+ *                         that share each B slice by TMA multicast.
+ *   TDG_SPLIT_TAIL=1      AG-GEMM: split the tiles of the last, partial wave
+ *                         into 128-column halves.
+ *   TDG_AG_PROD_ROUNDS=n  AG-GEMM SM mode: the producer clusters take n
+ *                         rounds of GEMM tiles after their copies (-1: none);
+ *                         unset, the split is estimated on the host.
+ *   TDG_RS_ORDER=1        GEMM-RS: rank-fastest tile order instead of owner
+ *                         blocks.
+ *   TDG_RS_RED_ROWS=r     GEMM-RS: rows of an owed reduction worked off per
+ *                         tile (4, 8, 16 or 32; default 32 for bf16 partials,
+ *                         8 for fp32).
+ *   TDG_LOG=1             print host-side failures (tensor-map encoding,
+ *                         MoE workspace) to stderr.
  */
 #ifndef TDG_H_
 #define TDG_H_
