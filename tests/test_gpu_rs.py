@@ -22,6 +22,25 @@ def test_integer_small_k_bit_exact_both_modes(W, M):
         assert np.array_equal(got, out16), mode
 
 
+@pytest.mark.parametrize("order", ["1", "0"])
+@pytest.mark.parametrize("W,M", [(4, 2048), (8, 4096)])
+def test_rank_fastest_tile_order_gives_the_same_bits(W, M, order, monkeypatch):
+    # TDG_RS_ORDER=1 walks the tiles rank-fastest instead of in owner blocks;
+    # the reduction still sums in rank order, so the bits do not change
+    monkeypatch.setenv("TDG_RS_ORDER", order)
+    inp = synth.rs_inputs(W, M, 64, 264, "int2", seed=W + M)
+    _, out16 = oracle.gemm_rs(inp.As, inp.Bs)
+    case = RSCase(inp)
+    for mode in ("sm", "serial"):
+        got, _ = case.run(mode=mode)
+        assert np.array_equal(got, out16), mode
+    monkeypatch.setenv("TDG_RS_ORDER", order)
+    f = synth.rs_inputs(W, M, 200, 264, "normal", seed=W * M)
+    ref = RSCase(f).run(mode="sm")[0]
+    monkeypatch.setenv("TDG_RS_ORDER", "0" if order == "1" else "1")
+    assert np.array_equal(RSCase(f).run(mode="sm")[0], ref)
+
+
 @pytest.mark.parametrize("pair", ["1", "0"])
 @pytest.mark.parametrize("b_layout", [tdg.B_KN, tdg.B_NK])
 @pytest.mark.parametrize("W,M,K,N", [
