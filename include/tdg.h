@@ -248,7 +248,7 @@ TDG_API int tdg_ag_gemm(tdg_symm *h, const tdg_ag_gemm_args *args, void *stream,
  * shard start at once; its flag waits are bounded by timeout_ns, within
  * which this call queues the copies behind it.  SERIAL mode: the copies,
  * then the GEMM, on `stream`.
- * Requirements: 1 <= world <= 64; K % 8 == 0; N % 8 == 0; offsets 16-byte
+ * Requirements: 1 <= world <= 64; K % 8 == 0; N % 8 == 0; c_f32 0 or 1; offsets 16-byte
  * aligned; every buffer inside its region (else TDG_ERR_NOMEM); the gathered
  * buffers and C_r overlapping no other buffer (else TDG_ERR_INVALID);
  * signal_rows dividing Ms; M / signal_rows <= signals_per_rank.  M == 0 or
@@ -264,6 +264,8 @@ typedef struct {
     uint64_t timeout_ns; /* bound of every device wait; 0 = 2 s               */
     uint64_t test_skip_notify; /* tests only: rank 0's flag of signal group g
                                   is not written when bit (g % 64) is set     */
+    int c_f32;           /* 1: C_r is float32 (M*N*4 bytes, the fp32
+                            accumulator unrounded); 0: bf16                   */
 } tdg_ag_gemm_all_args;
 
 TDG_API int tdg_ag_gemm_all_ranks(tdg_symm *h, const tdg_ag_gemm_all_args *args, void *stream,

@@ -6,21 +6,22 @@ import torch
 
 import oracle
 from tile_centric_comm_gb300 import synth, tdg
-from gpu_util import AGCase, POISON, align, assert_close, to_bits, to_dev_bf16
+from gpu_util import AGCase, POISON, align, assert_close, bf16_f64, to_bits, to_dev_bf16
 
 pytestmark = pytest.mark.gpu
 
 
 class AGAllCase:
-    def __init__(self, inp, b_layout=tdg.B_KN):
+    def __init__(self, inp, b_layout=tdg.B_KN, c_f32=False):
         self.inp = inp
+        self.c_f32 = c_f32
         W, Ms, K, N = inp.W, inp.Ms, inp.K, inp.N
         self.M = M = W * Ms
         self.a_off = 0
         self.g_off = align(Ms * K * 2)
         self.b_off = align(self.g_off + M * K * 2)
         self.c_off = align(self.b_off + K * N * 2)
-        self.symm = tdg.Symm(W, align(self.c_off + M * N * 2 + 1024), max(1024, M))
+        self.symm = tdg.Symm(W, align(self.c_off + M * N * (4 if c_f32 else 2) + 1024), max(1024, M))
         self.b_layout = b_layout
         for r in range(W):
             self.symm.view(r, self.a_off, (Ms, K), torch.bfloat16).copy_(to_dev_bf16(inp.shards[r]))
@@ -28,7 +29,8 @@ class AGAllCase:
             self.symm.view(r, self.b_off, b.shape, torch.bfloat16).copy_(to_dev_bf16(b))
 
     def C(self, r):
-        return self.symm.view(r, self.c_off, (self.M, self.inp.N), torch.bfloat16)
+        return self.symm.view(r, self.c_off, (self.M, self.inp.N),
+                              torch.float32 if self.c_f32 else torch.bfloat16)
 
     def gathered(self, r):
         return self.symm.view(r, self.g_off, (self.M, self.inp.K), torch.bfloat16)
@@ -36,15 +38,21 @@ class AGAllCase:
     def run(self, mode="ce", check_status=True, **kw):
         inp = self.inp
         for r in range(inp.W):
-            self.C(r).view(torch.int16).fill_(POISON)
+            if self.c_f32:
+                self.C(r).view(torch.int32).fill_(0x7FC00001)     # a NaN float32 pattern
+            else:
+                self.C(r).view(torch.int16).fill_(POISON)
             self.gathered(r).view(torch.int16).fill_(POISON)
         side = torch.cuda.Stream() if mode == "ce" else None
         tdg.ag_gemm_all_ranks(self.symm, inp.Ms, inp.K, inp.N, self.a_off, self.g_off, self.b_off,
-                              self.c_off, mode=mode, b_layout=self.b_layout, side_stream=side, **kw)
+                              self.c_off, mode=mode, b_layout=self.b_layout, side_stream=side,
+                              c_f32=self.c_f32, **kw)
         torch.cuda.synchronize()
         st = self.symm.status()
         if check_status:
             assert st["code"] == 0, st
+        if self.c_f32:
+            return [self.C(r).cpu().numpy() for r in range(inp.W)], st
         return [to_bits(self.C(r)) for r in range(inp.W)], st
 
 
@@ -106,3 +114,19 @@ def test_degenerate_shapes():
                           mode="serial")                         # M == 0: no-op
     torch.cuda.synchronize()
     assert case.symm.status()["code"] == 0
+
+
+@pytest.mark.parametrize("W,Ms,N", [(2, 512, 264), (4, 256, 136)])   # two-pair clusters; pairs
+def test_f32_output_exact_where_bf16_rounds(W, Ms, N):
+    # integers in [-2, 2] and K = 1032: every C_r value (up to 4128) is exact in
+    # the fp32 accumulator but not in bf16
+    inp = synth.ag_all_inputs(W, Ms, 1032, N, "int2", seed=W + N)
+    case = AGAllCase(inp, c_f32=True)
+    want = [oracle.ag_gemm(inp.shards, inp.Bs[r])[0] for r in range(W)]
+    assert any(not np.array_equal(bf16_f64(oracle.ag_gemm(inp.shards, inp.Bs[r])[1]), want[r])
+               for r in range(W))
+    for mode in ("ce", "serial"):
+        got, _ = case.run(mode=mode)
+        for r in range(W):
+            assert got[r].dtype == np.float32
+            assert np.array_equal(got[r].astype(np.float64), want[r]), (mode, r)

@@ -171,6 +171,8 @@ def test_ag_gemm_all_ranks_rejections():
     assert rc(g_off=c.a_off) == tdg.TDG_ERR_INVALID                   # gathered overlaps the shard
     assert rc(signal_rows=48) == tdg.TDG_ERR_INVALID                  # does not divide Ms
     assert rc(world=3) == tdg.TDG_ERR_INVALID
+    assert rc(c_f32=2) == tdg.TDG_ERR_INVALID
+    assert rc(c_f32=1) == tdg.TDG_ERR_NOMEM                         # fp32 C_r runs past the region
     assert rc(Ms=1 << 20) == tdg.TDG_ERR_NOMEM
     torch.cuda.synchronize()
     assert c.symm.status()["code"] == 0

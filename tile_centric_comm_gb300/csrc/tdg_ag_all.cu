@@ -26,7 +26,7 @@ struct AgAllParams {
     CUtensorMap tmA_g; // gathered A of every rank: {K, M, W}, plane stride = region bytes
     CUtensorMap tmA_l; // the shards, read in place: {K, Ms, W}
     CUtensorMap tmB;   // B_r: KN {N, K, W} box {64, 64, 1}; NK {K, N, W} box {64, rows, 1}
-    CUtensorMap tmC;   // C_r: {N, M, W} box {64, 32, 1}
+    CUtensorMap tmC;   // C_r: bf16 {N, M, W} box {64, 32, 1}, or fp32 box {32, 32, 1}
     DevStatus *status;
     uint32_t epoch;
     uint64_t timeout_ns;      // bound of a flag wait
@@ -44,12 +44,15 @@ struct AgAllParams {
     uint64_t nsig;         // flag words per rank
     int wait_flags;
     int64_t sig_rows;
+    int c_f32; // 1: C_r is fp32
 };
 
-template <int BMN> struct AgAllPolicy {
+template <int BMN, bool F32 = false> struct AgAllPolicy {
     using Params = AgAllParams;
     static constexpr int B_MN = BMN;
-    static constexpr bool F32_OUT = false; // C_r is bf16
+    // C_r is bf16, or with F32 the fp32 accumulator itself (32-column chunks)
+    static constexpr bool F32_OUT = F32;
+    __device__ static bool out_f32(const Params &) { return true; }
     struct EpiState {};
 
     __device__ static int64_t num_items(const Params &p) { return (int64_t)p.W * p.m_tiles * p.n_tiles; }
@@ -166,15 +169,24 @@ template <int BMN> struct AgAllPolicy {
             tma_store_3d(&p.tmC, buf, t.n0 + 64 * ch, row, t.owner);
     }
 
+    // (the second 32-column half of a 64-column chunk may start past N: skipped)
+    __device__ static void store_chunk_f32(const Params &p, const TileInfo &t, const void *buf, int sub, int q)
+    {
+        const int row = t.m0 + 32 * q;
+        const int col = t.n0 + 32 * sub;
+        if (row < p.M && col < p.N)
+            tma_store_3d(&p.tmC, buf, col, row, t.owner);
+    }
+
     __device__ static void after_tile(const Params &, const TileInfo &, int, int, EpiState &, bool) {}
 };
 
-template <int BMN, int CL>
+template <int BMN, int CL, bool F32>
 __global__ void __launch_bounds__(gm::NUM_THREADS, 1) ag_all_gemm_kernel(const __grid_constant__ AgAllParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
-    gemm_consumer<AgAllPolicy<BMN>, CL>(p, smem, (int)blockIdx.x / CL, (int)gridDim.x / CL);
+    gemm_consumer<AgAllPolicy<BMN, F32>, CL>(p, smem, (int)blockIdx.x / CL, (int)gridDim.x / CL);
 }
 
 } // namespace tdg
@@ -184,15 +196,18 @@ using namespace tdg_host;
 
 namespace {
 
-const void *ag_all_kernel_fn(int b_layout, int cl)
+template <int BMN, bool F32> const void *ag_all_kernel_cl(int cl)
+{
+    return cl == 4   ? reinterpret_cast<const void *>(&ag_all_gemm_kernel<BMN, 4, F32>)
+           : cl == 2 ? reinterpret_cast<const void *>(&ag_all_gemm_kernel<BMN, 2, F32>)
+                     : reinterpret_cast<const void *>(&ag_all_gemm_kernel<BMN, 1, F32>);
+}
+
+const void *ag_all_kernel_fn(int b_layout, int cl, bool f32)
 {
     if (b_layout == TDG_B_KN)
-        return cl == 4   ? reinterpret_cast<const void *>(&ag_all_gemm_kernel<1, 4>)
-               : cl == 2 ? reinterpret_cast<const void *>(&ag_all_gemm_kernel<1, 2>)
-                         : reinterpret_cast<const void *>(&ag_all_gemm_kernel<1, 1>);
-    return cl == 4   ? reinterpret_cast<const void *>(&ag_all_gemm_kernel<0, 4>)
-           : cl == 2 ? reinterpret_cast<const void *>(&ag_all_gemm_kernel<0, 2>)
-                     : reinterpret_cast<const void *>(&ag_all_gemm_kernel<0, 1>);
+        return f32 ? ag_all_kernel_cl<1, true>(cl) : ag_all_kernel_cl<1, false>(cl);
+    return f32 ? ag_all_kernel_cl<0, true>(cl) : ag_all_kernel_cl<0, false>(cl);
 }
 
 bool meet(uint64_t x0, uint64_t x1, uint64_t y0, uint64_t y1) { return x0 < y1 && y0 < x1; }
@@ -213,7 +228,10 @@ extern "C" int tdg_ag_gemm_all_ranks(tdg_symm *h, const tdg_ag_gemm_all_args *a,
         return TDG_ERR_INVALID;
     if (a->b_layout != TDG_B_KN && a->b_layout != TDG_B_NK)
         return TDG_ERR_INVALID;
+    if (a->c_f32 != 0 && a->c_f32 != 1)
+        return TDG_ERR_INVALID;
     const int64_t Ms = a->Ms, K = a->K, N = a->N, M = (int64_t)W * Ms;
+    const uint64_t c_elem = a->c_f32 ? 4 : 2;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (M == 0 || N == 0)
         return TDG_OK;
@@ -222,7 +240,7 @@ extern "C" int tdg_ag_gemm_all_ranks(tdg_symm *h, const tdg_ag_gemm_all_args *a,
         return TDG_ERR_INVALID;
     const uint64_t R = h->region_bytes;
     const uint64_t a_end = a->a_off + (uint64_t)Ms * K * 2, g_end = a->g_off + (uint64_t)M * K * 2;
-    const uint64_t b_end = a->b_off + (uint64_t)K * N * 2, c_end = a->c_off + (uint64_t)M * N * 2;
+    const uint64_t b_end = a->b_off + (uint64_t)K * N * 2, c_end = a->c_off + (uint64_t)M * N * c_elem;
     if (a_end > R || g_end > R || b_end > R || c_end > R)
         return TDG_ERR_NOMEM;
     // the buffers written (gathered, C) overlap nothing else
@@ -233,7 +251,7 @@ extern "C" int tdg_ag_gemm_all_ranks(tdg_symm *h, const tdg_ag_gemm_all_args *a,
         return TDG_ERR_INVALID;
     if (K == 0) {
         for (int r = 0; r < W; ++r) {
-            cudaError_t e = cudaMemsetAsync(h->base + (size_t)r * R + a->c_off, 0, (size_t)M * N * 2, s);
+            cudaError_t e = cudaMemsetAsync(h->base + (size_t)r * R + a->c_off, 0, (size_t)(M * N * c_elem), s);
             if (e != cudaSuccess)
                 return cuda_err(e, "ag all K==0");
         }
@@ -260,7 +278,8 @@ extern "C" int tdg_ag_gemm_all_ranks(tdg_symm *h, const tdg_ag_gemm_all_args *a,
     else
         ok = ok && map_bf16_3d(&p.tmB, h->base + a->b_off, K, N, W, K * 2, R, 64,
                                cl == 4 ? 64 : (pair ? 128 : 256), 1);
-    ok = ok && map_bf16_3d(&p.tmC, h->base + a->c_off, N, M, W, N * 2, R, 64, 32, 1);
+    ok = ok && (a->c_f32 ? map_f32_3d(&p.tmC, h->base + a->c_off, N, M, W, N * 4, R, 32, 32, 1)
+                         : map_bf16_3d(&p.tmC, h->base + a->c_off, N, M, W, N * 2, R, 64, 32, 1));
     if (!ok)
         return TDG_ERR_CUDA;
     const uint32_t epoch = next_epoch(h);
@@ -285,8 +304,9 @@ extern "C" int tdg_ag_gemm_all_ranks(tdg_symm *h, const tdg_ag_gemm_all_args *a,
     p.flags = h->flags;
     p.nsig = h->nsig;
     p.sig_rows = sig_rows;
+    p.c_f32 = a->c_f32;
 
-    const void *fn = ag_all_kernel_fn(a->b_layout, cl);
+    const void *fn = ag_all_kernel_fn(a->b_layout, cl, a->c_f32 != 0);
     if (cudaError_t e = set_smem(fn, gm::SMEM_BYTES); e != cudaSuccess)
         return cuda_err(e, "ag all set smem");
     int grid = h->sm_count;

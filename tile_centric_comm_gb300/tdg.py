@@ -60,7 +60,7 @@ class AgGemmAllArgs(ctypes.Structure):
     _fields_ = [("world", ctypes.c_int), ("Ms", _i64), ("K", _i64), ("N", _i64), ("a_off", _sz),
                 ("g_off", _sz), ("b_off", _sz), ("c_off", _sz), ("b_layout", ctypes.c_int),
                 ("mode", ctypes.c_int), ("signal_rows", _i64), ("timeout_ns", _u64),
-                ("test_skip_notify", _u64)]
+                ("test_skip_notify", _u64), ("c_f32", ctypes.c_int)]
 
 
 class GemmRsArgs(ctypes.Structure):
@@ -299,12 +299,14 @@ def ag_gemm(symm: Symm, rank: int, Ms: int, K: int, N: int, a_off: int, g_off: i
 
 def ag_gemm_all_ranks(symm: Symm, Ms: int, K: int, N: int, a_off: int, g_off: int, b_off: int,
                       c_off: int, mode="ce", b_layout=B_KN, signal_rows=0, timeout_ns=0,
-                      test_skip_notify=0, stream=None, side_stream=None):
+                      test_skip_notify=0, stream=None, side_stream=None, c_f32=False):
     """AllGather+GEMM of every rank in one call: C_r = concat(A_0..A_{W-1}) @ B_r,
-    with A_r, the gathered buffers, B_r and C_r all in the heap (offsets)."""
+    with A_r, the gathered buffers, B_r and C_r all in the heap (offsets).
+    c_f32: C_r is float32 (the fp32 accumulator, unrounded) instead of bf16."""
     a = AgGemmAllArgs(world=symm.world, Ms=Ms, K=K, N=N, a_off=a_off, g_off=g_off, b_off=b_off,
                       c_off=c_off, b_layout=b_layout, mode=MODES[mode], signal_rows=signal_rows,
-                      timeout_ns=timeout_ns, test_skip_notify=test_skip_notify)
+                      timeout_ns=timeout_ns, test_skip_notify=test_skip_notify,
+                      c_f32=1 if c_f32 else 0)
     side = _vp(side_stream.cuda_stream) if side_stream is not None else _vp(None)
     _check(lib().tdg_ag_gemm_all_ranks(symm.h, ctypes.byref(a), _stream(stream), side),
            "tdg_ag_gemm_all_ranks")
