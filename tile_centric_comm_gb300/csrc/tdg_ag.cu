@@ -756,12 +756,8 @@ extern "C" int tdg_ag_gemm(tdg_symm *h, const tdg_ag_gemm_args *a, void *stream,
     if (!side || side == s)
         return TDG_ERR_INVALID;
     cudaEvent_t ev0, ev1;
-    if (cudaEventCreateWithFlags(&ev0, cudaEventDisableTiming) != cudaSuccess)
+    if (!ce_events(h, ev0, ev1))
         return TDG_ERR_CUDA;
-    if (cudaEventCreateWithFlags(&ev1, cudaEventDisableTiming) != cudaSuccess) {
-        cudaEventDestroy(ev0);
-        return TDG_ERR_CUDA;
-    }
     int rc = TDG_OK;
     cudaError_t e = cudaEventRecord(ev0, s);
     if (e == cudaSuccess)
@@ -801,7 +797,5 @@ extern "C" int tdg_ag_gemm(tdg_symm *h, const tdg_ag_gemm_args *a, void *stream,
         e = cudaStreamWaitEvent(s, ev1, 0);
     if (e != cudaSuccess && rc == TDG_OK)
         rc = cuda_err(e, "ce join");
-    cudaEventDestroy(ev0);
-    cudaEventDestroy(ev1);
     return rc;
 }

@@ -360,12 +360,8 @@ extern "C" int tdg_ag_gemm_all_ranks(tdg_symm *h, const tdg_ag_gemm_all_args *a,
     if (!side || side == s)
         return TDG_ERR_INVALID;
     cudaEvent_t ev0, ev1;
-    if (cudaEventCreateWithFlags(&ev0, cudaEventDisableTiming) != cudaSuccess)
+    if (!ce_events(h, ev0, ev1))
         return TDG_ERR_CUDA;
-    if (cudaEventCreateWithFlags(&ev1, cudaEventDisableTiming) != cudaSuccess) {
-        cudaEventDestroy(ev0);
-        return TDG_ERR_CUDA;
-    }
     int rc = TDG_OK;
     cudaError_t e = cudaEventRecord(ev0, s);
     if (e == cudaSuccess)
@@ -387,7 +383,5 @@ extern "C" int tdg_ag_gemm_all_ranks(tdg_symm *h, const tdg_ag_gemm_all_args *a,
         e = cudaStreamWaitEvent(s, ev1, 0);
     if (e != cudaSuccess && rc == TDG_OK)
         rc = cuda_err(e, "ag all join");
-    cudaEventDestroy(ev0);
-    cudaEventDestroy(ev1);
     return rc;
 }

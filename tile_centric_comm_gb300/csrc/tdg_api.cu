@@ -264,6 +264,11 @@ int tdg_symm_alloc(void *dev_base, size_t bytes, int world, size_t region_bytes,
 
 int tdg_symm_free(tdg_symm *h)
 {
+    if (h) {
+        for (cudaEvent_t e : h->ce_ev)
+            if (e)
+                cudaEventDestroy(e); // pending work on an event may still finish; its resources go then
+    }
     delete h;
     return TDG_OK;
 }

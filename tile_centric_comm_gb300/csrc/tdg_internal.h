@@ -24,9 +24,24 @@ struct tdg_symm {
     uint32_t epoch;         // last epoch handed out
     int device;
     int sm_count;
+    cudaEvent_t ce_ev[2] = {nullptr, nullptr}; // fork / join events of CE-mode calls, made once
 };
 
 namespace tdg_host {
+
+// The handle's fork / join events for CE-mode calls, created on first use
+// (timing disabled) and destroyed with the handle.  Returns false on failure.
+inline bool ce_events(tdg_symm *h, cudaEvent_t &ev0, cudaEvent_t &ev1)
+{
+    for (int i = 0; i < 2; ++i)
+        if (!h->ce_ev[i] && cudaEventCreateWithFlags(&h->ce_ev[i], cudaEventDisableTiming) != cudaSuccess) {
+            h->ce_ev[i] = nullptr;
+            return false;
+        }
+    ev0 = h->ce_ev[0];
+    ev1 = h->ce_ev[1];
+    return true;
+}
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
