@@ -110,6 +110,8 @@ TDG_API size_t tdg_symm_bytes(int world, size_t region_bytes, size_t signals_per
  * The signal areas and the status block are zeroed here (synchronously, with
  * cudaMemset on the current device).  dev_base must be 1024-byte aligned.
  * The caller keeps ownership of the memory; tdg_symm_free never frees it.
+ * The handle owns two CUDA events (created by its first CE-mode call, for the
+ * fork to and join from the side stream); tdg_symm_free destroys them.
  * Returns TDG_OK and *out, or TDG_ERR_INVALID / TDG_ERR_NOMEM / TDG_ERR_CUDA.
  */
 TDG_API int tdg_symm_alloc(void *dev_base, size_t bytes, int world, size_t region_bytes,
