@@ -14,9 +14,14 @@ dispatch+combine bandwidth, the roofline of the dominant kernel and the CPU
 oracle's rate on a bounded sample.
 
 --impl reference times the CPU oracle on a bounded sample of the same
-workload each step (the reference arm for this path is the oracle).
-Under torchrun (N > 1) every rank runs its own replica; rank 0 prints the
-JSON line with the max-over-ranks time.
+workload each step (the reference arm for this path is the oracle); under
+torchrun rank 0 alone runs it.
+
+The path runs on one GPU: its W ranks are logical regions of one device, and
+its GEMMs share B slices between the CTA pairs of a cluster by TMA multicast,
+which is meant for one GPU's own memory.  With --gpus N > 1 (or under a
+torchrun of several processes) rank 0 prints one line with an "unavailable"
+key and every rank exits 0 without touching a GPU.
 """
 from __future__ import annotations
 
@@ -358,22 +363,6 @@ class MLP:
             st = s.status()
             if st["code"] != 0:
                 raise RuntimeError(f"device fault during the bench: {st}")
-
-
-def max_over_ranks(x, pg, torch, device):
-    """The slowest rank's value: the job's steps end when its last rank's do.
-    `pg` is torch.distributed (or None for one process)."""
-    if not pg:
-        return x
-    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
-    pg.all_reduce(t, op=pg.ReduceOp.MAX)
-    return float(t.item())
-
-
-def job_tflops(world, flop_per_rank_step, steps, max_total_ms):
-    """Whole-job throughput: every rank's work (weak scaling: the same work
-    on each rank) over the slowest rank's time."""
-    return world * flop_per_rank_step * steps / (max_total_ms * 1e-3) / 1e12
 
 
 def timed_steps(torch, fns, steps, warmup, flush):
@@ -814,6 +803,18 @@ def leg_flash(torch, tdg, synth, args, flush, pk):
     return extras["flash_decode"]
 
 
+def multi_gpu_unavailable(args, rank, n):
+    """--gpus N > 1: this path has no multi-GPU form; rank 0 says so in one
+    line, and nothing touches a GPU."""
+    if rank != 0:
+        return
+    print(json.dumps({"impl": "tdg", "metric": "AG-GEMM+GEMM-RS TFLOP/s (qwen32b_mlp_tp8)", "n_gpus": n,
+                      "steps": args.steps, "warmup": args.warmup,
+                      "unavailable": "the path runs on one GPU (W logical ranks in one device allocation; "
+                                     "its GEMMs multicast B slices inside a cluster, from this GPU's own "
+                                     "memory), so there is no run on several GPUs"}), flush=True)
+
+
 def main():
     args = parse()
     rank, world, local = dist_env()
@@ -825,14 +826,12 @@ def main():
     if args.impl == "reference":
         run_reference(args, rank)
         return
+    if world > 1 or args.gpus > 1:
+        multi_gpu_unavailable(args, rank, max(world, args.gpus))
+        return
     import torch
     from tile_centric_comm_gb300 import synth, tdg
     torch.cuda.set_device(local)
-    pg = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-        pg = dist
     sms, supported = tdg.device_info()
     if not supported:
         raise SystemExit("libtdg kernels need an sm_103 device")
@@ -859,7 +858,7 @@ def main():
         if rank == 0:
             key = "serial" if "ce_tflops" not in res else "ce"
             print(json.dumps({"metric": f"all-ranks AG-GEMM TFLOP/s ({key})", "value": res[f"{key}_tflops"],
-                              "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                              "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
                               "higher_is_better": True, "dtype": "bf16",
                               "roofline": {"bound": "tensor", "achieved": res[f"{key}_tflops"], "peak": pk["bf16"],
                                            "unit": "TFLOP/s", "frac": res[f"{key}_tflops"] / pk["bf16"]},
@@ -871,7 +870,7 @@ def main():
             res = leg(torch, tdg, synth, args, flush, pk)
         if rank == 0:
             print(json.dumps({"metric": f"{args.only} GB/s", "value": res["gbs"], "unit": "GB/s",
-                              "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                              "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
                               "higher_is_better": True, "dtype": "bf16" if args.only != "ring" else "f32",
                               "roofline": {"bound": "hbm", "achieved": res["gbs"], "peak": pk["hbm"],
                                            "unit": "GB/s", "frac": res["frac_of_hbm"]},
@@ -890,9 +889,6 @@ def main():
 
     def barrier():
         torch.cuda.synchronize()
-        if pg:
-            pg.barrier()
-        torch.cuda.synchronize()
 
     barrier()
     with Clocks(local) as clk:
@@ -902,11 +898,10 @@ def main():
     clocks = clk.summary()
     step_ms = [sum(p[i] for p in parts) for i in range(args.steps)]
     total_ms = sum(step_ms)
-    total_ms = max_over_ranks(total_ms, pg, torch, "cuda")
     ms_per_step = total_ms / args.steps
     ag_flop = 2 * AG["W"] * AG["Ms"] * AG["K"] * AG["N"]
     flop = (ag_flop if args.only != "rs" else 0) + (RS_FLOP if args.only != "ag" else 0)
-    value = job_tflops(world, flop, args.steps, total_ms)
+    value = flop * args.steps / (total_ms * 1e-3) / 1e12
     launches = 2 * args.steps if not args.only else args.steps
     ag_ms = statistics.mean(parts[0]) if args.only != "rs" else None
     rs_ms = statistics.mean(parts[-1]) if args.only != "ag" else None
@@ -958,16 +953,14 @@ def main():
         e_w = mlp.e2e_pipelined([mlp, mlp2], args.steps, args.warmup, weights=False)
         mlp2.check_status()
         del mlp2
-        # whole job, as for `value`: every rank's steps over the slowest rank's time
-        e_ms, e_one, e_w = (max_over_ranks(x, pg, torch, "cuda") for x in (e_ms, e_one, e_w))
-        e2e = {"value": world * STEP_FLOP / e_ms / 1e9, "unit": "TFLOP/s",
-               "h2d_bytes_per_step": world * mlp.h2d_bytes, "d2h_bytes_per_step": world * mlp.d2h_bytes,
+        e2e = {"value": STEP_FLOP / e_ms / 1e9, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": mlp.h2d_bytes, "d2h_bytes_per_step": mlp.d2h_bytes,
                "ms_per_step": e_ms,
                "how": "consecutive steps overlapped over two device buffer sets (upload, compute and "
                       "download streams); every step copies all its inputs H2D and both outputs D2H",
-               "one_step_at_a_time": {"value": world * STEP_FLOP / e_one / 1e9, "ms_per_step": e_one},
-               "weights_resident": {"value": world * STEP_FLOP / e_w / 1e9, "ms_per_step": e_w,
-                                    "h2d_bytes_per_step": world * mlp.h2d_act_bytes,
+               "one_step_at_a_time": {"value": STEP_FLOP / e_one / 1e9, "ms_per_step": e_one},
+               "weights_resident": {"value": STEP_FLOP / e_w / 1e9, "ms_per_step": e_w,
+                                    "h2d_bytes_per_step": mlp.h2d_act_bytes,
                                     "what": "activations (AG shards, RS A_r) H2D every step, outputs D2H; "
                                             "B and B_r uploaded once before the timed steps"}}
         mlp.check_status()
@@ -1018,19 +1011,16 @@ def main():
                 "peak_kind": f"bf16 dense burst, {pk['src']}",
                 "frac_of_sustained": achieved / pk["bf16_sus"]}
     line = {"metric": "AG-GEMM+GEMM-RS TFLOP/s (qwen32b_mlp_tp8)", "value": value, "unit": "TFLOP/s",
-            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
             "config": {"workload": WORKLOAD, "l2": "flushed before every step (256 MB write)",
                        "ag_mode": args.mode, "rs_mode": "sm (push + last-arriver reduction)",
                        "producers": (args.producers or 16) if args.mode == "sm" else None, "sm_count": sms,
-                       "parallelism": f"replicas x{world}, 8 logical ranks each"},
+                       "parallelism": "one GPU, 8 logical ranks (symmetric regions of one allocation)"},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
             "clocks": clocks, "parts": extras}
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    if pg:
-        pg.destroy_process_group()
+    print(json.dumps(line), flush=True)
 
 
 if __name__ == "__main__":
