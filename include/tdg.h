@@ -246,10 +246,10 @@ TDG_API int tdg_ag_gemm(tdg_symm *h, const tdg_ag_gemm_args *args, void *stream,
  * first, read in place when Ms is a whole number of tiles) and waits (bounded)
  * on the flags of the rows it reads; the W x W shard copies run on
  * `side_stream` (cudaMemcpyAsync, then a stream-ordered flag write), rank by
- * rank.  The GEMM is queued first, so that the tiles of each rank's own
- * shard start at once; its flag waits are bounded by timeout_ns, within
- * which this call queues the copies behind it.  SERIAL mode: the copies,
- * then the GEMM, on `stream`.
+ * rank.  The copies and flag writes are queued before the GEMM, so the call
+ * completes even when the two streams run one after the other; the GEMM does
+ * not wait behind the copies (the tiles of each rank's own shard start at
+ * once).  SERIAL mode: the copies, then the GEMM, on `stream`.
  * Requirements: 1 <= world <= 64; K % 8 == 0; N % 8 == 0; c_f32 0 or 1; offsets 16-byte
  * aligned; every buffer inside its region (else TDG_ERR_NOMEM); the gathered
  * buffers and C_r overlapping no other buffer (else TDG_ERR_INVALID);
@@ -464,11 +464,15 @@ TDG_API int tdg_moe_dispatch_combine(tdg_symm *h, const tdg_moe_args *args, void
  * library, TDG_MOE_STATIC_WORKSPACE_BYTES (2 MiB) in size, which every GPU that
  * loads the library keeps until the process exits.  Inputs and outputs are
  * still the caller's.  Nothing is allocated or freed by this call.
- *   - Returns TDG_ERR_NOMEM, launching nothing, when the routing phase is
- *     requested and tdg_moe_workspace_bytes(world, T, E) exceeds 2 MiB
- *     (that is, when W * ceil(T/64) * E > 262144).
+ *   - Arguments are checked first, exactly as tdg_moe_dispatch_combine does
+ *     (the same TDG_ERR_INVALID / TDG_ERR_NOMEM codes).  Then it returns
+ *     TDG_ERR_NOMEM, launching nothing, when the routing phase is requested
+ *     and tdg_moe_workspace_bytes(world, T, E) exceeds 2 MiB (that is, when
+ *     W * ceil(T/64) * E > 262144).
  *   - The first call on a device looks up the array's device address (with
- *     that device current); make that first call before any stream capture.
+ *     that device current) and keeps it for that device's context; a context
+ *     created anew (after cudaDeviceReset) looks it up again on its first
+ *     call.  Make that first call before any stream capture.
  *   - All calls on one device share the array and it keeps the last call's
  *     contents; nothing in it needs to start at zero (every entry a call reads
  *     is written earlier in the same call).  Calls that overlap on the GPU

@@ -368,15 +368,18 @@ extern "C" int tdg_ag_gemm_all_ranks(tdg_symm *h, const tdg_ag_gemm_all_args *a,
         e = cudaStreamWaitEvent(side, ev0, 0);
     if (e != cudaSuccess)
         rc = cuda_err(e, "ag all events");
-    // the GEMM first: its own shards need no copy, and its flag waits are
-    // bounded while the host is still queueing the W x W copies behind it
+    // The copies and their flag writes are queued before the GEMM that waits
+    // on them (the producer transfers, then signals; the consumer waits), so
+    // the call completes whatever order the two streams run in -- one after
+    // the other included.  The side stream starts only after ev0, so the GEMM
+    // is not behind the copies: the tiles of each rank's own shard start at once.
+    if (rc == TDG_OK)
+        rc = copies(side, true);
     if (rc == TDG_OK) {
         p.wait_flags = 1;
         rc = cuda_err(launch(fn, dim3(grid), dim3(gm::NUM_THREADS), gm::SMEM_BYTES, s, args, false, cl),
                       "ag all gemm launch");
     }
-    if (rc == TDG_OK)
-        rc = copies(side, true);
     // the call completes on the main stream only when the side stream has too
     e = cudaEventRecord(ev1, side);
     if (e == cudaSuccess)

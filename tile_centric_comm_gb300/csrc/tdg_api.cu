@@ -138,6 +138,16 @@ cudaError_t set_smem(const void *fn, int bytes)
     return e;
 }
 
+void *current_context()
+{
+    typedef CUresult (*PFN_ctxGetCurrent_t)(CUcontext *);
+    static PFN_ctxGetCurrent_t fn = reinterpret_cast<PFN_ctxGetCurrent_t>(driver_fn("cuCtxGetCurrent"));
+    CUcontext c = nullptr;
+    if (!fn || fn(&c) != CUDA_SUCCESS)
+        return nullptr;
+    return c;
+}
+
 int check_device(const tdg_symm *h)
 {
     int dev = -1;

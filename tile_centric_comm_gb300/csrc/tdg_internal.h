@@ -84,6 +84,10 @@ bool stream_write_u32(cudaStream_t s, uint32_t *dev_addr, uint32_t value);
 // several host threads.
 cudaError_t set_smem(const void *fn, int bytes);
 
+// The calling thread's current CUDA context (cuCtxGetCurrent through the
+// driver entry point), or nullptr when there is none or it cannot be read.
+void *current_context();
+
 // TDG_OK when the current device is the one the heap was allocated on (its
 // context is then current in the calling thread), TDG_ERR_INVALID when it is
 // another, TDG_ERR_CUDA when it cannot be read or made current.

@@ -343,12 +343,12 @@ extern "C" size_t tdg_moe_workspace_bytes(int world, int64_t T, int E)
     return (size_t)2 * world * (nc > 0 ? nc : 1) * E * sizeof(int32_t);
 }
 
-extern "C" int tdg_moe_dispatch_combine(tdg_symm *h, const tdg_moe_args *a, void *stream)
+namespace {
+
+// Every argument check of tdg_moe_dispatch_combine except the workspace's:
+// TDG_OK when the call may go ahead (T == 0 included).
+int moe_validate(const tdg_symm *h, const tdg_moe_args *a)
 {
-    if (!h || !a)
-        return TDG_ERR_INVALID;
-    if (const int drc = check_device(h))
-        return drc;
     const int W = a->world, E = a->E, k = a->k;
     const int64_t T = a->T, H = a->H;
     if (W != h->world || T < 0 || H < 0 || E <= 0 || E > moe::MAX_E || E % W || k < 1 || k > 32 || k > E)
@@ -378,6 +378,26 @@ extern "C" int tdg_moe_dispatch_combine(tdg_symm *h, const tdg_moe_args *a, void
         return TDG_ERR_INVALID;
     if ((a->row_src || a->row_tok || a->row_k) && !(a->row_src && a->row_tok && a->row_k))
         return TDG_ERR_INVALID;
+    return TDG_OK;
+}
+
+} // namespace
+
+extern "C" int tdg_moe_dispatch_combine(tdg_symm *h, const tdg_moe_args *a, void *stream)
+{
+    if (!h || !a)
+        return TDG_ERR_INVALID;
+    if (const int drc = check_device(h))
+        return drc;
+    if (const int vrc = moe_validate(h, a))
+        return vrc;
+    const int W = a->world, E = a->E, k = a->k;
+    const int64_t T = a->T, H = a->H;
+    if (T == 0)
+        return TDG_OK;
+    const uint64_t R = h->region_bytes;
+    const bool route = a->phases & TDG_MOE_ROUTE, disp = a->phases & TDG_MOE_DISPATCH,
+               comb = a->phases & TDG_MOE_COMBINE;
     const int nc = (int)((T + moe::TC - 1) / moe::TC);
     if (route && (!a->workspace || a->workspace_bytes < tdg_moe_workspace_bytes(W, T, E)))
         return TDG_ERR_NOMEM;
@@ -461,7 +481,9 @@ extern "C" int tdg_moe_dispatch_combine(tdg_symm *h, const tdg_moe_args *a, void
 // of this file instead of a caller-provided workspace, for callers that cannot
 // allocate device memory when they call.  Host code cannot pass the array's
 // name to a kernel (on the host it is only a stand-in symbol); its device
-// address is looked up once per device with cudaGetSymbolAddress.
+// address is looked up with cudaGetSymbolAddress, with the device current,
+// the first time a context uses it, and kept per (device, context): a context
+// built again after a device reset looks it up afresh.
 // ---------------------------------------------------------------------------
 #include <mutex>
 
@@ -469,8 +491,14 @@ namespace {
 
 static __device__ __align__(256) int32_t g_moe_static_ws[TDG_MOE_STATIC_WORKSPACE_BYTES / sizeof(int32_t)];
 
+struct StaticWs {
+    int dev;
+    void *ctx;
+    void *ptr;
+};
 std::mutex g_static_ws_mu;
-void *g_static_ws_ptr[64] = {};
+StaticWs g_static_ws[64] = {};
+int g_static_ws_n = 0;
 
 } // namespace
 
@@ -480,6 +508,12 @@ extern "C" int tdg_moe_dispatch_combine_noalloc(tdg_symm *h, const tdg_moe_args 
         return TDG_ERR_INVALID;
     if (const int drc = check_device(h))
         return drc;
+    // the arguments first, so that a bad argument gives the regular entry
+    // point's code whatever workspace it would need
+    if (const int vrc = moe_validate(h, a))
+        return vrc;
+    if (a->T == 0)
+        return TDG_OK;
     if ((a->phases & TDG_MOE_ROUTE) &&
         tdg_moe_workspace_bytes(a->world, a->T, a->E) > (size_t)TDG_MOE_STATIC_WORKSPACE_BYTES) {
         if (getenv("TDG_LOG"))
@@ -487,23 +521,25 @@ extern "C" int tdg_moe_dispatch_combine_noalloc(tdg_symm *h, const tdg_moe_args 
                     tdg_moe_workspace_bytes(a->world, a->T, a->E), TDG_MOE_STATIC_WORKSPACE_BYTES);
         return TDG_ERR_NOMEM;
     }
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess)
-        return cuda_err(e, "moe noalloc device");
-    if (dev < 0 || dev >= 64)
-        return TDG_ERR_UNSUPPORTED;
+    void *ctx = current_context();
+    if (!ctx)
+        return TDG_ERR_CUDA;
     void *ws = nullptr;
     {
         std::lock_guard<std::mutex> lock(g_static_ws_mu);
-        if (!g_static_ws_ptr[dev]) {
+        for (int i = 0; i < g_static_ws_n; ++i)
+            if (g_static_ws[i].dev == h->device && g_static_ws[i].ctx == ctx)
+                ws = g_static_ws[i].ptr;
+        if (!ws) {
             void *p = nullptr;
-            e = cudaGetSymbolAddress(&p, g_moe_static_ws);
+            cudaError_t e = cudaGetSymbolAddress(&p, g_moe_static_ws);
             if (e != cudaSuccess || !p)
                 return cuda_err(e != cudaSuccess ? e : cudaErrorInvalidSymbol, "moe noalloc symbol");
-            g_static_ws_ptr[dev] = p;
+            // one entry per (device, context); a full table reuses its oldest slot
+            StaticWs &slot = g_static_ws[g_static_ws_n < 64 ? g_static_ws_n++ : 0];
+            slot = StaticWs{h->device, ctx, p};
+            ws = p;
         }
-        ws = g_static_ws_ptr[dev];
     }
     tdg_moe_args b = *a;
     b.workspace = ws;
