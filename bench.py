@@ -534,8 +534,9 @@ def leg_ag_all(torch, tdg, args, flush, pk):
         sym.view(r, a_off, (Ms, K), torch.bfloat16).copy_(torch.randn(Ms, K, device="cuda", generator=g))
         sym.view(r, b_off, (K, N), torch.bfloat16).copy_(torch.randn(K, N, device="cuda", generator=g) * 0.02)
     side = torch.cuda.Stream()
-    call = lambda mode: (lambda: tdg.ag_gemm_all_ranks(sym, Ms, K, N, a_off, g_off, b_off, c_off, mode=mode,
-                                                       side_stream=side if mode == "ce" else None))
+    call = lambda mode, push=False: (lambda: tdg.ag_gemm_all_ranks(sym, Ms, K, N, a_off, g_off, b_off, c_off,
+                                                                   mode=mode, push=push,
+                                                                   side_stream=side if mode == "ce" else None))
     flop = W * AG_FLOP
     res = {"workload": "AG-GEMM Qwen-32B up for all 8 logical ranks in one call (8 x 8192x3200x5120, "
                        "56 remote shard copies)",
@@ -546,12 +547,14 @@ def leg_ag_all(torch, tdg, args, flush, pk):
         res.update({"serial_ms": ms, "serial_tflops": flop / ms / 1e9,
                     "serial_frac_of_bf16_peak": flop / ms / 1e9 / pk["bf16"]})
     else:
-        iv = interleaved_steps(torch, {"ce": [call("ce")], "serial": [call("serial")]}, 3,
-                               max(4, args.steps // 5), flush)
+        iv = interleaved_steps(torch, {"ce": [call("ce")], "serial": [call("serial")],
+                                       "ce_push": [call("ce", True)]}, 3, max(4, args.steps // 5), flush)
         res.update({"ce_ms": iv["ce"][0], "ce_tflops": flop / iv["ce"][0] / 1e9,
                     "ce_frac_of_bf16_peak": flop / iv["ce"][0] / 1e9 / pk["bf16"],
                     "serial_ms": iv["serial"][0], "serial_tflops": flop / iv["serial"][0] / 1e9,
-                    "ce_overlap_gain_vs_serial": iv["serial"][0] / iv["ce"][0]})
+                    "ce_overlap_gain_vs_serial": iv["serial"][0] / iv["ce"][0],
+                    "ce_push_ms": iv["ce_push"][0], "ce_push_tflops": flop / iv["ce_push"][0] / 1e9,
+                    "ce_push_overlap_gain_vs_serial": iv["serial"][0] / iv["ce_push"][0]})
         res["note"] += "; modes in 3 interleaved rounds"
     st = sym.status()
     if st["code"] != 0:
@@ -734,10 +737,12 @@ def leg_ring(torch, tdg, synth, args, flush, pk):
     return extras["ring_allreduce"]
 
 
-def leg_ag_config(torch, tdg, synth, args, flush, pk, W, Ms, K, N, dist, workload, modes=("ce", "sm")):
-    """One AllGather+GEMM config on its own: each overlapped mode against the
-    serial twin (copy launch, then GEMM launch), TFLOP/s and fraction of the
-    measured bf16 peak."""
+def leg_ag_config(torch, tdg, synth, args, flush, pk, W, Ms, K, N, dist, workload, modes=("ce", "sm"),
+                  variants=None):
+    """One AllGather+GEMM config on its own: each overlapped schedule against
+    the serial twin (copy launch, then GEMM launch), TFLOP/s and fraction of
+    the measured bf16 peak.  `variants` maps a name to (mode, extra args);
+    by default one variant per mode."""
     inp = synth.ag_inputs(W, Ms, K, N, dist, seed=0)
     g_off = _align(Ms * K * 2)
     ll_off = _align(g_off + W * Ms * K * 2)    # LL words: 4 bytes per element
@@ -750,28 +755,139 @@ def leg_ag_config(torch, tdg, synth, args, flush, pk, W, Ms, K, N, dist, workloa
     del inp
     side = torch.cuda.Stream()
     flop = 2 * W * Ms * K * N
+    if variants is None:
+        variants = {m: (m, {}) for m in modes}
+    variants = dict({"serial": ("serial", {})}, **variants)
 
-    def call(mode):
+    def call(mode, kw):
         return lambda: tdg.ag_gemm(sym, 0, Ms, K, N, 0, g_off, B, C, mode=mode, ll_off=ll_off,
-                                   side_stream=side if mode == "ce" else None)
-    res = {"workload": workload, "note": "modes timed in 5 interleaved rounds (same clock state)"}
-    for mode in ("serial",) + tuple(modes):   # warm every mode once
-        timed_steps(torch, [call(mode)], 1, args.warmup, flush)
-    iv = interleaved_steps(torch, {m: [call(m)] for m in ("serial",) + tuple(modes)}, 5,
+                                   side_stream=side if mode == "ce" else None, **kw)
+    res = {"workload": workload, "note": f"schedules timed in 5 interleaved rounds (same clock state)"}
+    for name, (mode, kw) in variants.items():   # warm every schedule once
+        timed_steps(torch, [call(mode, kw)], 1, args.warmup, flush)
+    iv = interleaved_steps(torch, {n: [call(m, kw)] for n, (m, kw) in variants.items()}, 5,
                            max(4, args.steps // 5), flush)
-    times = {m: v[0] for m, v in iv.items()}
-    for mode in ("serial",) + tuple(modes):
-        res[f"{mode}_ms"] = times[mode]
-        res[f"{mode}_tflops"] = flop / times[mode] / 1e9
-        res[f"{mode}_frac_of_bf16_peak"] = flop / times[mode] / 1e9 / pk["bf16"]
-        if mode != "serial":
-            res[f"{mode}_overlap_gain_vs_serial"] = times["serial"] / times[mode]
+    times = {n: v[0] for n, v in iv.items()}
+    for name in variants:
+        res[f"{name}_ms"] = times[name]
+        res[f"{name}_tflops"] = flop / times[name] / 1e9
+        res[f"{name}_frac_of_bf16_peak"] = flop / times[name] / 1e9 / pk["bf16"]
+        if name != "serial":
+            res[f"{name}_overlap_gain_vs_serial"] = times["serial"] / times[name]
     st = sym.status()
     if st["code"] != 0:
         raise RuntimeError(f"device fault in {workload}: {st}")
     del sym, B, C
     torch.cuda.empty_cache()
     return res
+
+
+# push and pull, copy engine and producer CTAs, for the AG configs
+AG_SCHEDULES = {"ce": ("ce", {}), "ce_push": ("ce", dict(push=True)), "sm": ("sm", {}),
+                "sm_push": ("sm", dict(push=True))}
+
+
+def leg_ag_copy(torch, tdg, args, flush, pk):
+    """The AllGather of the Qwen-32B up-projection alone (N = 0: gathered
+    buffer and flags, no GEMM): producer CTAs (the SERIAL copy launch on a
+    given number of CTAs) and the copy engine.  Bytes moved = the 8 shards
+    (84 MB), each read once and written once."""
+    W, Ms, K = AG["W"], AG["Ms"], AG["K"]
+    g_off = _align(Ms * K * 2)
+    sym = tdg.Symm(W, _align(g_off + W * Ms * K * 2 + 1024), 65536)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(0)
+    for r in range(W):
+        sym.view(r, 0, (Ms, K), torch.bfloat16).copy_(torch.randn(Ms, K, device="cuda", generator=g))
+    side = torch.cuda.Stream()
+    moved = W * Ms * K * 2
+    res = {"workload": "AllGather of 8 shards of 1024x5120 bf16 (84 MB moved; read + write 168 MB), no GEMM",
+           "bytes_moved": moved}
+    for n in (1, 16, 0):
+        ms = statistics.mean(timed_steps(torch, [lambda: tdg.ag_gemm(sym, 0, Ms, K, 0, 0, g_off, None, None,
+                                                                     mode="serial", producers=n)],
+                                         max(4, args.steps // 5), args.warmup, flush)[0])
+        ctas = n or sms_of(torch)
+        res[f"producers_{n or 'all'}_gbs"] = moved / ms / 1e6
+        res[f"producers_{n or 'all'}_gbs_per_cta"] = moved / ms / 1e6 / ctas
+        res[f"producers_{n or 'all'}_rw_frac_of_hbm"] = 2 * moved / ms / 1e6 / pk["hbm"]
+    ms = statistics.mean(timed_steps(torch, [lambda: tdg.ag_gemm(sym, 0, Ms, K, 0, 0, g_off, None, None,
+                                                                 mode="ce", side_stream=side)],
+                                     max(4, args.steps // 5), args.warmup, flush)[0])
+    res["copy_engine_gbs"] = moved / ms / 1e6
+    res["note"] = ("an SM writes to memory at about 63 GB/s at most (TMA bulk or plain stores), so one producer "
+                   "CTA moves about 50 GB/s")
+    st = sym.status()
+    if st["code"] != 0:
+        raise RuntimeError(f"device fault in the AllGather alone: {st}")
+    del sym
+    torch.cuda.empty_cache()
+    return res
+
+
+def sms_of(torch):
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
+def leg_autotune(torch, tdg, args, flush, pk):
+    """The distributed autotuner on the step's two operations (one process:
+    no ranks to agree with): every candidate schedule timed through the C ABI,
+    the best one reported beside the library's default."""
+    from tile_centric_comm_gb300 import autotune
+    out = {}
+    W, Ms, K, N = AG["W"], AG["Ms"], AG["K"], AG["N"]
+    g_off = _align(Ms * K * 2)
+    sym = tdg.Symm(W, _align(g_off + W * Ms * K * 2 + 1024), 65536)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(0)
+    for r in range(W):
+        sym.view(r, 0, (Ms, K), torch.bfloat16).copy_(torch.randn(Ms, K, device="cuda", generator=g))
+    B = (torch.randn(K, N, device="cuda", generator=g) * 0.02).to(torch.bfloat16)
+    C = torch.empty((W * Ms, N), dtype=torch.bfloat16, device="cuda")
+    side = torch.cuda.Stream()
+    cands = autotune.ag_candidates(W * Ms, Ms, producers=(0,), source_orders=(0,))
+
+    def run(cfg):
+        tdg.ag_gemm(sym, 0, Ms, K, N, 0, g_off, B, C, side_stream=side, **cfg)
+    best, table = autotune.tune(("ag", W, Ms, K, N), cands, run, warmup=2, iters=7, flush=flush.zero_,
+                                use_cache=False)
+    # the first candidate is the library's default schedule in CE mode (pull,
+    # the default cluster shape and stage count)
+    flop = 2 * W * Ms * K * N
+    out["ag_qwen32b_up"] = {"candidates": len(cands), "best": best,
+                            "best_tflops": flop / min(r["ms"] for r in table) / 1e9,
+                            "default": table[0]["cfg"], "default_tflops": flop / table[0]["ms"] / 1e9,
+                            "table": [dict(r["cfg"], tflops=round(flop / r["ms"] / 1e9, 1)) for r in table]}
+    del sym, B, C
+    torch.cuda.empty_cache()
+    W, M, K, N = RS["W"], RS["M"], RS["K"], RS["N"]
+    a_off, b_off = 0, _align(M * K * 2)
+    s_off = _align(b_off + K * N * 2)
+    o_off = _align(s_off + tdg.gemm_rs_stage_bytes(W, M, N))
+    sym = tdg.Symm(W, _align(o_off + (M // W) * N * 2 + 1024), 65536)
+    for r in range(W):
+        sym.view(r, a_off, (M, K), torch.bfloat16).copy_(torch.randn(M, K, device="cuda", generator=g))
+        sym.view(r, b_off, (K, N), torch.bfloat16).copy_(torch.randn(K, N, device="cuda", generator=g) * 0.02)
+    rc = autotune.rs_candidates(W, M // W, orders=(0,))
+
+    def run_rs(cfg):
+        tdg.gemm_rs(sym, M, K, N, a_off, b_off, s_off, o_off, **cfg)
+    best, table = autotune.tune(("rs", W, M, K, N), rc, run_rs, warmup=2, iters=5, flush=flush.zero_,
+                                use_cache=False)
+    dflt = [r["ms"] for r in table if r["cfg"] == dict(owner_block=2, order=0, cluster=4, stages=0)]
+    out["gemm_rs_qwen32b_down"] = {"candidates": len(rc), "best": best,
+                                   "best_tflops": RS_FLOP / min(r["ms"] for r in table) / 1e9,
+                                   "default": dict(owner_block=2, order=0, cluster=4, stages=0),
+                                   "default_tflops": RS_FLOP / dflt[0] / 1e9 if dflt else None,
+                                   "table": [dict(r["cfg"], tflops=round(RS_FLOP / r["ms"] / 1e9, 1))
+                                             for r in table]}
+    st = sym.status()
+    if st["code"] != 0:
+        raise RuntimeError(f"device fault in the autotune leg: {st}")
+    del sym
+    torch.cuda.empty_cache()
+    out["note"] = "candidates timed one after another (median of 7 / 5 calls, L2 flushed before each)"
+    return out
 
 
 def leg_flash(torch, tdg, synth, args, flush, pk):
@@ -979,9 +1095,15 @@ def main():
             "ag_shape_tflops": AG_FLOP / l_ag / 1e9, "rs_shapes_tflops": RS_FLOP / l_rs / 1e9}
         del mlp, a_cat, b_rs, a_rs, c_rs
         torch.cuda.empty_cache()
+        extras["ag_qwen32b_up_schedules"] = leg_ag_config(
+            torch, tdg, synth, args, flush, pk, 8, 1024, 5120, 3200, "normal",
+            "AG-GEMM Qwen-32B up: W=8, A_r 1024x5120, B 5120x3200, pull and push", variants=AG_SCHEDULES)
         extras["ag_llama70b_gateup"] = leg_ag_config(
             torch, tdg, synth, args, flush, pk, 8, 2048, 8192, 7168, "normal",
-            "AG-GEMM Llama-3-70B gate+up: W=8, A_r 2048x8192, B 8192x7168")
+            "AG-GEMM Llama-3-70B gate+up: W=8, A_r 2048x8192, B 8192x7168, pull and push",
+            variants=AG_SCHEDULES)
+        extras["ag_copy_alone_qwen32b"] = leg_ag_copy(torch, tdg, args, flush, pk)
+        extras["autotune"] = leg_autotune(torch, tdg, args, flush, pk)
         extras["ag_tiny"] = leg_ag_config(
             torch, tdg, synth, args, flush, pk, 2, 64, 256, 128, "int2",
             "AG-GEMM tiny: W=2, A_r 64x256, B 256x128, integers (latency bound)", modes=("ce", "sm", "ll"))
@@ -1016,7 +1138,8 @@ def main():
             "data": "synthetic",
             "config": {"workload": WORKLOAD, "l2": "flushed before every step (256 MB write)",
                        "ag_mode": args.mode, "rs_mode": "sm (push + last-arriver reduction)",
-                       "producers": (args.producers or 16) if args.mode == "sm" else None, "sm_count": sms,
+                       "producers": (args.producers or "library default") if args.mode == "sm" else None,
+                       "sm_count": sms,
                        "parallelism": "one GPU, 8 logical ranks (symmetric regions of one allocation)"},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
             "clocks": clocks, "parts": extras}

@@ -32,22 +32,13 @@
  *     device is current returns TDG_ERR_INVALID.  Any host thread may call:
  *     the call makes that device's context current in the calling thread.
  *
- * Environment variables (read at each call; each selects among schedules of
- * the same computation, and the tests check every setting against the oracle):
- *   TDG_PAIR=0            GEMMs on one CTA per 128-row tile instead of CTA
- *                         pairs (cta_group::2, 256-row tiles).
- *   TDG_QUAD=0            CTA pairs alone instead of clusters of two pairs
- *                         that share each B slice by TMA multicast.
- *   TDG_SPLIT_TAIL=1      AG-GEMM: split the tiles of the last, partial wave
- *                         into 128-column halves.
- *   TDG_AG_PROD_ROUNDS=n  AG-GEMM SM mode: the producer clusters take n
- *                         rounds of GEMM tiles after their copies (-1: none);
- *                         unset, the split is estimated on the host.
- *   TDG_RS_ORDER=1        GEMM-RS: rank-fastest tile order instead of owner
- *                         blocks.
- *   TDG_RS_RED_ROWS=r     GEMM-RS: rows of an owed reduction worked off per
- *                         tile (4, 8, 16 or 32; default 32 for bf16 partials,
- *                         8 for fp32).
+ * Schedules.  Several args fields choose among schedules of the same
+ * computation (GEMM cluster shape, ring stages, tile order, producer shape,
+ * push or pull); 0 always means the library's default for the shape, and the
+ * tests check every setting against the oracle.  They are per call, so two
+ * threads or two shapes in one process may use different schedules.
+ *
+ * Environment variable:
  *   TDG_LOG=1             print host-side failures (tensor-map encoding,
  *                         MoE workspace) to stderr.
  */
@@ -176,13 +167,15 @@ TDG_API int tdg_device_info(int *sm_count, int *supported);
  *
  * Shard s (Ms x K bf16) sits at region(s) + a_off.  The AllGather writes the
  * gathered M x K matrix (M = W*Ms) into region(rank) + g_off, shard s at rows
- * [s*Ms, (s+1)*Ms) -- rank `rank` pulls every shard, its own included.
+ * [s*Ms, (s+1)*Ms) -- every shard reaches it, its own included (pulled by
+ * rank `rank`, or in push mode delivered by the senders in their order).
  * Producers signal per group of `signal_rows` gathered rows (flag word
  * g = row / signal_rows of rank `rank`'s flags, set to the call's epoch with
  * release semantics); the GEMM waits on every group its A tile needs
  * (bounded acquire spin), so it computes on tiles that have arrived while
  * others are still in flight.  Tiles are visited in the rank-swizzled order
- * pid_m = (pid_m + rank*Ms/BM) % m_tiles ("Triton-distributed 语义", 线程块交织)
+ * pid_m = (pid_m + rank*Ms/BM) % m_tiles ("Triton-distributed 语义", 线程块交织;
+ * mirrored in push mode, so the tiles follow the shards' arrival order)
  * when swizzle != 0; when Ms is a multiple of BM the local shard is read in
  * place, with no wait.
  *
@@ -197,8 +190,9 @@ TDG_API int tdg_device_info(int *sm_count, int *supported);
  * neither the shard nor the gathered buffer; SM / LL producer CTAs fewer than
  * the GEMM's grid (TDG_ERR_INVALID otherwise).  g_off + M*K*2, a_off + Ms*K*2
  * (and ll_off + M*K*4) <= region_bytes and M / signal_rows <=
- * signals_per_rank (TDG_ERR_NOMEM otherwise).  M == 0 or N == 0 is a no-op;
- * K == 0 writes C = 0.
+ * signals_per_rank (TDG_ERR_NOMEM otherwise).  M == 0 is a no-op; N == 0
+ * runs the AllGather alone (the gathered buffer and the flags, in the given
+ * mode; B and C may be NULL); K == 0 writes C = 0.
  */
 typedef struct {
     int world, rank;
@@ -208,7 +202,10 @@ typedef struct {
     void *C;
     int b_layout;        /* TDG_B_KN or TDG_B_NK                            */
     int mode;            /* TDG_MODE_SM / CE / LL / SERIAL                  */
-    int producers;       /* producer CTAs in SM / LL mode (0 = default)     */
+    int producers;       /* producer CTAs in SM / LL mode (0 = default: SM
+                            mode enough to copy the shards within the GEMM's
+                            time at about 50 GB/s each, 4..32; LL 8 senders),
+                            copy CTAs of the SERIAL copy launch (0 = every SM) */
     int64_t signal_rows; /* rows per signal; 0 = BM if Ms % BM == 0, else Ms */
     int swizzle;         /* 1 = rank-swizzled tile order, 0 = linear        */
     uint64_t timeout_ns; /* bound of every device wait; 0 = 2 s             */
@@ -223,6 +220,32 @@ typedef struct {
                             published NVSwitch swizzle); 1: all sources at once,
                             round robin over sources (their full-mesh order) */
     int c_f32;           /* 1: C is float32; 0: bf16                         */
+    /* schedule (0 = default for the shape) */
+    int cluster;         /* CTAs per GEMM cluster: 1 (128-row tiles), 2 (a CTA
+                            pair, cta_group::2, 256-row tiles; needs M > 128)
+                            or 4 (two pairs sharing each B slice by TMA
+                            multicast, 512-row tiles; needs Ms % 512 == 0).
+                            Default: the largest the shape allows            */
+    int stages;          /* operand ring stages of the GEMM: 2 .. 4 (cluster
+                            1) or 2 .. 6 (clusters 2 and 4); default all     */
+    int split_tail;      /* 1: cut the tiles of the last, partial wave of the
+                            persistent GEMM into 128-column halves (not with
+                            SM-mode producer items)                          */
+    int producer_items;  /* SM mode: GEMM items the producer CTAs take from
+                            the end of the order once their copies are done:
+                            0 = balanced on the host from the copy and tile
+                            times, -1 = none, n > 0 = the last n items       */
+    int producer_warps;  /* SM / SERIAL mode: copy workers (warps) per
+                            producer CTA, 1..4 (default 2)                   */
+    int producer_chunk;  /* SM / SERIAL mode: bytes per TMA bulk copy, a
+                            multiple of 1024 in [4096, 65536] (default 32768) */
+    int push;            /* 1: push-mode AllGather: the senders order the
+                            transfers (sender s reaches destination
+                            (s + j) mod W at step j), so rank `rank` receives
+                            the shards in the order rank-1, rank-2, ... (all
+                            at once with source_order 1) and its GEMM visits
+                            the m tiles in that order; 0: pull (rank+1,
+                            rank+2, ...)                                     */
 } tdg_ag_gemm_args;
 
 TDG_API int tdg_ag_gemm(tdg_symm *h, const tdg_ag_gemm_args *args, void *stream,
@@ -268,6 +291,17 @@ typedef struct {
                                   is not written when bit (g % 64) is set     */
     int c_f32;           /* 1: C_r is float32 (M*N*4 bytes, the fp32
                             accumulator unrounded); 0: bf16                   */
+    /* schedule (0 = default for the shape) */
+    int cluster;         /* as in tdg_ag_gemm_args                            */
+    int stages;          /* as in tdg_ag_gemm_args                            */
+    int push;            /* 1: push-mode AllGather: the copies go step by
+                            step, sender s to destination (s + j) mod W at
+                            step j = 1 .. W-1, so every destination receives
+                            one shard per step from a different sender; the
+                            GEMM follows the same steps (each rank's own
+                            shard first, then the shard each step brings).
+                            0: pull, rank by rank (rank r's shards r+1,
+                            r+2, ...), the GEMM rank by rank                 */
 } tdg_ag_gemm_all_args;
 
 TDG_API int tdg_ag_gemm_all_ranks(tdg_symm *h, const tdg_ag_gemm_all_args *args, void *stream,
@@ -312,6 +346,15 @@ typedef struct {
     int owner_block;     /* tile order: owners per block, each rank's tiles of
                             a block back to back (0 = 2; must divide world)  */
     int partial_f32;     /* 1: fp32 partials (twice the staging), 0: bf16     */
+    /* schedule (0 = default for the shape) */
+    int cluster;         /* CTAs per GEMM cluster: 1, 2 (needs (M/W) % 256
+                            == 0) or 4 (needs (M/W) % 512 == 0); default the
+                            largest the shape allows                         */
+    int stages;          /* as in tdg_ag_gemm_args                            */
+    int order;           /* 0: owner blocks (owner_block); 1: rank fastest   */
+    int red_rows;        /* rows of an owed reduction an epilogue warp works
+                            off after each tile: 4, 8, 16 or 32 (default 32
+                            for bf16 partials, 8 for fp32)                   */
 } tdg_gemm_rs_args;
 
 /* Bytes of one owner's staging area for the given shape (all W partials),

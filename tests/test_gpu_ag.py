@@ -27,7 +27,7 @@ def test_tiny_integer_bit_exact_all_modes_and_ranks():
             _gathered_ok(case, rank)
 
 
-@pytest.mark.parametrize("pair", ["1", "0"])
+@pytest.mark.parametrize("cluster", [0, 1])
 @pytest.mark.parametrize("b_layout", [tdg.B_KN, tdg.B_NK])
 @pytest.mark.parametrize("W,Ms,K,N", [
     (4, 256, 320, 520),     # 8 m tiles, 3 n tiles (last one 8 columns), 5 k blocks
@@ -35,24 +35,22 @@ def test_tiny_integer_bit_exact_all_modes_and_ranks():
     (2, 128, 64, 256),      # exactly one k block, full n tile
     (2, 384, 128, 136),     # pairs: 3 tiles of 256 rows, the last half empty
 ])
-def test_float_parity_small(W, Ms, K, N, b_layout, pair, monkeypatch):
-    # pair "1": CTA pairs (cta_group::2, 256-row tiles) where the shape allows;
-    # pair "0": one CTA per 128-row tile
-    monkeypatch.setenv("TDG_PAIR", pair)
+def test_float_parity_small(W, Ms, K, N, b_layout, cluster):
+    # cluster 0: the default shape (CTA pairs, cta_group::2, 256-row tiles,
+    # where the shape allows); cluster 1: one CTA per 128-row tile
     inp = synth.ag_inputs(W, Ms, K, N, "normal", seed=W * 7 + K)
     C64, C16 = oracle.ag_gemm(inp.shards, inp.B)
     case = AGCase(inp, b_layout=b_layout)
     for mode in ("sm", "serial", "ce"):
-        got, _ = case.run(rank=W - 1, mode=mode)
+        got, _ = case.run(rank=W - 1, mode=mode, cluster=cluster)
         assert_close(got, C64)
         _gathered_ok(case, W - 1)
 
 
-@pytest.mark.parametrize("pair", ["1", "0"])
-def test_integer_exact_larger_and_swizzle_invariance(pair, monkeypatch):
+@pytest.mark.parametrize("cluster", [0, 1])
+def test_integer_exact_larger_and_swizzle_invariance(cluster):
     # integer inputs, |sums| <= 4K: exact in fp32; output identical for every
     # rank, swizzle on/off, signal granularity and producer count
-    monkeypatch.setenv("TDG_PAIR", pair)
     inp = synth.ag_inputs(4, 256, 512, 384, "int2", seed=3)
     _, C16 = oracle.ag_gemm(inp.shards, inp.B)
     case = AGCase(inp)
@@ -61,26 +59,24 @@ def test_integer_exact_larger_and_swizzle_invariance(pair, monkeypatch):
         for swz in (True, False):
             for sig in (0, 64, 256):
                 got, _ = case.run(rank=rank, mode="sm", swizzle=swz, signal_rows=sig,
-                                  producers=4 + rank)
+                                  producers=4 + rank, cluster=cluster)
                 outs.append(got)
     for o in outs:
         assert np.array_equal(o, C16)
 
 
-@pytest.mark.parametrize("pair", ["1", "0"])
+@pytest.mark.parametrize("cluster", [2, 1])
 @pytest.mark.parametrize("N", [2440, 2432])
-def test_split_tail_wave_bit_exact(N, pair, monkeypatch):
+def test_split_tail_wave_bit_exact(N, cluster):
     # 2048 x N: 80 pair tiles (160 single tiles) over 76 pairs (152 CTAs), so
     # the last wave's few tiles are cut into 128-column halves; with N = 2440
     # the last n tile is 136 wide (halves of 128 and 8), with N = 2432 it is
     # 128 wide (its second half is empty and skipped by every role)
-    monkeypatch.setenv("TDG_PAIR", pair)
-    monkeypatch.setenv("TDG_SPLIT_TAIL", "1")
     inp = synth.ag_inputs(8, 256, 64, N, "int2", seed=N)
     _, C16 = oracle.ag_gemm(inp.shards, inp.B)
     case = AGCase(inp)
     for mode in ("ce", "sm", "serial"):
-        got, _ = case.run(rank=5, mode=mode)
+        got, _ = case.run(rank=5, mode=mode, cluster=cluster, split_tail=True, producer_items=-1)
         assert np.array_equal(got, C16), mode
 
 
@@ -219,17 +215,17 @@ def test_ll_second_heap_on_the_same_memory():
     assert np.array_equal(got, C2)
 
 
-@pytest.mark.parametrize("rounds", ["0", "1", "-1"])
-def test_sm_mode_producers_take_the_last_items(rounds, monkeypatch):
+@pytest.mark.parametrize("items", [4, 1, 0, -1, 40])
+def test_sm_mode_producers_take_the_last_items(items):
     # 36 two-pair-cluster tiles (M 6144, 3 n tiles); 16 producer CTAs are 4
-    # clusters.  With TDG_AG_PROD_ROUNDS=0 the producer clusters take the last
-    # 4 items after their copies (the 32 GEMM clusters then need one round,
-    # not two); with 1 or -1 they take none.  Every split gives the oracle's bits.
-    monkeypatch.setenv("TDG_AG_PROD_ROUNDS", rounds)
+    # clusters.  producer_items n > 0: the producer clusters take the last n
+    # items after their copies (40 > 36: all of them, the GEMM clusters none);
+    # 0: the split balanced on the host; -1: none.  Every split gives the
+    # oracle's bits.
     inp = synth.ag_inputs(4, 1536, 128, 520, "int2", seed=17)
     _, C16 = oracle.ag_gemm(inp.shards, inp.B)
     case = AGCase(inp)
     for rank in (0, 3):
-        got, _ = case.run(rank=rank, mode="sm", producers=16)
+        got, _ = case.run(rank=rank, mode="sm", producers=16, producer_items=items)
         assert np.array_equal(got, C16), rank
         _gathered_ok(case, rank)

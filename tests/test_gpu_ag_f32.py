@@ -10,23 +10,21 @@ from gpu_util import AGCase, bf16_f64
 
 pytestmark = pytest.mark.gpu
 
-# (TDG_QUAD, TDG_PAIR): two-pair clusters, CTA pairs, one CTA per tile
-SHAPES = [("1", "1"), ("0", "1"), ("0", "0")]
+# GEMM cluster shapes: two-pair clusters, CTA pairs, one CTA per tile
+SHAPES = [4, 2, 1]
 
 
-@pytest.mark.parametrize("quad,pair", SHAPES)
+@pytest.mark.parametrize("cluster", SHAPES)
 @pytest.mark.parametrize("b_layout", [tdg.B_KN, tdg.B_NK])
-def test_integer_sums_exact_in_every_mode(quad, pair, b_layout, monkeypatch):
+def test_integer_sums_exact_in_every_mode(cluster, b_layout):
     # integers in [-2, 2] and K = 1032: |sums| <= 4128, exact in fp32 but not
     # in bf16, so the fp32 output is the oracle's exact value and bf16 is not
-    monkeypatch.setenv("TDG_QUAD", quad)
-    monkeypatch.setenv("TDG_PAIR", pair)
     inp = synth.ag_inputs(2, 512, 1032, 264, "int2", seed=41)
     C64, C16 = oracle.ag_gemm(inp.shards, inp.B)
     assert not np.array_equal(bf16_f64(C16), C64)     # bf16 would have rounded
     case = AGCase(inp, b_layout=b_layout, ll=True, c_f32=True)
     for mode in ("sm", "serial", "ce", "ll"):
-        got, _ = case.run(rank=1, mode=mode, ll_off=case.ll_off)
+        got, _ = case.run(rank=1, mode=mode, ll_off=case.ll_off, cluster=cluster)
         assert got.dtype == np.float32
         assert np.array_equal(got.astype(np.float64), C64), mode
 

@@ -71,15 +71,14 @@ def _rs_cases(n=12, seed=2025):
 
 
 @pytest.mark.parametrize("W,Ms,K,N,lay,seed", _ag_cases())
-def test_ag_sm_mode_producers_take_items_random_shapes(W, Ms, K, N, lay, seed, monkeypatch):
-    # TDG_AG_PROD_ROUNDS=0: producer clusters take GEMM items from the end as
-    # soon as that shortens the schedule (their copies still come first)
-    monkeypatch.setenv("TDG_AG_PROD_ROUNDS", "0")
+def test_ag_sm_mode_producers_take_items_random_shapes(W, Ms, K, N, lay, seed):
+    # producer clusters take the last 3 GEMM items once their copies are done
+    # (all of them when there are fewer)
     inp = synth.ag_inputs(W, Ms, K, N, "int2", seed=seed)
     _, C16 = oracle.ag_gemm(inp.shards, inp.B)
     case = AGCase(inp, b_layout=tdg.B_KN if lay == 0 else tdg.B_NK)
     for producers in (4, 16):
-        got, _ = case.run(rank=seed % W, mode="sm", producers=producers)
+        got, _ = case.run(rank=seed % W, mode="sm", producers=producers, producer_items=3)
         assert np.array_equal(got, C16), producers
         assert np.array_equal(to_bits(case.gathered(seed % W)), np.concatenate(inp.shards)), producers
 

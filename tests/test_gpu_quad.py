@@ -1,6 +1,6 @@
 """GPU parity of the GEMM on clusters of two CTA pairs (512-row tiles, each B
 slice fetched by one pair and multicast to the other) against the CPU oracle
-and against the same call on single pairs (TDG_QUAD=0)."""
+and against the same call on single pairs (cluster 2)."""
 import numpy as np
 import pytest
 
@@ -17,19 +17,18 @@ pytestmark = pytest.mark.gpu
 # N = 256: one full tile.
 @pytest.mark.parametrize("b_layout", [tdg.B_KN, tdg.B_NK])
 @pytest.mark.parametrize("N", [3200, 520, 456, 256])
-def test_ag_integer_bit_exact_quad_and_pair(N, b_layout, monkeypatch):
+def test_ag_integer_bit_exact_quad_and_pair(N, b_layout):
     inp = synth.ag_inputs(2, 512, 192, N, "int2", seed=N)
     _, C16 = oracle.ag_gemm(inp.shards, inp.B)
     case = AGCase(inp, b_layout=b_layout)
-    for quad in ("1", "0"):
-        monkeypatch.setenv("TDG_QUAD", quad)
+    for cluster in (4, 2):
         for mode in ("sm", "serial", "ce"):
-            got, _ = case.run(rank=1, mode=mode)
-            assert np.array_equal(got, C16), (quad, mode)
+            got, _ = case.run(rank=1, mode=mode, cluster=cluster)
+            assert np.array_equal(got, C16), (cluster, mode)
 
 
 @pytest.mark.parametrize("b_layout", [tdg.B_KN, tdg.B_NK])
-def test_ag_float_parity_and_same_bits_as_pairs(b_layout, monkeypatch):
+def test_ag_float_parity_and_same_bits_as_pairs(b_layout):
     # W=4, Ms=1024 (two 512-row tiles per shard), K=200 (ragged k block),
     # N=712 (last n tile 200 wide).  The quad and pair kernels run the same
     # MMA sequence per output tile, so their outputs agree bit for bit.
@@ -37,43 +36,40 @@ def test_ag_float_parity_and_same_bits_as_pairs(b_layout, monkeypatch):
     C64, _ = oracle.ag_gemm(inp.shards, inp.B)
     case = AGCase(inp, b_layout=b_layout)
     outs = {}
-    for quad in ("1", "0"):
-        monkeypatch.setenv("TDG_QUAD", quad)
+    for cluster in (4, 2):
         for rank in (0, 3):
-            got, _ = case.run(rank=rank, mode="sm")
+            got, _ = case.run(rank=rank, mode="sm", cluster=cluster)
             assert_close(got, C64)
-            outs[(quad, rank)] = got
+            outs[(cluster, rank)] = got
     for rank in (0, 3):
-        assert np.array_equal(outs[("1", rank)], outs[("0", rank)]), rank
+        assert np.array_equal(outs[(4, rank)], outs[(2, rank)]), rank
 
 
 # Mo = M / W a multiple of 512: one or more 512-row tiles per owner.  K = 64
 # keeps every bf16 partial exact, so the reduced output is exact too.
 @pytest.mark.parametrize("b_layout", [tdg.B_KN, tdg.B_NK])
 @pytest.mark.parametrize("W,M,N", [(2, 1024, 520), (4, 2048, 3200), (2, 2048, 456)])
-def test_rs_integer_bit_exact_quad_and_pair(W, M, N, b_layout, monkeypatch):
+def test_rs_integer_bit_exact_quad_and_pair(W, M, N, b_layout):
     inp = synth.rs_inputs(W, M, 64, N, "int2", seed=W + N)
     _, out16 = oracle.gemm_rs(inp.As, inp.Bs)
     case = RSCase(inp, b_layout=b_layout)
-    for quad in ("1", "0"):
-        monkeypatch.setenv("TDG_QUAD", quad)
+    for cluster in (4, 2):
         for mode in ("sm", "serial"):
-            got, _ = case.run(mode=mode)
-            assert np.array_equal(got, out16), (quad, mode)
+            got, _ = case.run(mode=mode, cluster=cluster)
+            assert np.array_equal(got, out16), (cluster, mode)
 
 
 @pytest.mark.parametrize("b_layout", [tdg.B_KN, tdg.B_NK])
-def test_rs_float_parity_and_same_bits_as_pairs(b_layout, monkeypatch):
+def test_rs_float_parity_and_same_bits_as_pairs(b_layout):
     inp = synth.rs_inputs(2, 1024, 328, 776, "normal", seed=13)
     out64, _ = oracle.gemm_rs(inp.As, inp.Bs)
     case = RSCase(inp, b_layout=b_layout)
     outs = {}
-    for quad in ("1", "0"):
-        monkeypatch.setenv("TDG_QUAD", quad)
-        got, _ = case.run(mode="sm")
+    for cluster in (4, 2):
+        got, _ = case.run(mode="sm", cluster=cluster)
         assert_close(got, out64)
-        outs[quad] = got
-    assert np.array_equal(outs["1"], outs["0"])
+        outs[cluster] = got
+    assert np.array_equal(outs[4], outs[2])
 
 
 @pytest.mark.parametrize("mode", ["sm", "ce"])

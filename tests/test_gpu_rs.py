@@ -22,26 +22,23 @@ def test_integer_small_k_bit_exact_both_modes(W, M):
         assert np.array_equal(got, out16), mode
 
 
-@pytest.mark.parametrize("order", ["1", "0"])
+@pytest.mark.parametrize("order", [1, 0])
 @pytest.mark.parametrize("W,M", [(4, 2048), (8, 4096)])
-def test_rank_fastest_tile_order_gives_the_same_bits(W, M, order, monkeypatch):
-    # TDG_RS_ORDER=1 walks the tiles rank-fastest instead of in owner blocks;
-    # the reduction still sums in rank order, so the bits do not change
-    monkeypatch.setenv("TDG_RS_ORDER", order)
+def test_rank_fastest_tile_order_gives_the_same_bits(W, M, order):
+    # order 1 walks the tiles rank-fastest instead of in owner blocks; the
+    # reduction still sums in rank order, so the bits do not change
     inp = synth.rs_inputs(W, M, 64, 264, "int2", seed=W + M)
     _, out16 = oracle.gemm_rs(inp.As, inp.Bs)
     case = RSCase(inp)
     for mode in ("sm", "serial"):
-        got, _ = case.run(mode=mode)
+        got, _ = case.run(mode=mode, order=order)
         assert np.array_equal(got, out16), mode
-    monkeypatch.setenv("TDG_RS_ORDER", order)
     f = synth.rs_inputs(W, M, 200, 264, "normal", seed=W * M)
-    ref = RSCase(f).run(mode="sm")[0]
-    monkeypatch.setenv("TDG_RS_ORDER", "0" if order == "1" else "1")
-    assert np.array_equal(RSCase(f).run(mode="sm")[0], ref)
+    ref = RSCase(f).run(mode="sm", order=order)[0]
+    assert np.array_equal(RSCase(f).run(mode="sm", order=1 - order)[0], ref)
 
 
-@pytest.mark.parametrize("pair", ["1", "0"])
+@pytest.mark.parametrize("cluster", [0, 1])
 @pytest.mark.parametrize("b_layout", [tdg.B_KN, tdg.B_NK])
 @pytest.mark.parametrize("W,M,K,N", [
     (2, 256, 200, 264),    # ragged k block and n tile
@@ -49,13 +46,12 @@ def test_rank_fastest_tile_order_gives_the_same_bits(W, M, order, monkeypatch):
     (8, 1024, 128, 256),
     (2, 1024, 136, 136),   # pairs with a narrow n tile
 ])
-def test_float_parity_small(W, M, K, N, b_layout, pair, monkeypatch):
-    monkeypatch.setenv("TDG_PAIR", pair)
+def test_float_parity_small(W, M, K, N, b_layout, cluster):
     inp = synth.rs_inputs(W, M, K, N, "normal", seed=M + K)
     out64, _ = oracle.gemm_rs(inp.As, inp.Bs)
     case = RSCase(inp, b_layout=b_layout)
     for mode in ("sm", "serial"):
-        got, _ = case.run(mode=mode)
+        got, _ = case.run(mode=mode, cluster=cluster)
         assert_close(got, out64)
 
 
@@ -136,18 +132,17 @@ def test_f32_partials_float_within_one_ulp(b_layout):
     assert np.max(np.abs(got64 - out64)) <= np.max(np.abs(b64 - out64))
 
 
-@pytest.mark.parametrize("red_rows", ["4", "8", "32"])
-def test_owed_reductions_worked_off_in_slices(red_rows, monkeypatch):
+@pytest.mark.parametrize("red_rows", [4, 8, 32])
+def test_owed_reductions_worked_off_in_slices(red_rows):
     # many tiles per epilogue warp (W = 8, 2 x 8 quad tiles per owner), fp32
     # partials: the last arriver queues its reduction and works it off a few
     # rows per tile (with 4 rows a third owed reduction often finishes the
     # oldest at once); every output must match the oracle and the separate
     # reduction launch bit for bit (integer inputs: exact)
-    monkeypatch.setenv("TDG_RS_RED_ROWS", red_rows)
     W, M, K, N = 8, 8192, 64, 2048
     inp = synth.rs_inputs(W, M, K, N, "int2", seed=41)
     case = RSCase(inp, f32=True)
-    fused, _ = case.run(mode="sm")
+    fused, _ = case.run(mode="sm", red_rows=red_rows)
     serial, _ = case.run(mode="serial")
     assert np.array_equal(fused, serial)
     g = np.random.default_rng(5)

@@ -78,20 +78,52 @@ def tune(key: tuple, candidates: List[dict], run: Callable[[dict], None], group=
     return candidates[best], table
 
 
-def ag_candidates(M: int, modes=("ce", "sm"), producers=(8, 16, 24), signal_rows=(0,),
-                  source_orders=(0, 1)) -> List[dict]:
+def _clusters(allow2: bool, allow4: bool) -> List[int]:
+    """GEMM cluster shapes a shape allows, the library's default first."""
     out = []
-    for mode, so, sr in itertools.product(modes, source_orders, signal_rows):
+    if allow4:
+        out.append(4)
+    if allow2:
+        out.append(2)
+    return out or [1]
+
+
+def ag_candidates(M: int, Ms: int = 0, modes=("ce", "sm"), producers=(0, 8, 16), signal_rows=(0,),
+                  source_orders=(0, 1), pushes=(0, 1), clusters=None, stages=(0, 4)) -> List[dict]:
+    """AllGather+GEMM schedules: mode x source order x push x GEMM cluster
+    shape x ring stages (x producer CTAs in SM mode; 0 = the library's
+    default count).  Ms = 0 leaves the cluster shape to the library."""
+    if clusters is None:
+        clusters = _clusters(M > 128, Ms > 0 and Ms % 512 == 0) if Ms else [0]
+    out = []
+    for mode, so, sr, push, cl, st in itertools.product(modes, source_orders, signal_rows, pushes, clusters,
+                                                         stages):
+        if cl == 1 and st > 4:
+            continue
+        base = dict(mode=mode, signal_rows=sr, source_order=so, push=push, cluster=cl, stages=st)
         if mode == "sm":
             for pr in producers:
-                out.append(dict(mode=mode, producers=pr, signal_rows=sr, source_order=so))
+                out.append(dict(base, producers=pr))
         else:
-            out.append(dict(mode=mode, producers=0, signal_rows=sr, source_order=so))
+            out.append(dict(base, producers=0))
     return out
 
 
-def rs_candidates(world: int) -> List[dict]:
-    return [dict(owner_block=ob) for ob in range(1, world + 1) if world % ob == 0]
+def rs_candidates(world: int, Mo: int = 0, clusters=None, stages=(0, 4), orders=(0, 1)) -> List[dict]:
+    """GEMM+ReduceScatter schedules: owner block x tile order x GEMM cluster
+    shape x ring stages.  Mo (rows per owner) = 0 leaves the cluster shape to
+    the library."""
+    if clusters is None:
+        clusters = _clusters(Mo % 256 == 0, Mo % 512 == 0) if Mo else [0]
+    out = []
+    for ob in (d for d in range(1, world + 1) if world % d == 0):
+        for order, cl, st in itertools.product(orders, clusters, stages):
+            if order == 1 and ob != 1:
+                continue    # the rank-fastest order has no owner blocks
+            if cl == 1 and st > 4:
+                continue
+            out.append(dict(owner_block=ob, order=order, cluster=cl, stages=st))
+    return out
 
 
 def clear_cache():

@@ -1,40 +1,54 @@
 // tdg_ag.cu -- tile-centric overlapped AllGather + GEMM ("Triton-distributed
 // 语义", 内核设计模式 "AllGather + GEMM 重叠"; paper summary, 方法: AllGather
-// on SMs or on the copy engine, resource partitioning, NVSwitch swizzle).
+// on SMs or on the copy engine, push or pull, resource partitioning, NVSwitch
+// swizzle).
 //
 // SM mode: one cooperative persistent launch.  CTAs [0, P) are producers:
-// their copy workers (one thread per warp, 1-D TMA bulk copies through a
-// shared-memory ring) pull shard tiles from the peer regions into the
-// gathered buffer, one signal group at a time, in source order
-// (rank+1, rank+2, ..., rank) -- one source at a time, the NVSwitch order of
-// Triton-distributed -- and publish each finished group with st.release of the
-// call's epoch.  CTAs [P, grid) are the persistent tcgen05 GEMM; its loader
-// waits on the groups of each A tile with a bounded ld.acquire spin, then
-// fences the async proxy and issues TMA.  The local shard is read in place.
-// Once its copies are done, a producer cluster takes GEMM items from the end
-// of the order (the host balances that split from the copy and tile times).
+// each has a few copy workers (one thread per warp) that stream their signal
+// groups of shard rows from the peer regions into the gathered buffer through
+// a ring in shared memory (1-D TMA bulk copies, global -> shared -> global),
+// keeping all but one ring slot loading at all times, across group
+// boundaries.  A group's flag is released (st.release of the call's epoch)
+// once its stores are complete, while the stores of later groups are still
+// in flight.  Sources go one at a time (the NVSwitch order: rank+1, rank+2,
+// ..., the local shard last) or all at once (round robin over sources).
+// CTAs [P, grid) are the persistent tcgen05 GEMM; its loader waits on the
+// groups of each A tile with a bounded ld.acquire spin, then fences the async
+// proxy and issues TMA.  The local shard is read in place.  Once its copies
+// are done, a producer cluster takes GEMM items from the end of the order.
+// Push mode: the senders choose the order -- sender s reaches destination
+// (s + j) mod W at step j -- so rank r receives rank-1, rank-2, ..., and the
+// GEMM visits the m tiles in that order; pull: rank+1, rank+2, ...
 // CE mode: cudaMemcpyAsync per group on the side stream, each followed by a
-// stream-ordered cuStreamWriteValue32 of the flag; the GEMM-only launch on
-// the main stream waits on the flags.
+// stream-ordered cuStreamWriteValue32 of the flag, all queued before the
+// GEMM-only launch on the main stream that waits on the flags.
 // LL mode: one cooperative launch of sender CTAs (8-byte {payload, epoch}
 // words into the rank's LL buffer), receiver CTAs (poll every word, unpack it
 // into the gathered buffer, release the group's flag) and the GEMM, which
 // waits on those flags as in SM mode.
 // SERIAL mode: a copy-only launch (all SMs), then a GEMM-only launch that does
 // not wait; the two are ordered by the stream.
-// Tile order: Triton-distributed's rank swizzle over m tiles; m-major while B fits in
-// about half of L2, else groups of 8 m tiles with n outer inside a group.
+// Tile order: Triton-distributed's rank swizzle over m tiles (mirrored in push
+// mode); m-major while B fits in about half of L2, else groups of 8 m tiles
+// with n outer inside a group.
 #include "tdg_gemm.cuh"
 #include "tdg_internal.h"
 
 namespace tdg {
 
 namespace ag {
-constexpr int PW = 4;          // copy workers (warps) per producer CTA
-constexpr int PSLOTS = 3;      // ring slots per worker
-constexpr int PCHUNK = 16384;  // bytes per bulk copy
-constexpr int OFF_PBAR = PW * PSLOTS * PCHUNK;
-static_assert(OFF_PBAR + PW * PSLOTS * 8 <= gm::SMEM_BYTES - 1024, "producer smem");
+// The producer's ring is the GEMM's operand ring (a producer CTA is not a
+// GEMM CTA until its copies are done); its slot barriers sit after it, in
+// the GEMM's epilogue staging area.
+constexpr int PRING = gm::RING_BYTES;
+constexpr int PMAX_SLOTS = 32;      // per worker (one phase bit each)
+constexpr int PMAX_WARPS = 4;
+constexpr int OFF_PBAR = PRING;
+constexpr int LAG_DONE = 4;         // a group's flag waits until all but its 4 latest stores are complete
+constexpr int PFIFO = 8;            // groups whose stores are issued but whose flag is not yet released
+constexpr int DEF_WARPS = 2;
+constexpr uint32_t DEF_CHUNK = 32768;
+static_assert(OFF_PBAR + PMAX_WARPS * PMAX_SLOTS * 8 <= gm::SMEM_BYTES - 1024, "producer smem");
 } // namespace ag
 
 struct AgParams {
@@ -79,6 +93,13 @@ struct AgParams {
     int n_send;
     uint64_t *ll_buf; // M * K / 2 words in region(rank)
     int c_f32;        // 1: C is fp32
+    int stages;       // GEMM ring stages in use
+    int push;         // 1: sources in push order (rank-1, rank-2, ...)
+    int mirror;       // 1: the m tiles in push order (push with the swizzle on)
+    int t_end;        // the m tile of the local shard's last row (the mirror's start)
+    int pw;           // copy workers per producer CTA
+    uint32_t pchunk;  // bytes per bulk copy
+    int pslots;       // ring slots per worker
 };
 
 template <int BMN, bool F32 = false> struct AgPolicy {
@@ -122,7 +143,11 @@ template <int BMN, bool F32 = false> struct AgPolicy {
             pm0 = grp * GM + (int)(in % rows);
         }
         // Triton-distributed's swizzle: pid_m = (pid_m + rank * tiles_per_pe) % total
-        const int pm = (pm0 + p.swz) % p.m_tiles;
+        // (local shard first, then rank+1, rank+2, ...).  Push mode mirrors it,
+        // pid_m = (t_end - pid_m) mod total: the local shard first, then
+        // rank-1, rank-2, ..., the order in which the senders deliver.
+        const int pm = p.mirror ? ((p.t_end - pm0) % p.m_tiles + p.m_tiles) % p.m_tiles
+                              : (pm0 + p.swz) % p.m_tiles;
         t.m0 = pm * tm + sub * gm::BM;
         t.n0 = t.pn * gm::BN;
         t.n_valid = (int)min((int64_t)gm::BN, p.N - t.n0);
@@ -235,92 +260,172 @@ template <int BMN, bool F32 = false> struct AgPolicy {
     __device__ static void after_tile(const Params &, const TileInfo &, int, int, EpiState &, bool) {}
 };
 
-// One copy worker: copy `bytes` from src to dst through its ring.  Returns
-// false if a wait ran out of time (after draining its own loads in flight).
-__device__ bool ring_copy(uint8_t *dst, const uint8_t *src, uint64_t bytes, uint8_t *ring,
-                          uint64_t *bar, uint32_t &phases, uint64_t tmo)
+// Unit u of the producers (one signal group of one shard): the source and
+// destination rows.  Sources one at a time: every part of the first source,
+// then the next; all at once: part 0 of every source, then part 1, ...  Pull
+// visits rank+1, rank+2, ... (the local shard last when it is read in place,
+// first otherwise); push visits rank-1, rank-2, ..., and the parts of a shard
+// from its last rows to its first, the order in which the GEMM takes them.
+struct CopyUnit {
+    const uint8_t *src;
+    uint8_t *dst;
+    uint64_t bytes;
+    int64_t g; // flag word of the group
+};
+
+__device__ CopyUnit copy_unit(const AgParams &p, int64_t u)
+{
+    const int seq = p.mesh ? (int)(u % p.W) : (int)(u / p.units_per_shard);
+    int64_t part = p.mesh ? u / p.W : u % p.units_per_shard;
+    int shard;
+    if (p.push) {
+        const int back = p.local_last ? 1 + seq : seq;
+        shard = ((p.rank - back) % p.W + p.W) % p.W;
+        part = p.units_per_shard - 1 - part;
+    } else {
+        shard = p.local_last ? (p.rank + 1 + seq) % p.W : (p.rank + seq) % p.W;
+    }
+    const uint64_t row_bytes = (uint64_t)p.K * 2;
+    const int64_t row0 = part * p.unit_rows;
+    const int64_t rows = min(p.unit_rows, p.Ms - row0);
+    const int64_t grow = (int64_t)shard * p.Ms + row0;
+    CopyUnit c;
+    c.src = p.regions + (uint64_t)shard * p.region_bytes + p.a_off + (uint64_t)row0 * row_bytes;
+    c.dst = p.gathered + (uint64_t)grow * row_bytes;
+    c.bytes = (uint64_t)rows * row_bytes;
+    c.g = grow / p.sig_rows;
+    return c;
+}
+
+// notify: the group's stores are complete (the caller waited on their bulk
+// groups); order them before the generic release of the flag
+__device__ __forceinline__ void producer_notify(const AgParams &p, int64_t g)
+{
+    fence_proxy_async_global();
+    if (p.signal && !((p.skip_mask >> (g & 63)) & 1ull))
+        st_release_gpu(p.flags_w + g, p.epoch);
+}
+
+// One copy worker (one thread): it copies its units u = worker, worker +
+// nworkers, ... chunk by chunk through a ring of S slots of `chunk` bytes
+// (1-D TMA bulk copies global -> shared -> global).  Loads run S - 1 chunks
+// ahead of the stores, across unit boundaries; a slot is refilled as soon as
+// the store of its previous chunk has read it.  A unit's flag is released
+// once all but the LAG_DONE latest stores are complete, so the pipeline never
+// drains between units.  Returns false when a wait ran out of time (after
+// waiting, bounded, for its own loads in flight).
+__device__ bool copy_worker(const AgParams &p, int64_t worker, int64_t nworkers, uint8_t *ring,
+                            uint64_t *bar, int S, uint32_t chunk)
 {
     using namespace ag;
-    const int64_t nch = (int64_t)((bytes + PCHUNK - 1) / PCHUNK);
-    uint32_t pending = 0;
-    auto csize = [&](int64_t i) -> uint32_t {
-        const uint64_t off = (uint64_t)i * PCHUNK;
-        return (uint32_t)min((uint64_t)PCHUNK, bytes - off);
+    if (worker >= p.n_units)
+        return true;
+    // load cursor (unit lu, byte lo) and store cursor (unit su, byte so)
+    int64_t lu = worker, su = worker;
+    uint64_t lo = 0, so = 0;
+    CopyUnit lc = copy_unit(p, lu), sc = lc;
+    uint32_t ql = 0, q = 0; // chunks loaded (issued) and stored so far
+    uint32_t phases = 0, pending = 0;
+    int64_t fg[PFIFO];
+    uint32_t flast[PFIFO];
+    int fh = 0, fn = 0;
+    auto load_next = [&]() {
+        if (lu >= p.n_units)
+            return;
+        const int s = (int)(ql % (uint32_t)S);
+        const uint32_t b = (uint32_t)min((uint64_t)chunk, lc.bytes - lo);
+        mbar_arrive_expect_tx(&bar[s], b);
+        bulk_load(ring + (size_t)s * chunk, lc.src + lo, b, &bar[s]);
+        pending |= 1u << s;
+        ++ql;
+        lo += b;
+        if (lo >= lc.bytes) {
+            lu += nworkers;
+            lo = 0;
+            if (lu < p.n_units)
+                lc = copy_unit(p, lu);
+        }
     };
-    for (int64_t i = 0; i < nch && i < PSLOTS; ++i) {
-        mbar_arrive_expect_tx(&bar[i], csize(i));
-        bulk_load(ring + i * PCHUNK, src + (uint64_t)i * PCHUNK, csize(i), &bar[i]);
-        pending |= 1u << i;
-    }
-    for (int64_t i = 0; i < nch; ++i) {
-        const int s = (int)(i % PSLOTS);
-        if (!mbar_wait(&bar[s], (phases >> s) & 1u, tmo)) {
-            for (int t = 0; t < PSLOTS; ++t)
-                if ((pending >> t) & 1u) {
-                    if (t != s && mbar_wait(&bar[t], (phases >> t) & 1u, tmo))
-                        phases ^= 1u << t;
-                }
+    for (int i = 0; i < S - 1; ++i)
+        load_next();
+    while (q < ql) {
+        const int s = (int)(q % (uint32_t)S);
+        if (!mbar_wait(&bar[s], (phases >> s) & 1u, p.timeout_ns)) {
+            report_fault(p.status, TDG_ERR_TIMEOUT, TDG_WHERE_PIPE, (uint32_t)su, p.epoch);
+            for (int t = 0; t < S; ++t) // every load in flight, this one included (bounded)
+                if ((pending >> t) & 1u)
+                    (void)mbar_wait(&bar[t], (phases >> t) & 1u, p.timeout_ns);
             bulk_wait<0>();
             return false;
         }
         phases ^= 1u << s;
         pending &= ~(1u << s);
-        bulk_store(dst + (uint64_t)i * PCHUNK, ring + s * PCHUNK, csize(i));
+        const uint32_t b = (uint32_t)min((uint64_t)chunk, sc.bytes - so);
+        bulk_store(sc.dst + so, ring + (size_t)s * chunk, b);
         bulk_commit();
-        const int64_t j = i - 1 + PSLOTS;
-        if (i >= 1 && j < nch) {
-            bulk_wait_read<1>(); // the store of chunk i-1 has read its slot
-            const int s2 = (int)(j % PSLOTS);
-            mbar_arrive_expect_tx(&bar[s2], csize(j));
-            bulk_load(ring + s2 * PCHUNK, src + (uint64_t)j * PCHUNK, csize(j), &bar[s2]);
-            pending |= 1u << s2;
+        so += b;
+        if (so >= sc.bytes) { // the unit's last store is issued
+            if (fn == PFIFO) { // (units of one chunk each): release the oldest at once
+                bulk_wait<0>();
+                while (fn > 0) {
+                    producer_notify(p, fg[fh]);
+                    fh = (fh + 1) % PFIFO;
+                    --fn;
+                }
+            }
+            fg[(fh + fn) % PFIFO] = sc.g;
+            flast[(fh + fn) % PFIFO] = q;
+            ++fn;
+            su += nworkers;
+            so = 0;
+            if (su < p.n_units)
+                sc = copy_unit(p, su);
         }
+        ++q;
+        // the slot to refill held the chunk before the one just stored: wait
+        // until that store has read it (all but the latest store group)
+        bulk_wait_read<1>();
+        load_next();
+        // stores 0 .. q-1 are issued; all but the LAG_DONE latest complete
+        // means every unit whose last store is at most q-1-LAG_DONE is done
+        if (fn > 0 && flast[fh] + LAG_DONE < q) {
+            bulk_wait<LAG_DONE>();
+            while (fn > 0 && flast[fh] + LAG_DONE < q) {
+                producer_notify(p, fg[fh]);
+                fh = (fh + 1) % PFIFO;
+                --fn;
+            }
+        }
+    }
+    bulk_wait<0>();
+    while (fn > 0) {
+        producer_notify(p, fg[fh]);
+        fh = (fh + 1) % PFIFO;
+        --fn;
     }
     return true;
 }
 
-// Producer CTA: PW copy workers (lane 0 of warps 0..PW-1).
+// Producer CTA: p.pw copy workers (lane 0 of warps 0 .. pw-1), each with
+// p.pslots slots of p.pchunk bytes.
 __device__ void ag_producer(const AgParams &p, uint8_t *smem)
 {
     using namespace ag;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (warp >= PW || lane != 0)
+    if (warp >= p.pw || lane != 0)
         return;
-    uint8_t *ring = smem + warp * PSLOTS * PCHUNK;
-    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + OFF_PBAR) + warp * PSLOTS;
-    for (int i = 0; i < PSLOTS; ++i)
+    const int S = p.pslots;
+    uint8_t *ring = smem + (size_t)warp * S * p.pchunk;
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + OFF_PBAR) + warp * PMAX_SLOTS;
+    for (int i = 0; i < S; ++i)
         mbar_init(&bar[i], 1);
     fence_mbar_init();
     fence_proxy_async_smem();
-    uint32_t phases = 0;
-    const int64_t worker = (int64_t)blockIdx.x * PW + warp;
-    const int64_t nworkers = (int64_t)p.n_prod * PW;
-    const uint64_t row_bytes = (uint64_t)p.K * 2;
-    for (int64_t u = worker; u < p.n_units; u += nworkers) {
-        // one source at a time: all parts of source seq, then seq + 1, ...;
-        // all sources at once: part 0 of every source, then part 1, ...
-        const int seq = p.mesh ? (int)(u % p.W) : (int)(u / p.units_per_shard);
-        const int64_t part = p.mesh ? u / p.W : u % p.units_per_shard;
-        const int shard = p.local_last ? (p.rank + 1 + seq) % p.W : (p.rank + seq) % p.W;
-        const int64_t row0 = part * p.unit_rows;
-        const int64_t rows = min(p.unit_rows, p.Ms - row0);
-        const uint8_t *src = p.regions + (uint64_t)shard * p.region_bytes + p.a_off + (uint64_t)row0 * row_bytes;
-        const int64_t grow = (int64_t)shard * p.Ms + row0;
-        uint8_t *dst = p.gathered + (uint64_t)grow * row_bytes;
-        if (!ring_copy(dst, src, (uint64_t)rows * row_bytes, ring, bar, phases, p.timeout_ns)) {
-            report_fault(p.status, TDG_ERR_TIMEOUT, TDG_WHERE_PIPE, (uint32_t)u, p.epoch);
-            break;
-        }
-        bulk_wait<0>();             // the group's writes are complete ...
-        fence_proxy_async_global(); // ... and ordered before the generic release
-        if (p.signal) {
-            const int64_t g = grow / p.sig_rows;
-            if (!((p.skip_mask >> (g & 63)) & 1ull))
-                st_release_gpu(p.flags_w + g, p.epoch); // notify
-        }
-    }
+    const int64_t worker = (int64_t)blockIdx.x * p.pw + warp;
+    const int64_t nworkers = (int64_t)p.n_prod * p.pw;
+    (void)copy_worker(p, worker, nworkers, ring, bar, S, p.pchunk);
     // the ring's shared memory may serve another role next
-    for (int i = 0; i < PSLOTS; ++i)
+    for (int i = 0; i < S; ++i)
         mbar_inval(&bar[i]);
 }
 
@@ -360,7 +465,7 @@ __device__ void ll_sender(const AgParams &p, int cta, int ncta)
                 seq = (int)(w / wps);
                 off = w % wps;
             }
-            const int shard = (p.rank + 1 + seq) % p.W;
+            const int shard = p.push ? ((p.rank - 1 - seq) % p.W + p.W) % p.W : (p.rank + 1 + seq) % p.W;
             const int64_t word = (int64_t)shard * wps + off;
             const int64_t g = (word * 2 / p.K) / p.sig_rows;
             if ((p.skip_mask >> (g & 63)) & 1ull)
@@ -502,29 +607,45 @@ int ag_grid(const AgParams &p, int b_layout, int sms)
 }
 
 // SM mode: once a producer cluster has copied its share of the shards it
-// takes GEMM items from the end of the order (rows that arrive last).  The
-// split balances the rounds of tiles: GEMM clusters run ceil(T_c / n_cc)
-// rounds, producer clusters c rounds' worth of copying and then
-// ceil((T - T_c) / n_pc) rounds.  c is estimated from the bytes each producer
-// CTA moves (about 45 GB/s each, measured: 16 CTAs copy the Qwen-32B shards
-// in about 115 us) against the time of one tile (about 12 TFLOP/s per SM);
-// TDG_AG_PROD_ROUNDS overrides it (-1: producers take no items).
-int64_t producer_tail_lo(const AgParams &p, int grid, int TM)
+// takes GEMM items from the end of the order (rows that arrive last).
+// `req` > 0 gives them the last req items, -1 none; 0 balances the rounds of
+// tiles: GEMM clusters run ceil(T_c / n_cc) rounds, producer clusters c
+// rounds' worth of copying and then ceil((T - T_c) / n_pc) rounds, with c
+// estimated from the bytes each producer CTA moves (PROD_BPS) against the
+// time of one tile (TILE_FLOPS per SM).  Returns the first item of the
+// producers' share.
+//
+// PROD_BPS: an SM writes to memory at most about 63 GB/s (TMA bulk stores and
+// plain stores alike, measured on one GB300), so a global -> global copy runs
+// at about 50 GB/s per producer CTA with the default ring; a GEMM CTA
+// computes about 12 TFLOP/s.
+constexpr double PROD_BPS = 48e9;
+constexpr double TILE_FLOPS = 12e12;
+
+// Default producer CTAs in SM mode: enough to copy the shards within the
+// time of the GEMM on every SM (so that the copies stay ahead of the tiles
+// that need them), in whole clusters, 4 .. 32.
+int default_producers(const AgParams &p, int grid, int TM)
+{
+    const double tiles = (double)p.m_tiles * p.n_tiles;
+    const double tile_s = 2.0 * TM * gm::BN * p.K / (p.cl * TILE_FLOPS);
+    const double gemm_s = tiles * tile_s / ((double)grid / p.cl);
+    const double bytes = (double)p.W * p.Ms * p.K * 2.0;
+    int n = (int)ceil(bytes / (gemm_s * PROD_BPS));
+    n = (n + p.cl - 1) / p.cl * p.cl;
+    return n < 4 ? ((4 + p.cl - 1) / p.cl * p.cl) : (n > 32 ? 32 : n);
+}
+int64_t producer_tail_lo(const AgParams &p, int grid, int TM, int req)
 {
     const int64_t T = (int64_t)p.m_tiles * p.n_tiles;
     const int n_pc = p.n_prod / p.cl, n_cc = (grid - p.n_prod) / p.cl;
-    if (n_pc <= 0 || n_cc <= 0)
+    if (n_pc <= 0 || n_cc <= 0 || req < 0)
         return T;
-    int64_t c;
-    if (const char *e = getenv("TDG_AG_PROD_ROUNDS")) {
-        c = atoi(e);
-        if (c < 0)
-            return T;
-    } else {
-        const double copy_s = (double)p.W * p.Ms * p.K * 2.0 / p.n_prod / 45e9;
-        const double tile_s = 2.0 * TM * gm::BN * p.K / (p.cl * 12e12);
-        c = (int64_t)ceil(copy_s / tile_s);
-    }
+    if (req > 0)
+        return req >= T ? 0 : T - req;
+    const double copy_s = (double)p.W * p.Ms * p.K * 2.0 / p.n_prod / PROD_BPS;
+    const double tile_s = 2.0 * TM * gm::BN * p.K / (p.cl * TILE_FLOPS);
+    const int64_t c = (int64_t)ceil(copy_s / tile_s);
     int64_t best_t = 0, best_r = (T + n_cc - 1) / n_cc;
     for (int64_t t = 1; t <= T; ++t) {
         const int64_t rc = (T - t + n_cc - 1) / n_cc;
@@ -538,7 +659,7 @@ int64_t producer_tail_lo(const AgParams &p, int grid, int TM)
     return T - best_t;
 }
 
-int launch_ag(const AgParams &p, int b_layout, int grid, bool coop, cudaStream_t s)
+int launch_ag(const AgParams &p, int b_layout, int grid, bool coop, cudaStream_t s, int split_tail = 0)
 {
     const void *fn = ag_kernel_fn(b_layout, p.cl, p.c_f32 != 0);
     int rc = prepare(fn);
@@ -555,12 +676,11 @@ int launch_ag(const AgParams &p, int b_layout, int grid, bool coop, cudaStream_t
         grid = p.n_prod + (int)(p.cl * units);
     }
     q.split = 0;
-    // opt-in (TDG_SPLIT_TAIL=1): measured slower at the Qwen-32B up-projection
+    // opt-in (split_tail): measured slower at the Qwen-32B up-projection
     // shape, where the half-width tiles move more operand bytes per FLOP and the
     // tail tiles wait on the shard that arrives last anyway.  Not combined with
     // producer clusters that take the last items.
-    const char *st = getenv("TDG_SPLIT_TAIL");
-    if (st && st[0] == '1' && p.tail_lo >= T && units > 0 && T > units && (T % units) > 0 &&
+    if (split_tail && p.tail_lo >= T && units > 0 && T > units && (T % units) > 0 &&
         2 * (T % units) <= units)
         q.split = (int)(T % units);
     if (q.tail_lo >= T)
@@ -597,9 +717,11 @@ extern "C" int tdg_ag_gemm(tdg_symm *h, const tdg_ag_gemm_args *a, void *stream,
     const int64_t Ms = a->Ms, K = a->K, N = a->N, M = (int64_t)W * Ms;
     const size_t c_elem = a->c_f32 ? 4 : 2;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (M == 0 || N == 0)
+    if (M == 0)
         return TDG_OK;
-    if (!a->C || !a->B || !aligned16(a->C) || !aligned16(a->B) || !aligned16(a->a_off) ||
+    // N == 0: the AllGather alone (gathered buffer and flags), no GEMM
+    const bool gemm = N > 0;
+    if ((gemm && (!a->C || !a->B || !aligned16(a->C) || !aligned16(a->B))) || !aligned16(a->a_off) ||
         !aligned16(a->g_off) || (K % 8) != 0 || (N % 8) != 0)
         return TDG_ERR_INVALID;
     if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX)
@@ -610,7 +732,7 @@ extern "C" int tdg_ag_gemm(tdg_symm *h, const tdg_ag_gemm_args *a, void *stream,
     if (a->g_off < a->a_off + shard_bytes && a->a_off < a->g_off + gath_bytes && K > 0)
         return TDG_ERR_INVALID; // the gathered buffer overlaps the shard
     if (K == 0)
-        return cuda_err(cudaMemsetAsync(a->C, 0, (size_t)M * N * c_elem, s), "ag K==0");
+        return gemm ? cuda_err(cudaMemsetAsync(a->C, 0, (size_t)M * N * c_elem, s), "ag K==0") : TDG_OK;
     const bool ll = a->mode == TDG_MODE_LL;
     const uint64_t ll_bytes = (uint64_t)M * K * 4;
     if (ll) {
@@ -624,8 +746,19 @@ extern "C" int tdg_ag_gemm(tdg_symm *h, const tdg_ag_gemm_args *a, void *stream,
     const int BM = gm::BM;
     // CTA pairs (256-row tiles) once there is more than one 128-row tile; two
     // pairs sharing B (512-row tiles) when every shard is a whole number of them
-    const int pair = (pairs_enabled() && M > BM) ? 1 : 0;
-    const int cl = pair ? ((quads_enabled() && Ms % (4 * BM) == 0) ? 4 : 2) : 1;
+    const int cl = pick_cluster(a->cluster, M > BM, Ms % (4 * BM) == 0);
+    const int stages = cl ? pick_stages(a->stages, cl) : 0;
+    if (!cl || !stages || (a->split_tail & ~1) || (a->push & ~1) || a->producer_items < -1 ||
+        a->producer_warps < 0 || a->producer_warps > ag::PMAX_WARPS || a->producer_chunk < 0)
+        return TDG_ERR_INVALID;
+    const int pair = cl >= 2 ? 1 : 0;
+    const int pw = a->producer_warps ? a->producer_warps : ag::DEF_WARPS;
+    const uint32_t pchunk = a->producer_chunk ? (uint32_t)a->producer_chunk : ag::DEF_CHUNK;
+    if (pchunk % 1024 || pchunk < 4096 || pchunk > 65536)
+        return TDG_ERR_INVALID;
+    const int pslots = (int)min((uint32_t)ag::PMAX_SLOTS, (uint32_t)ag::PRING / (uint32_t)pw / pchunk);
+    if (pslots < 3) // at least two loads in flight per worker
+        return TDG_ERR_INVALID;
     const int TM = cl * BM;
     const bool inplace = (Ms % TM) == 0;
     int64_t sig_rows = a->signal_rows;
@@ -643,13 +776,17 @@ extern "C" int tdg_ag_gemm(tdg_symm *h, const tdg_ag_gemm_args *a, void *stream,
 
     AgParams p;
     memset(&p, 0, sizeof p);
-    bool ok = map_bf16_2d(&p.tmA_g, gathered, K, M, K * 2, 64, BM);
-    ok = ok && map_bf16_2d(&p.tmA_l, region_r + a->a_off, K, Ms, K * 2, 64, BM);
-    if (a->b_layout == TDG_B_KN)
-        ok = ok && map_bf16_2d(&p.tmB, a->B, N, K, N * 2, 64, 64);
-    else
-        ok = ok && map_bf16_2d(&p.tmB, a->B, K, N, K * 2, 64, cl == 4 ? 64 : (pair ? 128 : 256));
-    ok = ok && (a->c_f32 ? map_f32_2d(&p.tmC, a->C, N, M, N * 4, 32, 32) : map_bf16_2d(&p.tmC, a->C, N, M, N * 2, 64, 32));
+    bool ok = true;
+    if (gemm) {
+        ok = map_bf16_2d(&p.tmA_g, gathered, K, M, K * 2, 64, BM);
+        ok = ok && map_bf16_2d(&p.tmA_l, region_r + a->a_off, K, Ms, K * 2, 64, BM);
+        if (a->b_layout == TDG_B_KN)
+            ok = ok && map_bf16_2d(&p.tmB, a->B, N, K, N * 2, 64, 64);
+        else
+            ok = ok && map_bf16_2d(&p.tmB, a->B, K, N, K * 2, 64, cl == 4 ? 64 : (pair ? 128 : 256));
+        ok = ok && (a->c_f32 ? map_f32_2d(&p.tmC, a->C, N, M, N * 4, 32, 32)
+                             : map_bf16_2d(&p.tmC, a->C, N, M, N * 2, 64, 32));
+    }
     if (!ok)
         return TDG_ERR_CUDA;
 
@@ -690,6 +827,13 @@ extern "C" int tdg_ag_gemm(tdg_symm *h, const tdg_ag_gemm_args *a, void *stream,
     if (a->source_order != 0 && a->source_order != 1)
         return TDG_ERR_INVALID;
     p.mesh = a->source_order;
+    p.stages = stages;
+    p.push = a->push;
+    p.mirror = a->push && a->swizzle;
+    p.t_end = (int)((((int64_t)rank + 1) * Ms - 1) / TM);
+    p.pw = pw;
+    p.pchunk = pchunk;
+    p.pslots = pslots;
 
     const int sms = h->sm_count;
     const int ggrid = ag_grid(p, a->b_layout, sms); // GEMM-only grid
@@ -711,10 +855,10 @@ extern "C" int tdg_ag_gemm(tdg_symm *h, const tdg_ag_gemm_args *a, void *stream,
         p.n_prod = n_send + n_recv;
         p.wait_flags = 1;
         p.n_units = 0;
-        return launch_ag(p, a->b_layout, ggrid, true, s);
+        return launch_ag(p, a->b_layout, gemm ? ggrid : p.n_prod, true, s, a->split_tail);
     }
     if (a->mode == TDG_MODE_SM) {
-        int nprod = a->producers > 0 ? a->producers : 16;
+        int nprod = a->producers > 0 ? a->producers : default_producers(p, ggrid, TM);
         nprod = (nprod + cl - 1) / cl * cl; // producer CTAs fill whole clusters
         if (nprod >= ggrid)
             return TDG_ERR_INVALID;
@@ -724,13 +868,14 @@ extern "C" int tdg_ag_gemm(tdg_symm *h, const tdg_ag_gemm_args *a, void *stream,
         p.unit_rows = sig_rows;
         p.units_per_shard = Ms / sig_rows;
         p.n_units = (int64_t)W * p.units_per_shard;
-        p.tail_lo = producer_tail_lo(p, ggrid, TM);
-        return launch_ag(p, a->b_layout, ggrid, true, s);
+        p.tail_lo = producer_tail_lo(p, ggrid, TM, a->producer_items);
+        return launch_ag(p, a->b_layout, gemm ? ggrid : nprod, true, s, a->split_tail);
     }
     if (a->mode == TDG_MODE_SERIAL) {
-        // copy phase: every SM copies, fine-grained units, no signals
+        // copy phase: every SM (or `producers` CTAs) copies, fine-grained
+        // units, no signals
         AgParams c = p;
-        c.n_prod = sms;
+        c.n_prod = a->producers > 0 ? (a->producers < sms ? a->producers : sms) : sms;
         c.signal = 0;
         c.wait_flags = 0;
         c.unit_rows = Ms >= 8 ? 8 : Ms;
@@ -741,15 +886,16 @@ extern "C" int tdg_ag_gemm(tdg_symm *h, const tdg_ag_gemm_args *a, void *stream,
         c.local_last = 0;
         c.pair = 0;
         c.cl = 1;
-        int rc = launch_ag(c, a->b_layout, sms, false, s);
-        if (rc != TDG_OK)
+        c.stages = pick_stages(0, 1);
+        int rc = launch_ag(c, a->b_layout, c.n_prod, false, s);
+        if (rc != TDG_OK || !gemm)
             return rc;
         // GEMM phase: stream-ordered after the copy, no waits
         AgParams g = p;
         g.n_prod = 0;
         g.wait_flags = 0;
         g.n_units = 0;
-        return launch_ag(g, a->b_layout, ggrid, false, s);
+        return launch_ag(g, a->b_layout, ggrid, false, s, a->split_tail);
     }
     // CE mode
     cudaStream_t side = static_cast<cudaStream_t>(side_stream);
@@ -766,9 +912,17 @@ extern "C" int tdg_ag_gemm(tdg_symm *h, const tdg_ag_gemm_args *a, void *stream,
         rc = cuda_err(e, "ce events");
     const int64_t ups = Ms / sig_rows;
     for (int64_t u = 0; u < (int64_t)W * ups && rc == TDG_OK; ++u) {
+        // the producers' order (see copy_unit): pull rank+1, rank+2, ...;
+        // push rank-1, rank-2, ..., each shard's groups from its last rows
         const int seq = p.mesh ? (int)(u % W) : (int)(u / ups);
-        const int64_t part = p.mesh ? u / W : u % ups;
-        const int shard = inplace ? (rank + 1 + seq) % W : (rank + seq) % W;
+        int64_t part = p.mesh ? u / W : u % ups;
+        int shard;
+        if (a->push) {
+            shard = ((rank - (inplace ? 1 + seq : seq)) % W + W) % W;
+            part = ups - 1 - part;
+        } else {
+            shard = inplace ? (rank + 1 + seq) % W : (rank + seq) % W;
+        }
         {
             const int64_t row0 = part * sig_rows;
             const int64_t grow = (int64_t)shard * Ms + row0;
@@ -784,12 +938,12 @@ extern "C" int tdg_ag_gemm(tdg_symm *h, const tdg_ag_gemm_args *a, void *stream,
                 rc = TDG_ERR_UNSUPPORTED;
         }
     }
-    if (rc == TDG_OK) {
+    if (rc == TDG_OK && gemm) {
         AgParams g = p;
         g.n_prod = 0;
         g.wait_flags = 1;
         g.n_units = 0;
-        rc = launch_ag(g, a->b_layout, ggrid, false, s);
+        rc = launch_ag(g, a->b_layout, ggrid, false, s, a->split_tail);
     }
     // the call completes on the main stream only when the side stream has too
     e = cudaEventRecord(ev1, side);

@@ -15,6 +15,11 @@
 // m tiles in Triton-distributed's swizzled order (its own shard first, read in place);
 // a tile's loader waits on the groups of its A rows with a bounded
 // ld.acquire spin before its TMA loads.
+// Push mode (CE): the senders order the copies step by step -- at step j
+// every sender s copies its shard to destination (s + j) mod W -- so each
+// destination receives one shard per step from a different sender, and the
+// GEMM follows the steps: each rank's own shard first (step 0), then at step
+// j the shard (r - j) mod W of every rank r.  Pull goes rank by rank.
 // SERIAL mode: the same copies on the main stream, then the GEMM launch,
 // which does not wait.
 #include "tdg_gemm.cuh"
@@ -45,6 +50,8 @@ struct AgAllParams {
     int wait_flags;
     int64_t sig_rows;
     int c_f32; // 1: C_r is fp32
+    int stages; // GEMM ring stages in use
+    int steps;  // 1: push order (items step by step, see tile()); 0: rank by rank
 };
 
 template <int BMN, bool F32 = false> struct AgAllPolicy {
@@ -63,6 +70,21 @@ template <int BMN, bool F32 = false> struct AgAllPolicy {
     {
         const int tm = p.cl * gm::BM;
         const int64_t per_rank = (int64_t)p.m_tiles * p.n_tiles;
+        if (p.steps) {
+            // push order (whole tiles per shard): step j, then rank r, then the
+            // m tiles of shard (r - j) mod W, n inner
+            const int64_t per_shard = (int64_t)p.tiles_per_shard * p.n_tiles;
+            const int64_t per_step = (int64_t)p.W * per_shard;
+            const int j = (int)(item / per_step);
+            const int64_t rem = item % per_step;
+            const int r = (int)(rem / per_shard);
+            const int64_t in = rem % per_shard;
+            const int shard = ((r - j) % p.W + p.W) % p.W;
+            const int pm = shard * p.tiles_per_shard + (int)(in / p.n_tiles);
+            t.pn = (int)(in % p.n_tiles);
+            set_tile(p, t, r, pm, sub, tm);
+            return;
+        }
         const int r = (int)(item / per_rank);
         const int64_t tid = item % per_rank;
         int pm0;
@@ -80,6 +102,12 @@ template <int BMN, bool F32 = false> struct AgAllPolicy {
         }
         // Triton-distributed's swizzle: pid_m = (pid_m + rank * tiles_per_pe) % total
         const int pm = (pm0 + (int)(((int64_t)r * p.Ms / tm) % p.m_tiles)) % p.m_tiles;
+        set_tile(p, t, r, pm, sub, tm);
+    }
+
+    // the rest of tile (r, pm, t.pn): rows, columns, A source
+    __device__ static void set_tile(const Params &p, TileInfo &t, int r, int pm, int sub, int tm)
+    {
         t.m0 = pm * tm + sub * gm::BM;
         t.n0 = t.pn * gm::BN;
         t.n_valid = (int)min((int64_t)gm::BN, p.N - t.n0);
@@ -259,8 +287,11 @@ extern "C" int tdg_ag_gemm_all_ranks(tdg_symm *h, const tdg_ag_gemm_all_args *a,
     }
 
     const int BM = gm::BM;
-    const int pair = (pairs_enabled() && M > BM) ? 1 : 0;
-    const int cl = pair ? ((quads_enabled() && Ms % (4 * BM) == 0) ? 4 : 2) : 1;
+    const int cl = pick_cluster(a->cluster, M > BM, Ms % (4 * BM) == 0);
+    const int stages = cl ? pick_stages(a->stages, cl) : 0;
+    if (!cl || !stages || (a->push & ~1))
+        return TDG_ERR_INVALID;
+    const int pair = cl >= 2 ? 1 : 0;
     const int TM = cl * BM;
     const bool inplace = (Ms % TM) == 0;
     int64_t sig_rows = a->signal_rows > 0 ? a->signal_rows : Ms;
@@ -305,6 +336,10 @@ extern "C" int tdg_ag_gemm_all_ranks(tdg_symm *h, const tdg_ag_gemm_all_args *a,
     p.nsig = h->nsig;
     p.sig_rows = sig_rows;
     p.c_f32 = a->c_f32;
+    p.stages = stages;
+    // the GEMM follows the push steps when every shard is whole tiles (else it
+    // keeps the rank-by-rank order: the same result, only the waits differ)
+    p.steps = (a->push && a->mode == TDG_MODE_CE && inplace) ? 1 : 0;
 
     const void *fn = ag_all_kernel_fn(a->b_layout, cl, a->c_f32 != 0);
     if (cudaError_t e = set_smem(fn, gm::SMEM_BYTES); e != cudaSuccess)
@@ -321,30 +356,44 @@ extern "C" int tdg_ag_gemm_all_ranks(tdg_symm *h, const tdg_ag_gemm_all_args *a,
     if (grid / cl > items)
         grid = (int)(cl * items);
 
-    // the copies: rank r's remote shards r+1, r+2, ... (its own shard last when
-    // it is read in place, else first), one signal group per copy
-    auto copies = [&](cudaStream_t cs, bool signal) -> int {
+    // One shard copy: shard `shard` into rank r's gathered buffer, one signal
+    // group per copy, each followed by rank r's flag for it.
+    auto copy_shard = [&](cudaStream_t cs, bool signal, int r, int shard) -> int {
         const int64_t ups = Ms / sig_rows;
-        for (int r = 0; r < W; ++r) {
-            uint8_t *gathered = h->base + (size_t)r * R + a->g_off;
-            uint32_t *fl = h->flags + (size_t)r * h->nsig;
-            for (int j = 0; j < W; ++j) {
-                const int shard = inplace ? (r + 1 + j) % W : (r + j) % W;
-                for (int64_t part = 0; part < ups; ++part) {
-                    const int64_t row0 = part * sig_rows, grow = (int64_t)shard * Ms + row0;
-                    const uint8_t *src = h->base + (size_t)shard * R + a->a_off + (size_t)row0 * K * 2;
-                    cudaError_t e = cudaMemcpyAsync(gathered + (size_t)grow * K * 2, src,
-                                                    (size_t)sig_rows * K * 2, cudaMemcpyDeviceToDevice, cs);
-                    if (e != cudaSuccess)
-                        return cuda_err(e, "ag all memcpy");
-                    const int64_t g = grow / sig_rows;
-                    const bool skip = r == 0 && ((a->test_skip_notify >> (g & 63)) & 1ull);
-                    if (signal && !skip && !stream_write_u32(cs, fl + g, epoch))
-                        return TDG_ERR_UNSUPPORTED;
-                }
-            }
+        uint8_t *gathered = h->base + (size_t)r * R + a->g_off;
+        uint32_t *fl = h->flags + (size_t)r * h->nsig;
+        for (int64_t part = 0; part < ups; ++part) {
+            const int64_t row0 = part * sig_rows, grow = (int64_t)shard * Ms + row0;
+            const uint8_t *src = h->base + (size_t)shard * R + a->a_off + (size_t)row0 * K * 2;
+            cudaError_t e = cudaMemcpyAsync(gathered + (size_t)grow * K * 2, src, (size_t)sig_rows * K * 2,
+                                            cudaMemcpyDeviceToDevice, cs);
+            if (e != cudaSuccess)
+                return cuda_err(e, "ag all memcpy");
+            const int64_t g = grow / sig_rows;
+            const bool skip = r == 0 && ((a->test_skip_notify >> (g & 63)) & 1ull);
+            if (signal && !skip && !stream_write_u32(cs, fl + g, epoch))
+                return TDG_ERR_UNSUPPORTED;
         }
         return TDG_OK;
+    };
+    // Pull: rank by rank, rank r's remote shards r+1, r+2, ... (its own shard
+    // last when it is read in place, else first).  Push: step by step, sender
+    // s to destination (s + j) mod W at step j (the own shards as step 0: last
+    // when read in place, else first).
+    auto copies = [&](cudaStream_t cs, bool signal) -> int {
+        int rc = TDG_OK;
+        if (!a->push) {
+            for (int r = 0; r < W && rc == TDG_OK; ++r)
+                for (int j = 0; j < W && rc == TDG_OK; ++j)
+                    rc = copy_shard(cs, signal, r, inplace ? (r + 1 + j) % W : (r + j) % W);
+            return rc;
+        }
+        for (int jj = 0; jj < W && rc == TDG_OK; ++jj) {
+            const int j = inplace ? (jj + 1) % W : jj;
+            for (int snd = 0; snd < W && rc == TDG_OK; ++snd)
+                rc = copy_shard(cs, signal, (snd + j) % W, snd);
+        }
+        return rc;
     };
     void *args[] = {&p};
     if (a->mode == TDG_MODE_SERIAL) {

@@ -100,7 +100,7 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p)
 
 // Policy P provides:
 //   struct Params { ... DevStatus *status; uint32_t epoch; uint64_t timeout_ns, pipe_timeout_ns;
-//                   int k_blocks; };
+//                   int k_blocks; int stages; };   (stages: ring stages in use, 2 .. Shape::STAGES)
 //   static constexpr int B_MN;                                   // 1: B is K x N
 //   __device__ static int64_t num_items(const Params&);
 //   __device__ static void tile(const Params&, int64_t item, TileInfo&, int sub);
@@ -148,6 +148,8 @@ __device__ void gemm_consumer(const typename P::Params &p, uint8_t *smem, int un
     const uint16_t pair_mask = (uint16_t)(3u << (2 * pidx));
     const uint16_t empty_mask = QUAD ? (uint16_t)0xF : pair_mask;
     PipeSmem *ps = reinterpret_cast<PipeSmem *>(smem + OFF_BAR);
+    // ring stages in use (the host checks the range; the ring holds S::STAGES)
+    const int NST = (p.stages >= 2 && p.stages < S::STAGES) ? p.stages : S::STAGES;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < S::STAGES; ++i) {
@@ -217,7 +219,7 @@ __device__ void gemm_consumer(const typename P::Params &p, uint8_t *smem, int un
                     P::template load_a<CL>(p, ti, sa, bar, kb);
                     P::template load_b<CL>(p, ti, sa + A_BYTES, bar, kb, col0, cols, pidx, half);
                     ++issued;
-                    if (++stage == S::STAGES) {
+                    if (++stage == NST) {
                         stage = 0;
                         phase ^= 1u;
                     }
@@ -279,7 +281,7 @@ __device__ void gemm_consumer(const typename P::Params &p, uint8_t *smem, int un
                     else
                         umma_commit(&ps->empty[stage]);
                     ++consumed;
-                    if (++stage == S::STAGES) {
+                    if (++stage == NST) {
                         stage = 0;
                         phase ^= 1u;
                     }
@@ -415,12 +417,12 @@ __device__ void gemm_consumer(const typename P::Params &p, uint8_t *smem, int un
         // wait (bounded) until no TMA write of this CTA is still in flight.
         if (!PAIR || leader) {
             for (uint32_t f = ps->consumed; f < ps->issued; ++f)
-                (void)mbar_wait(&ps->full[f % S::STAGES], (f / S::STAGES) & 1u, tmo);
+                (void)mbar_wait(&ps->full[f % NST], (f / NST) & 1u, tmo);
         } else {
             // a peer's fill is known done once the leader has freed its slot
-            for (uint32_t f = ps->issued > (uint32_t)S::STAGES ? ps->issued - S::STAGES : 0u;
+            for (uint32_t f = ps->issued > (uint32_t)NST ? ps->issued - NST : 0u;
                  f < ps->issued; ++f)
-                (void)mbar_wait(&ps->empty[f % S::STAGES], (f / S::STAGES) & 1u, tmo);
+                (void)mbar_wait(&ps->empty[f % NST], (f / NST) & 1u, tmo);
         }
     }
     __syncthreads();

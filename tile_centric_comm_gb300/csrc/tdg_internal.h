@@ -101,18 +101,30 @@ cudaError_t launch(const void *fn, dim3 grid, dim3 block, size_t smem, cudaStrea
 // Number of `cl`-CTA clusters of `fn` that can be resident at once (0 on error).
 int max_clusters(const void *fn, int block, int smem, int cl);
 
-// CTA pairs (cta_group::2) unless TDG_PAIR=0 is set in the environment.
-inline bool pairs_enabled()
+// The GEMM cluster shape of a call: `req` (0 = the default, the largest the
+// shape allows) against what the shape allows -- allow2: CTA pairs
+// (cta_group::2), allow4: clusters of two pairs sharing B.  Returns 1, 2 or 4,
+// or 0 when the request is not allowed.
+inline int pick_cluster(int req, bool allow2, bool allow4)
 {
-    const char *e = getenv("TDG_PAIR");
-    return !(e && e[0] == '0');
+    allow4 = allow4 && allow2;
+    switch (req) {
+    case 0: return allow4 ? 4 : (allow2 ? 2 : 1);
+    case 1: return 1;
+    case 2: return allow2 ? 2 : 0;
+    case 4: return allow4 ? 4 : 0;
+    default: return 0;
+    }
 }
 
-// Clusters of two CTA pairs sharing B by multicast, unless TDG_QUAD=0.
-inline bool quads_enabled()
+// Operand ring stages of the GEMM: `req` (0 = all that fit the ring: 4 of
+// 48 KB with one CTA per tile, 6 of 32 KB with pairs), or 0 when out of range.
+inline int pick_stages(int req, int cl)
 {
-    const char *e = getenv("TDG_QUAD");
-    return !(e && e[0] == '0');
+    const int mx = cl == 1 ? 4 : 6;
+    if (req == 0)
+        return mx;
+    return (req >= 2 && req <= mx) ? req : 0;
 }
 
 inline int cuda_err(cudaError_t e, const char *what)

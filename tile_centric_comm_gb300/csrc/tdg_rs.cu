@@ -51,6 +51,7 @@ struct RsParams {
     uint64_t nsig;
     int f32; // 1: partials are pushed as fp32, 0: as bf16
     int red_rows; // rows of owed reductions an epilogue warp works off per tile
+    int stages;   // GEMM ring stages in use
 };
 
 __device__ __forceinline__ uint8_t *rs_stage_row(const RsParams &p, int o, int r, int m_loc, int pn, int row)
@@ -421,8 +422,12 @@ extern "C" int tdg_gemm_rs(tdg_symm *h, const tdg_gemm_rs_args *a, void *stream)
 
     // CTA pairs when every owner holds whole 256-row tiles; two pairs sharing
     // B when it holds whole 512-row tiles
-    const int pair = (pairs_enabled() && Mo % (2 * gm::BM) == 0) ? 1 : 0;
-    const int cl = pair ? ((quads_enabled() && Mo % (4 * gm::BM) == 0) ? 4 : 2) : 1;
+    const int cl = pick_cluster(a->cluster, Mo % (2 * gm::BM) == 0, Mo % (4 * gm::BM) == 0);
+    const int stages = cl ? pick_stages(a->stages, cl) : 0;
+    if (!cl || !stages || (a->order & ~1) ||
+        (a->red_rows != 0 && (a->red_rows < 4 || a->red_rows > 32 || 32 % a->red_rows)))
+        return TDG_ERR_INVALID;
+    const int pair = cl >= 2 ? 1 : 0;
     RsParams p;
     memset(&p, 0, sizeof p);
     bool ok = map_bf16_3d(&p.tmA, h->base + a->a_off, K, M, W, K * 2, R, 64, gm::BM, 1);
@@ -453,7 +458,8 @@ extern "C" int tdg_gemm_rs(tdg_symm *h, const tdg_gemm_rs_args *a, void *stream)
     p.cl = cl;
     p.mtp = mt / cl;
     p.n_tiles = n_tiles;
-    p.order = getenv("TDG_RS_ORDER") ? atoi(getenv("TDG_RS_ORDER")) : 0;
+    p.order = a->order;
+    p.stages = stages;
     // two owners per block measured best at the Qwen-32B down-projection shape
     // (B_r streamed W/2 times instead of W; partials of a block stay L2-warm)
     if (a->owner_block < 0 || (a->owner_block > 0 && W % a->owner_block))
@@ -470,12 +476,7 @@ extern "C" int tdg_gemm_rs(tdg_symm *h, const tdg_gemm_rs_args *a, void *stream)
     // measured at the Qwen-32B down-projection shape: a bf16 quarter's
     // reduction fits in the slack of one tile, so it is done at once; an fp32
     // one (twice the bytes) goes fastest in slices of 8 rows per tile
-    p.red_rows = f32 ? 8 : 32;
-    if (const char *rr = getenv("TDG_RS_RED_ROWS")) {
-        const int v = atoi(rr);
-        if (v >= 4 && v <= 32 && 32 % v == 0)
-            p.red_rows = v;
-    }
+    p.red_rows = a->red_rows ? a->red_rows : (f32 ? 8 : 32);
 
     const void *fn;
     if (a->b_layout == TDG_B_KN)

@@ -53,21 +53,26 @@ class AgGemmArgs(ctypes.Structure):
                 ("b_layout", ctypes.c_int), ("mode", ctypes.c_int), ("producers", ctypes.c_int),
                 ("signal_rows", _i64), ("swizzle", ctypes.c_int), ("timeout_ns", _u64),
                 ("ll_off", _sz), ("test_skip_notify", _u64), ("source_order", ctypes.c_int),
-                ("c_f32", ctypes.c_int)]
+                ("c_f32", ctypes.c_int), ("cluster", ctypes.c_int), ("stages", ctypes.c_int),
+                ("split_tail", ctypes.c_int), ("producer_items", ctypes.c_int),
+                ("producer_warps", ctypes.c_int), ("producer_chunk", ctypes.c_int),
+                ("push", ctypes.c_int)]
 
 
 class AgGemmAllArgs(ctypes.Structure):
     _fields_ = [("world", ctypes.c_int), ("Ms", _i64), ("K", _i64), ("N", _i64), ("a_off", _sz),
                 ("g_off", _sz), ("b_off", _sz), ("c_off", _sz), ("b_layout", ctypes.c_int),
                 ("mode", ctypes.c_int), ("signal_rows", _i64), ("timeout_ns", _u64),
-                ("test_skip_notify", _u64), ("c_f32", ctypes.c_int)]
+                ("test_skip_notify", _u64), ("c_f32", ctypes.c_int), ("cluster", ctypes.c_int),
+                ("stages", ctypes.c_int), ("push", ctypes.c_int)]
 
 
 class GemmRsArgs(ctypes.Structure):
     _fields_ = [("world", ctypes.c_int), ("M", _i64), ("K", _i64), ("N", _i64), ("a_off", _sz),
                 ("b_off", _sz), ("stage_off", _sz), ("out_off", _sz), ("b_layout", ctypes.c_int),
                 ("mode", ctypes.c_int), ("timeout_ns", _u64), ("owner_block", ctypes.c_int),
-                ("partial_f32", ctypes.c_int)]
+                ("partial_f32", ctypes.c_int), ("cluster", ctypes.c_int), ("stages", ctypes.c_int),
+                ("order", ctypes.c_int), ("red_rows", ctypes.c_int)]
 
 
 class MoeArgs(ctypes.Structure):
@@ -282,31 +287,43 @@ class Symm:
 def ag_gemm(symm: Symm, rank: int, Ms: int, K: int, N: int, a_off: int, g_off: int, B, C,
             mode="sm", b_layout=B_KN, producers=0, signal_rows=0, swizzle=True,
             timeout_ns=0, ll_off=0, test_skip_notify=0, source_order=0, stream=None,
-            side_stream=None, c_f32=False):
-    """c_f32: C is float32 (the fp32 accumulator, unrounded) instead of bf16."""
+            side_stream=None, c_f32=False, cluster=0, stages=0, split_tail=False,
+            producer_items=0, producer_warps=0, producer_chunk=0, push=False):
+    """c_f32: C is float32 (the fp32 accumulator, unrounded) instead of bf16.
+    cluster / stages / split_tail / producer_items / producer_warps /
+    producer_chunk / push choose the schedule (0 / False: the default for the
+    shape); see tdg_ag_gemm_args in include/tdg.h."""
     import torch
     dev = symm.buf.device
+    # N == 0 runs the AllGather alone: B and C may then be None
     a = AgGemmArgs(world=symm.world, rank=rank, Ms=Ms, K=K, N=N, a_off=a_off, g_off=g_off,
-                   B=_tensor(B, "B", torch.bfloat16, K * N, dev),
-                   C=_tensor(C, "C", torch.float32 if c_f32 else torch.bfloat16, symm.world * Ms * N, dev),
+                   B=None if (N == 0 and B is None) else _tensor(B, "B", torch.bfloat16, K * N, dev),
+                   C=None if (N == 0 and C is None) else
+                   _tensor(C, "C", torch.float32 if c_f32 else torch.bfloat16, symm.world * Ms * N, dev),
                    b_layout=b_layout, mode=MODES[mode],
                    producers=producers, signal_rows=signal_rows, swizzle=1 if swizzle else 0,
                    timeout_ns=timeout_ns, ll_off=ll_off, test_skip_notify=test_skip_notify,
-                   source_order=source_order, c_f32=1 if c_f32 else 0)
+                   source_order=source_order, c_f32=1 if c_f32 else 0, cluster=cluster,
+                   stages=stages, split_tail=1 if split_tail else 0, producer_items=producer_items,
+                   producer_warps=producer_warps, producer_chunk=producer_chunk,
+                   push=1 if push else 0)
     side = _vp(side_stream.cuda_stream) if side_stream is not None else _vp(None)
     _check(lib().tdg_ag_gemm(symm.h, ctypes.byref(a), _stream(stream), side), "tdg_ag_gemm")
 
 
 def ag_gemm_all_ranks(symm: Symm, Ms: int, K: int, N: int, a_off: int, g_off: int, b_off: int,
                       c_off: int, mode="ce", b_layout=B_KN, signal_rows=0, timeout_ns=0,
-                      test_skip_notify=0, stream=None, side_stream=None, c_f32=False):
+                      test_skip_notify=0, stream=None, side_stream=None, c_f32=False,
+                      cluster=0, stages=0, push=False):
     """AllGather+GEMM of every rank in one call: C_r = concat(A_0..A_{W-1}) @ B_r,
     with A_r, the gathered buffers, B_r and C_r all in the heap (offsets).
-    c_f32: C_r is float32 (the fp32 accumulator, unrounded) instead of bf16."""
+    c_f32: C_r is float32 (the fp32 accumulator, unrounded) instead of bf16.
+    push: the copies go step by step, sender s to destination (s + j) mod W."""
     a = AgGemmAllArgs(world=symm.world, Ms=Ms, K=K, N=N, a_off=a_off, g_off=g_off, b_off=b_off,
                       c_off=c_off, b_layout=b_layout, mode=MODES[mode], signal_rows=signal_rows,
                       timeout_ns=timeout_ns, test_skip_notify=test_skip_notify,
-                      c_f32=1 if c_f32 else 0)
+                      c_f32=1 if c_f32 else 0, cluster=cluster, stages=stages,
+                      push=1 if push else 0)
     side = _vp(side_stream.cuda_stream) if side_stream is not None else _vp(None)
     _check(lib().tdg_ag_gemm_all_ranks(symm.h, ctypes.byref(a), _stream(stream), side),
            "tdg_ag_gemm_all_ranks")
@@ -318,13 +335,15 @@ def gemm_rs_stage_bytes(world: int, M: int, N: int) -> int:
 
 def gemm_rs(symm: Symm, M: int, K: int, N: int, a_off: int, b_off: int, stage_off: int,
             out_off: int, mode="sm", b_layout=B_KN, timeout_ns=0, owner_block=0,
-            partial_f32=False, stream=None):
+            partial_f32=False, stream=None, cluster=0, stages=0, order=0, red_rows=0):
     """partial_f32: push fp32 partials (the staging area must then hold
-    2 * gemm_rs_stage_bytes(world, M, N) bytes)."""
+    2 * gemm_rs_stage_bytes(world, M, N) bytes).  cluster / stages / order /
+    red_rows / owner_block choose the schedule (0: the default for the shape)."""
     a = GemmRsArgs(world=symm.world, M=M, K=K, N=N, a_off=a_off, b_off=b_off,
                    stage_off=stage_off, out_off=out_off, b_layout=b_layout,
                    mode=MODES[mode], timeout_ns=timeout_ns, owner_block=owner_block,
-                   partial_f32=1 if partial_f32 else 0)
+                   partial_f32=1 if partial_f32 else 0, cluster=cluster, stages=stages,
+                   order=order, red_rows=red_rows)
     _check(lib().tdg_gemm_rs(symm.h, ctypes.byref(a), _stream(stream)), "tdg_gemm_rs")
 
 
