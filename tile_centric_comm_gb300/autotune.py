@@ -66,12 +66,23 @@ def time_candidate(run: Callable[[dict], None], cfg: dict, warmup: int = 2, iter
 
 
 def tune(key: tuple, candidates: List[dict], run: Callable[[dict], None], group=None,
-         warmup: int = 2, iters: int = 5, flush=None, use_cache: bool = True) -> Tuple[dict, List[dict]]:
+         warmup: int = 2, iters: int = 5, flush=None, use_cache: bool = True,
+         rounds: int = 3) -> Tuple[dict, List[dict]]:
     """Time every candidate, agree on the best across ranks, cache it.
-    Returns (best config, table of {cfg, ms})."""
+    The candidates are timed in `rounds` rounds, the order rotated every
+    round, and each keeps the median of its rounds: a GPU's clock drifts over
+    a long run (the power cap), which would otherwise favour whichever
+    candidate runs first.  Returns (best config, table of {cfg, ms})."""
     if use_cache and key in _cache:
         return _cache[key], []
-    times = [time_candidate(run, c, warmup, iters, flush) for c in candidates]
+    per = [[] for _ in candidates]
+    n = len(candidates)
+    for r in range(max(1, rounds)):
+        start = (r * n) // max(1, rounds)
+        for j in range(n):
+            i = (start + j) % n
+            per[i].append(time_candidate(run, candidates[i], warmup if r == 0 else 1, iters, flush))
+    times = [statistics.median(t) for t in per]
     best, combined = choose(times, group)
     table = [dict(cfg=c, ms=t) for c, t in zip(candidates, combined)]
     _cache[key] = candidates[best]

@@ -878,7 +878,14 @@ extern "C" int tdg_ag_gemm(tdg_symm *h, const tdg_ag_gemm_args *a, void *stream,
         c.n_prod = a->producers > 0 ? (a->producers < sms ? a->producers : sms) : sms;
         c.signal = 0;
         c.wait_flags = 0;
-        c.unit_rows = Ms >= 8 ? 8 : Ms;
+        // units of a few rows, about 4 per copy worker (the workers stream
+        // their units back to back, so small units cost nothing but balance
+        // the load)
+        const int64_t workers = (int64_t)c.n_prod * c.pw;
+        c.unit_rows = M / (4 * workers);
+        c.unit_rows = c.unit_rows < 1 ? 1 : (c.unit_rows > 64 ? 64 : c.unit_rows);
+        if (c.unit_rows > Ms)
+            c.unit_rows = Ms;
         while (Ms % c.unit_rows)
             c.unit_rows--;
         c.units_per_shard = Ms / c.unit_rows;
