@@ -49,9 +49,9 @@ WORKLOAD = ("qwen32b_mlp_tp8: AG-GEMM up-proj (W=8, A_r 1024x5120, B 5120x3200) 
 
 
 # DRAM traffic of one rs_gemm_kernel launch at this workload, dram__bytes_read.sum +
-# dram__bytes_write.sum from one ncu capture (2.367 GB read + 0.741 GB written).  It is
+# dram__bytes_write.sum from one ncu capture (2.447 GB read + 0.741 GB written).  It is
 # reported only while the kernel's sources still hash to the value the capture was taken with.
-RS_TRAFFIC = {"sources": "8c1a6840926fe0d0", "bytes": 2_366_814_720 + 740_667_904}
+RS_TRAFFIC = {"sources": "f4f8c37dddcead5e", "bytes": 2_447_496_192 + 741_324_288}
 RS_SOURCES = ["tdg_gemm.cuh", "tdg_rs.cu", "tdg_ptx.cuh"]
 
 
@@ -79,7 +79,8 @@ def parse():
     ap.add_argument("--no-extras", action="store_true", help="skip serial/e2e/MoE/CPU legs")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--only", default="", help="measure one operation alone, not the bench line: "
-                    "ag, rs, moe, ring, flash or ag_all (the AG-GEMM of all ranks in one call); "
+                    "ag, rs, moe, ring, flash, ag_all (the AG-GEMM of all ranks in one call) or copy "
+                    "(the AllGather alone, SERIAL copy launch on --producers CTAs or --mode ce); "
                     "'library' times torch.matmul (cuBLAS) on the AG GEMM shape as context")
     ap.add_argument("--ag-shape", default="", help="W,Ms,K,N for --only ag|library, e.g. 8,2048,8192,7168 "
                     "(the Llama-3-70B gate+up shape)")
@@ -979,6 +980,36 @@ def main():
                               "roofline": {"bound": "tensor", "achieved": res[f"{key}_tflops"], "peak": pk["bf16"],
                                            "unit": "TFLOP/s", "frac": res[f"{key}_tflops"] / pk["bf16"]},
                               "clocks": clk.summary(), "detail": res}), flush=True)
+        return
+    if args.only == "copy":
+        # the AllGather alone (N = 0): the SERIAL copy launch on --producers CTAs
+        # (0 = every SM), or the copy engine with --mode ce
+        W, Ms, K = AG["W"], AG["Ms"], AG["K"]
+        g_off = _align(Ms * K * 2)
+        sym = tdg.Symm(W, _align(g_off + W * Ms * K * 2 + 1024), 65536)
+        gen = torch.Generator(device="cuda")
+        gen.manual_seed(0)
+        for r in range(W):
+            sym.view(r, 0, (Ms, K), torch.bfloat16).copy_(torch.randn(Ms, K, device="cuda", generator=gen))
+        side = torch.cuda.Stream()
+        mode = "ce" if args.mode == "ce" else "serial"
+        with Clocks(local) as clk:
+            cp = timed_steps(torch, [lambda: tdg.ag_gemm(sym, 0, Ms, K, 0, 0, g_off, None, None, mode=mode,
+                                                         producers=args.producers,
+                                                         side_stream=side if mode == "ce" else None)],
+                             args.steps, args.warmup, flush)
+        ms = statistics.mean(cp[0])
+        moved = W * Ms * K * 2
+        if sym.status()["code"] != 0:
+            raise RuntimeError(f"device fault in the AllGather alone: {sym.status()}")
+        ctas = args.producers or sms
+        print(json.dumps({"metric": f"AllGather alone GB/s moved ({mode})", "value": moved / ms / 1e6,
+                          "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+                          "per_cta_gbs": moved / ms / 1e6 / ctas if mode == "serial" else None,
+                          "roofline": {"bound": "hbm", "achieved": 2 * moved / ms / 1e6, "peak": pk["hbm"],
+                                       "unit": "GB/s", "frac": 2 * moved / ms / 1e6 / pk["hbm"],
+                                       "what": "read + write bytes"},
+                          "clocks": clk.summary()}), flush=True)
         return
     if args.only in ("moe", "ring", "flash"):
         leg = {"moe": leg_moe, "ring": leg_ring, "flash": leg_flash}[args.only]
