@@ -206,7 +206,7 @@ __device__ void gemm_consumer(const typename P::Params &p, uint8_t *smem, int un
                 const int col0 = ti.n0 + (PAIR ? half * cols : 0);
                 const uint32_t my_bytes = A_BYTES + P::b_bytes(p, ti, cols);
                 for (int kb = 0; kb < p.k_blocks; ++kb) {
-                    if (!mbar_wait(&ps->empty[stage], phase ^ 1u, tmo)) {
+                    if (!mbar_wait_sleep(&ps->empty[stage], phase ^ 1u, tmo, 64)) {
                         report_fault(p.status, TDG_ERR_TIMEOUT, TDG_WHERE_PIPE, 0, p.epoch);
                         ps->abort = 1;
                         break;
@@ -332,7 +332,7 @@ __device__ void gemm_consumer(const typename P::Params &p, uint8_t *smem, int un
             // memory probes while the mainloop runs)
             bool ok = true;
             if (lane == 0)
-                ok = mbar_wait(&ps->tfull[acc], acc_phase, tmo);
+                ok = mbar_wait_sleep(&ps->tfull[acc], acc_phase, tmo, 256);
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
             if (!ok || ps->abort) {
                 if (lane == 0 && !ok)

@@ -103,6 +103,26 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64
     }
 }
 
+// The same wait with a back-off sleep of `ns` between polls, for roles that
+// can wait a little longer (the GEMM's loader when its ring is full, the
+// epilogue between tiles): fewer issue slots taken from the warps that share
+// their scheduler (the MMA issuer).
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t *bar, uint32_t parity, uint64_t timeout_ns,
+                                                uint32_t ns)
+{
+    const uint32_t a = smem_u32(bar);
+    if (mbar_try_wait(a, parity))
+        return true;
+    const uint64_t t0 = globaltimer();
+    while (true) {
+        __nanosleep(ns);
+        if (mbar_try_wait(a, parity))
+            return true;
+        if (globaltimer() - t0 > timeout_ns)
+            return false;
+    }
+}
+
 // --------------------------------------------------------------- fences ----
 // Order this thread's generic-proxy accesses with async-proxy (TMA) accesses.
 __device__ __forceinline__ void fence_proxy_async_global()
