@@ -212,3 +212,76 @@ def test_flash_decode_random_shapes(W, B, Hq, Hkv, S, chunk, seed):
     ref = oracle.attention_decode(case.q, case.full(case.k), case.full(case.v))
     for _ in range(2):
         assert_close(case.run(), ref)
+
+
+def _schedule_cases(n=16, seed=2031):
+    """Random shapes with a random schedule drawn from what each shape allows:
+    push or pull, one source at a time or all at once, GEMM cluster shape,
+    ring stages, producer count and copy-ring shape."""
+    g = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        W = int(g.choice([1, 2, 3, 4, 8]))
+        Ms = int(g.choice([64, 96, 256, 512, 1024]))
+        while W * Ms > 4096:
+            Ms //= 2
+        K = int(g.choice([8, 72, 136, 520]))
+        N = int(g.choice([8, 136, 264, 520]))
+        M = W * Ms
+        clusters = [1] + ([2] if M > 128 else []) + ([4] if Ms % 512 == 0 else [])
+        cl = int(g.choice(clusters))
+        st = int(g.integers(2, (4 if cl == 1 else 6) + 1))
+        warps = int(g.integers(1, 5))
+        chunk = int(g.choice([4096, 8192, 16384, 32768]))
+        while (196608 // warps) // chunk < 3:
+            chunk //= 2
+        sched = dict(push=bool(g.integers(0, 2)), source_order=int(g.integers(0, 2)), cluster=cl, stages=st,
+                     producers=int(g.choice([0, 4, 8])), producer_warps=warps, producer_chunk=chunk,
+                     producer_items=int(g.choice([0, -1, 2])))
+        out.append((W, Ms, K, N, int(g.integers(0, 2)), 6000 + i, sched))
+    return out
+
+
+@pytest.mark.parametrize("W,Ms,K,N,lay,seed,sched", _schedule_cases())
+def test_ag_random_schedules_bit_exact(W, Ms, K, N, lay, seed, sched):
+    inp = synth.ag_inputs(W, Ms, K, N, "int2", seed=seed)
+    _, C16 = oracle.ag_gemm(inp.shards, inp.B)
+    case = AGCase(inp, b_layout=tdg.B_KN if lay == 0 else tdg.B_NK)
+    rank = seed % W
+    for mode in ("sm", "ce", "serial"):
+        kw = dict(sched)
+        if mode != "sm":
+            kw.pop("producer_items")
+        got, _ = case.run(rank=rank, mode=mode, **kw)
+        assert np.array_equal(got, C16), (mode, sched)
+        assert np.array_equal(to_bits(case.gathered(rank)), np.concatenate(inp.shards)), (mode, "gathered")
+
+
+def _rs_schedule_cases(n=10, seed=2032):
+    g = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        W = int(g.choice([1, 2, 4, 8]))
+        Mo = int(g.choice([128, 256, 512, 1024]))
+        while W * Mo > 4096:
+            Mo //= 2
+        K = int(g.choice([8, 64]))
+        N = int(g.choice([8, 264, 520]))
+        clusters = [1] + ([2] if Mo % 256 == 0 else []) + ([4] if Mo % 512 == 0 else [])
+        cl = int(g.choice(clusters))
+        obs = [d for d in range(1, W + 1) if W % d == 0]
+        sched = dict(cluster=cl, stages=int(g.integers(2, (4 if cl == 1 else 6) + 1)),
+                     order=int(g.integers(0, 2)), owner_block=int(g.choice(obs)),
+                     red_rows=int(g.choice([4, 8, 16, 32])), partial_f32=bool(g.integers(0, 2)))
+        out.append((W, W * Mo, K, N, 7000 + i, sched))
+    return out
+
+
+@pytest.mark.parametrize("W,M,K,N,seed,sched", _rs_schedule_cases())
+def test_rs_random_schedules_bit_exact(W, M, K, N, seed, sched):
+    inp = synth.rs_inputs(W, M, K, N, "int2", seed=seed)
+    _, out16 = oracle.gemm_rs(inp.As, inp.Bs)
+    case = RSCase(inp, f32=sched["partial_f32"])
+    for mode in ("sm", "serial"):
+        got, _ = case.run(mode=mode, **sched)
+        assert np.array_equal(got, out16), (mode, sched)
