@@ -100,6 +100,7 @@ struct AgParams {
     int pw;           // copy workers per producer CTA
     uint32_t pchunk;  // bytes per bulk copy
     int pslots;       // ring slots per worker
+    int full_n;       // N is a multiple of BN and no tile is split: every tile is full width
 };
 
 template <int BMN, bool F32 = false> struct AgPolicy {
@@ -685,6 +686,7 @@ int launch_ag(const AgParams &p, int b_layout, int grid, bool coop, cudaStream_t
         q.split = (int)(T % units);
     if (q.tail_lo >= T)
         q.tail_lo = T + q.split; // every item goes to the GEMM CTAs
+    q.full_n = (p.N % gm::BN) == 0 && q.split == 0 ? 1 : 0;
     void *args[] = {&q};
     cudaError_t e = launch(fn, dim3(grid), dim3(gm::NUM_THREADS), gm::SMEM_BYTES, s, args, coop, p.cl);
     if (e != cudaSuccess && coop && p.cl > 1) {

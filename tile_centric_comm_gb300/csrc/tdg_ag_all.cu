@@ -51,6 +51,7 @@ struct AgAllParams {
     int64_t sig_rows;
     int c_f32; // 1: C_r is fp32
     int stages; // GEMM ring stages in use
+    int full_n; // N is a multiple of BN: every tile is full width
     int steps;  // 1: push order (items step by step, see tile()); 0: rank by rank
 };
 
@@ -337,6 +338,7 @@ extern "C" int tdg_ag_gemm_all_ranks(tdg_symm *h, const tdg_ag_gemm_all_args *a,
     p.sig_rows = sig_rows;
     p.c_f32 = a->c_f32;
     p.stages = stages;
+    p.full_n = (N % gm::BN) == 0 ? 1 : 0;
     // the GEMM follows the push steps when every shard is whole tiles (else it
     // keeps the rank-by-rank order: the same result, only the waits differ)
     p.steps = (a->push && a->mode == TDG_MODE_CE && inplace) ? 1 : 0;

@@ -52,6 +52,7 @@ struct RsParams {
     int f32; // 1: partials are pushed as fp32, 0: as bf16
     int red_rows; // rows of owed reductions an epilogue warp works off per tile
     int stages;   // GEMM ring stages in use
+    int full_n;   // N is a multiple of BN: every tile is full width
 };
 
 __device__ __forceinline__ uint8_t *rs_stage_row(const RsParams &p, int o, int r, int m_loc, int pn, int row)
@@ -460,6 +461,7 @@ extern "C" int tdg_gemm_rs(tdg_symm *h, const tdg_gemm_rs_args *a, void *stream)
     p.n_tiles = n_tiles;
     p.order = a->order;
     p.stages = stages;
+    p.full_n = (N % gm::BN) == 0 ? 1 : 0;
     // two owners per block measured best at the Qwen-32B down-projection shape
     // (B_r streamed W/2 times instead of W; partials of a block stay L2-warm)
     if (a->owner_block < 0 || (a->owner_block > 0 && W % a->owner_block))
