@@ -138,7 +138,7 @@ def test_allgather_alone_when_n_is_zero(push):
     inp = synth.ag_inputs(4, 512, 264, 8, "int2", seed=5)
     case = AGCase(inp, ll=True)
     M, K = case.M, inp.K
-    for mode, kw in (("sm", dict(producers=4)), ("ce", {}), ("ll", dict(ll_off=case.ll_off)),
+    for mode, kw in (("sm", dict(producers=4)), ("sm", {}), ("ce", {}), ("ll", dict(ll_off=case.ll_off)),
                      ("serial", dict(producers=3)), ("serial", {})):
         for rank in (0, 3):
             case.gathered(rank).view(torch.int16).fill_(0x7FC1)

@@ -5,8 +5,8 @@ side stream and a GEMM on the main stream that waits (bounded) on those flags.
 The copies are queued first, so the call completes whatever order the two
 streams take -- also fully serialised, as under CUDA_LAUNCH_BLOCKING=1, a
 profiler's replay, or a host thread that stalls between launches.  The child
-process below runs the single-rank and the all-ranks AG-GEMM in CE mode with
-every launch blocking and a 50 ms bound on each wait: a call that queued its
+process below runs the single-rank and the all-ranks AG-GEMM in CE mode, pull
+and push, with every launch blocking and a 50 ms bound on each wait: a call that queued its
 GEMM first would run out of time (TDG_ERR_TIMEOUT) instead of returning the
 oracle's bits.
 """
@@ -35,13 +35,14 @@ inp = synth.ag_inputs(4, 512, 128, 264, "int2", seed=31)
 _, C16 = oracle.ag_gemm(inp.shards, inp.B)
 case = AGCase(inp)
 for rank in (0, 3):
-    got, st = case.run(rank=rank, mode="ce", timeout_ns=T, check_status=False)
-    assert st["code"] == 0, ("single rank", rank, st)
-    assert np.array_equal(got, C16), ("single rank", rank)
+    for push in (False, True):
+        got, st = case.run(rank=rank, mode="ce", timeout_ns=T, check_status=False, push=push)
+        assert st["code"] == 0, ("single rank", rank, push, st)
+        assert np.array_equal(got, C16), ("single rank", rank, push)
 aa = synth.ag_all_inputs(4, 512, 128, 264, "int2", seed=32)
 case = AGAllCase(aa)
-for rep in range(2):
-    got, st = case.run(mode="ce", timeout_ns=T, check_status=False)
+for rep, push in ((0, False), (1, True)):
+    got, st = case.run(mode="ce", timeout_ns=T, check_status=False, push=push)
     assert st["code"] == 0, ("all ranks", rep, st)
     for r in range(4):
         assert np.array_equal(got[r], oracle.ag_gemm(aa.shards, aa.Bs[r])[1]), ("all ranks", r)

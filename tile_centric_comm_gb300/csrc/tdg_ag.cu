@@ -625,16 +625,21 @@ constexpr double TILE_FLOPS = 12e12;
 
 // Default producer CTAs in SM mode: enough to copy the shards within the
 // time of the GEMM on every SM (so that the copies stay ahead of the tiles
-// that need them), in whole clusters, 4 .. 32.
+// that need them), in whole clusters, 4 .. 32; 32 when there is no GEMM
+// (N == 0: the AllGather alone).
 int default_producers(const AgParams &p, int grid, int TM)
 {
+    const int lo = (4 + p.cl - 1) / p.cl * p.cl, hi = 32 / p.cl * p.cl;
     const double tiles = (double)p.m_tiles * p.n_tiles;
     const double tile_s = 2.0 * TM * gm::BN * p.K / (p.cl * TILE_FLOPS);
     const double gemm_s = tiles * tile_s / ((double)grid / p.cl);
-    const double bytes = (double)p.W * p.Ms * p.K * 2.0;
-    int n = (int)ceil(bytes / (gemm_s * PROD_BPS));
-    n = (n + p.cl - 1) / p.cl * p.cl;
-    return n < 4 ? ((4 + p.cl - 1) / p.cl * p.cl) : (n > 32 ? 32 : n);
+    if (!(gemm_s > 0.0))
+        return hi;
+    const double want = (double)p.W * p.Ms * p.K * 2.0 / (gemm_s * PROD_BPS);
+    if (want >= hi)
+        return hi;
+    const int n = ((int)ceil(want) + p.cl - 1) / p.cl * p.cl;
+    return n < lo ? lo : (n > hi ? hi : n);
 }
 int64_t producer_tail_lo(const AgParams &p, int grid, int TM, int req)
 {
