@@ -38,6 +38,8 @@
 // the transpose bit of the instruction descriptor) or K-major (N x K).
 #pragma once
 
+#include <type_traits>
+
 #include "tdg.h"
 #include "tdg_ptx.cuh"
 
@@ -239,36 +241,23 @@ __device__ void gemm_consumer(const typename P::Params &p, uint8_t *smem, int un
             uint32_t acc_phase = 0;
             uint32_t consumed = 0; // kept in a register; published once for the abort drain
             const uint32_t sbase = smem_u32(smem);
-            for (int64_t it = item_lo + unit; it < items && !ps->abort; it += nunits) {
-                // The issue loop, not the tensor pipe, is what the MMAs wait on
-                // at tile changes: with full-width tiles only (the common case)
-                // it skips the tile's index arithmetic (64-bit divisions), which
-                // measured 1.5 % of the GEMM at 50 k-blocks per tile.
-                int n_mma = BN;
-                if (!p.full_n) {
-                    TileInfo ti;
-                    P::tile(p, it, ti, crank);
-                    if (ti.n_valid <= 0)
-                        continue;
-                    n_mma = ti.n_mma;
-                }
-                const uint32_t idesc = idesc_bf16(S::TILE_M, n_mma, P::B_MN);
-                if (!mbar_wait(&ps->tempty[acc], acc_phase ^ 1u, tmo)) {
-                    report_fault(p.status, TDG_ERR_TIMEOUT, TDG_WHERE_PIPE, 1, p.epoch);
-                    ps->abort = 1;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-                bool ok = true;
+            // The issue loop, not the tensor pipe, is what the MMAs wait on
+            // (each stage's wait, descriptors and commit sit between its
+            // MMAs and the next stage's): with full-width tiles only (the
+            // common case) it skips the tile's index arithmetic (64-bit
+            // divisions) and issues with a compile-time instruction
+            // descriptor, which measured 1.5 % of the GEMM at 50 k-blocks per
+            // tile.  An N edge tile takes the general copy of the loop.
+            auto k_loop = [&](auto full_width, uint32_t idesc_rt, uint32_t d_tmem) -> bool {
+                constexpr bool FULL = decltype(full_width)::value;
                 for (int kb = 0; kb < p.k_blocks; ++kb) {
                     if (!mbar_wait(&ps->full[stage], phase, tmo)) {
                         report_fault(p.status, TDG_ERR_TIMEOUT, TDG_WHERE_PIPE, 2, p.epoch);
                         ps->abort = 1;
-                        ok = false;
-                        break;
+                        return false;
                     }
                     tc_fence_after();
+                    const uint32_t idesc = FULL ? idesc_bf16(S::TILE_M, BN, P::B_MN) : idesc_rt;
                     const uint32_t a_addr = sbase + stage * S::STAGE_BYTES;
                     const uint32_t b_addr = a_addr + A_BYTES;
                     // MN-major B: 64-column chunks 8 KB apart (LBO), 8 K-rows 1 KB
@@ -297,6 +286,26 @@ __device__ void gemm_consumer(const typename P::Params &p, uint8_t *smem, int un
                         phase ^= 1u;
                     }
                 }
+                return true;
+            };
+            for (int64_t it = item_lo + unit; it < items && !ps->abort; it += nunits) {
+                uint32_t idesc_rt = 0;
+                if (!p.full_n) {
+                    TileInfo ti;
+                    P::tile(p, it, ti, crank);
+                    if (ti.n_valid <= 0)
+                        continue;
+                    idesc_rt = idesc_bf16(S::TILE_M, ti.n_mma, P::B_MN);
+                }
+                if (!mbar_wait(&ps->tempty[acc], acc_phase ^ 1u, tmo)) {
+                    report_fault(p.status, TDG_ERR_TIMEOUT, TDG_WHERE_PIPE, 1, p.epoch);
+                    ps->abort = 1;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+                const bool ok = p.full_n ? k_loop(std::true_type{}, 0u, d_tmem)
+                                         : k_loop(std::false_type{}, idesc_rt, d_tmem);
                 if (!ok)
                     break;
                 if (PAIR)
