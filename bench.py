@@ -869,7 +869,7 @@ def leg_autotune(torch, tdg, args, flush, pk):
     for r in range(W):
         sym.view(r, a_off, (M, K), torch.bfloat16).copy_(torch.randn(M, K, device="cuda", generator=g))
         sym.view(r, b_off, (K, N), torch.bfloat16).copy_(torch.randn(K, N, device="cuda", generator=g) * 0.02)
-    rc = autotune.rs_candidates(W, M // W, orders=(0,))
+    rc = autotune.rs_candidates(W, M // W, orders=(0,), spares=(0, 2))
 
     def run_rs(cfg):
         tdg.gemm_rs(sym, M, K, N, a_off, b_off, s_off, o_off, **cfg)

@@ -206,7 +206,9 @@ typedef struct {
                             mode enough to copy the shards within the GEMM's
                             time at about 50 GB/s each, 4..32; LL 8 senders),
                             copy CTAs of the SERIAL copy launch (0 = every SM) */
-    int64_t signal_rows; /* rows per signal; 0 = BM if Ms % BM == 0, else Ms */
+    int64_t signal_rows; /* rows per signal; 0 = Ms (one per shard) in CE
+                            mode, else 32 when Ms is a multiple of the GEMM's
+                            rows per tile and of 32, else Ms                */
     int swizzle;         /* 1 = rank-swizzled tile order, 0 = linear        */
     uint64_t timeout_ns; /* bound of every device wait; 0 = 2 s             */
     size_t ll_off;       /* LL mode: LL buffer (M*K*4 bytes) in region(rank);
@@ -355,6 +357,13 @@ typedef struct {
     int red_rows;        /* rows of an owed reduction an epilogue warp works
                             off after each tile: 4, 8, 16 or 32 (default 32
                             for bf16 partials, 8 for fp32)                   */
+    int spare;           /* the SMs that 4-CTA clusters leave idle (order 0,
+                            TDG_B_KN): a second launch of CTA pairs on them
+                            takes the last `spare` of the W*W (owner block,
+                            rank, owner) groups of tiles, starting as soon as
+                            every CTA of the first launch runs.  0 = none
+                            (default), at most W*W - 1; ignored where it
+                            does not apply                                  */
 } tdg_gemm_rs_args;
 
 /* Bytes of one owner's staging area for the given shape (all W partials),

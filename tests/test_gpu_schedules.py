@@ -83,6 +83,28 @@ def test_ring_stages_bit_exact(cluster, stages):
         assert np.array_equal(got[r], oracle.ag_gemm(aa.shards, aa.Bs[r])[1]), r
 
 
+@pytest.mark.parametrize("W,Mo,N,spare", [(2, 512, 520, 1), (2, 1024, 264, 3), (4, 512, 520, 5),
+                                           (8, 512, 264, 63), (8, 1024, 8, 2)])
+def test_spare_sm_pairs_bit_exact(W, Mo, N, spare):
+    # CTA pairs on the SMs the 4-CTA clusters leave idle take the last `spare`
+    # (owner block, rank, owner) tile groups in a second launch: the same
+    # partials and reductions, so the oracle's bits in both modes and with
+    # fp32 partials, and bits equal to the clusters alone on float data
+    inp = synth.rs_inputs(W, W * Mo, 64, N, "int2", seed=W * 1000 + spare)
+    _, out16 = oracle.gemm_rs(inp.As, inp.Bs)
+    for f32 in (False, True):
+        case = RSCase(inp, f32=f32)
+        for mode in ("sm", "serial"):
+            got, _ = case.run(mode=mode, cluster=4, spare=spare)
+            assert np.array_equal(got, out16), (f32, mode)
+    fl = synth.rs_inputs(W, W * Mo, 520, N, "normal", seed=W + spare)
+    case = RSCase(fl)
+    base, _ = case.run(mode="sm", cluster=4)
+    for mode in ("sm", "serial"):
+        got, _ = case.run(mode=mode, cluster=4, spare=spare)
+        assert np.array_equal(got, base), mode
+
+
 @pytest.mark.parametrize("warps,chunk", [(1, 4096), (1, 65536), (2, 16384), (3, 8192), (4, 16384), (4, 4096)])
 def test_producer_ring_shapes_bit_exact(warps, chunk):
     # unit sizes that are not a multiple of the chunk (K = 520: 1040-byte rows),
@@ -119,7 +141,8 @@ def test_out_of_range_schedules_are_rejected():
         rc = tdg.lib().tdg_ag_gemm(case.symm.h, ctypes.byref(a), tdg._stream(None), None)
         assert rc == tdg.TDG_ERR_INVALID, field
     rs = RSCase(synth.rs_inputs(2, 512, 64, 264, "int2", seed=4))   # 256 rows per owner
-    for kw in (dict(cluster=4), dict(order=2), dict(red_rows=3), dict(red_rows=64), dict(stages=9)):
+    for kw in (dict(cluster=4), dict(order=2), dict(red_rows=3), dict(red_rows=64), dict(stages=9),
+               dict(spare=-1), dict(spare=4)):
         with pytest.raises(tdg.TdgError) as ei:
             rs.run(mode="sm", **kw)
         assert ei.value.code == tdg.TDG_ERR_INVALID, kw

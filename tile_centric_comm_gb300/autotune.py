@@ -120,10 +120,12 @@ def ag_candidates(M: int, Ms: int = 0, modes=("ce", "sm"), producers=(0, 8, 16),
     return out
 
 
-def rs_candidates(world: int, Mo: int = 0, clusters=None, stages=(0, 4), orders=(0, 1)) -> List[dict]:
+def rs_candidates(world: int, Mo: int = 0, clusters=None, stages=(0, 4), orders=(0, 1),
+                  spares=(0,)) -> List[dict]:
     """GEMM+ReduceScatter schedules: owner block x tile order x GEMM cluster
-    shape x ring stages.  Mo (rows per owner) = 0 leaves the cluster shape to
-    the library."""
+    shape x ring stages (x, for order 0 on 4-CTA clusters, the tile groups
+    given to CTA pairs on the SMs the clusters leave idle).  Mo (rows per
+    owner) = 0 leaves the cluster shape to the library."""
     if clusters is None:
         clusters = _clusters(Mo % 256 == 0, Mo % 512 == 0) if Mo else [0]
     out = []
@@ -134,6 +136,9 @@ def rs_candidates(world: int, Mo: int = 0, clusters=None, stages=(0, 4), orders=
             if cl == 1 and st > 4:
                 continue
             out.append(dict(owner_block=ob, order=order, cluster=cl, stages=st))
+            if order == 0 and cl == 4:
+                out += [dict(owner_block=ob, order=order, cluster=cl, stages=st, spare=sp)
+                        for sp in spares if 0 < sp < world * world]
     return out
 
 

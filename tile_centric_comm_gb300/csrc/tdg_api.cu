@@ -162,14 +162,14 @@ int check_device(const tdg_symm *h)
 }
 
 cudaError_t launch(const void *fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s,
-                   void **args, bool cooperative, int cluster)
+                   void **args, bool cooperative, int cluster, bool after_prev)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[2];
+    cudaLaunchAttribute attr[3];
     int n = 0;
     attr[n].id = cudaLaunchAttributeCooperative;
     attr[n].val.cooperative = cooperative ? 1 : 0;
@@ -179,6 +179,11 @@ cudaError_t launch(const void *fn, dim3 grid, dim3 block, size_t smem, cudaStrea
         attr[n].val.clusterDim.x = (unsigned)cluster;
         attr[n].val.clusterDim.y = 1;
         attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    if (after_prev) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
         ++n;
     }
     cfg.attrs = attr;

@@ -94,9 +94,12 @@ void *current_context();
 int check_device(const tdg_symm *h);
 
 // Launch with the cooperative attribute (all CTAs co-resident, which the
-// cross-CTA signal waits rely on).
+// cross-CTA signal waits rely on).  `after_prev`: the programmatic
+// serialisation attribute, so that the kernel may start while the previous
+// one in the stream still runs, once that one's CTAs have all run
+// griddepcontrol.launch_dependents.
 cudaError_t launch(const void *fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s,
-                   void **args, bool cooperative, int cluster = 1);
+                   void **args, bool cooperative, int cluster = 1, bool after_prev = false);
 
 // Number of `cl`-CTA clusters of `fn` that can be resident at once (0 on error).
 int max_clusters(const void *fn, int block, int smem, int cl);

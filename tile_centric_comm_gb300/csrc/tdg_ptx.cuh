@@ -123,6 +123,19 @@ __device__ __forceinline__ bool mbar_wait_sleep(uint64_t *bar, uint32_t parity, 
     }
 }
 
+// --------------------------------------------------- dependent launches ----
+// Let the launch that follows this grid in its stream (launched with the
+// programmatic-serialisation attribute) start once every CTA of this grid has
+// run this instruction (or exited).
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Wait until the grid this one was launched after has completed and its
+// memory operations are visible.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // --------------------------------------------------------------- fences ----
 // Order this thread's generic-proxy accesses with async-proxy (TMA) accesses.
 __device__ __forceinline__ void fence_proxy_async_global()

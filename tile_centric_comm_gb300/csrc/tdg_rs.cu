@@ -53,6 +53,9 @@ struct RsParams {
     int red_rows; // rows of owed reductions an epilogue warp works off per tile
     int stages;   // GEMM ring stages in use
     int full_n;   // N is a multiple of BN: every tile is full width
+    int64_t item_lo, item_hi; // this launch's items (item_hi < 0: all)
+    int dep;      // 1: a second launch on the spare SMs follows this one;
+                  // 2: this is that launch (it ends after the first)
 };
 
 __device__ __forceinline__ uint8_t *rs_stage_row(const RsParams &p, int o, int r, int m_loc, int pn, int row)
@@ -338,7 +341,11 @@ __global__ void __launch_bounds__(gm::NUM_THREADS, 1) rs_gemm_kernel(const __gri
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
-    gemm_consumer<RsPolicy<BMN>, CL>(p, smem, (int)blockIdx.x / CL, (int)gridDim.x / CL);
+    if (p.dep == 1)
+        griddep_launch_dependents(); // every CTA is resident: the spare-SM launch may start
+    gemm_consumer<RsPolicy<BMN>, CL>(p, smem, (int)blockIdx.x / CL, (int)gridDim.x / CL, p.item_lo, p.item_hi);
+    if (p.dep == 2)
+        griddep_wait(); // what follows in the stream then also follows the first launch
 }
 
 // SERIAL reduction: one 4-warp CTA per output tile.
@@ -426,7 +433,8 @@ extern "C" int tdg_gemm_rs(tdg_symm *h, const tdg_gemm_rs_args *a, void *stream)
     const int cl = pick_cluster(a->cluster, Mo % (2 * gm::BM) == 0, Mo % (4 * gm::BM) == 0);
     const int stages = cl ? pick_stages(a->stages, cl) : 0;
     if (!cl || !stages || (a->order & ~1) ||
-        (a->red_rows != 0 && (a->red_rows < 4 || a->red_rows > 32 || 32 % a->red_rows)))
+        (a->red_rows != 0 && (a->red_rows < 4 || a->red_rows > 32 || 32 % a->red_rows)) ||
+        a->spare < 0 || a->spare >= W * W)
         return TDG_ERR_INVALID;
     const int pair = cl >= 2 ? 1 : 0;
     RsParams p;
@@ -503,9 +511,50 @@ extern "C" int tdg_gemm_rs(tdg_symm *h, const tdg_gemm_rs_args *a, void *stream)
     const int64_t items = (int64_t)W * W * p.mtp * n_tiles;
     if (grid / cl > items)
         grid = (int)(cl * items);
+    p.item_lo = 0;
+    p.item_hi = -1;
+    // The SMs that the 4-CTA clusters leave idle (152 - 144 on a GB300) take
+    // a share of the tiles as CTA pairs.  The tile order of order 0 is a
+    // sequence of (owner block, rank, owner) groups of Mo/512 x n_tiles
+    // cluster tiles, each of which is twice as many pair tiles in the same
+    // place of the pairs' order, so the pairs take the last groups and the
+    // clusters the rest.  The pairs launch after the clusters (programmatic
+    // serialisation: once every cluster CTA is resident, so they cannot take
+    // a cluster's place) and end after them.
+    // Measured at the Qwen-32B down-projection shape: as fast as the clusters
+    // alone in short bursts, up to a few percent faster on some boxes; under
+    // sustained load the GPU sits at its power cap and the extra SMs only
+    // lower the clock, so it is off by default.
+    const int spare_pairs = cl == 4 ? (h->sm_count - grid) / 2 : 0;
+    const int groups = (spare_pairs > 0 && a->order == 0 && a->b_layout == TDG_B_KN) ? a->spare : 0;
+    RsParams q = p;
+    const void *fn2 = nullptr;
+    if (groups > 0) {
+        fn2 = reinterpret_cast<const void *>(&rs_gemm_kernel<1, 2>);
+        if (cudaError_t e = set_smem(fn2, gm::SMEM_BYTES); e != cudaSuccess)
+            return cuda_err(e, "rs set smem");
+        const int64_t per_group = (int64_t)p.mtp * n_tiles; // cluster tiles
+        p.item_hi = items - groups * per_group;
+        p.dep = 1;
+        q.cl = 2;
+        q.pair = 1;
+        q.mtp = mt / 2;
+        q.item_lo = 2 * p.item_hi;
+        q.item_hi = 2 * items;
+        q.dep = 2;
+    }
+    // no more pairs than the pairs' tiles
+    const int64_t pair_items = groups > 0 ? 2 * (items - p.item_hi) : 0;
+    const int n_pairs = pair_items < spare_pairs ? (int)pair_items : spare_pairs;
     void *args[] = {&p};
     int rc = cuda_err(launch(fn, dim3(grid), dim3(gm::NUM_THREADS), gm::SMEM_BYTES, s, args, false, cl),
                       "rs gemm launch");
+    if (rc == TDG_OK && fn2) {
+        void *args2[] = {&q};
+        rc = cuda_err(launch(fn2, dim3(2 * n_pairs), dim3(gm::NUM_THREADS), gm::SMEM_BYTES, s, args2, false,
+                             2, true),
+                      "rs spare launch");
+    }
     if (rc != TDG_OK || a->mode == TDG_MODE_SM)
         return rc;
     const unsigned tiles = (unsigned)(W * mt * n_tiles);

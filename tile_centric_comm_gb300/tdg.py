@@ -72,7 +72,7 @@ class GemmRsArgs(ctypes.Structure):
                 ("b_off", _sz), ("stage_off", _sz), ("out_off", _sz), ("b_layout", ctypes.c_int),
                 ("mode", ctypes.c_int), ("timeout_ns", _u64), ("owner_block", ctypes.c_int),
                 ("partial_f32", ctypes.c_int), ("cluster", ctypes.c_int), ("stages", ctypes.c_int),
-                ("order", ctypes.c_int), ("red_rows", ctypes.c_int)]
+                ("order", ctypes.c_int), ("red_rows", ctypes.c_int), ("spare", ctypes.c_int)]
 
 
 class MoeArgs(ctypes.Structure):
@@ -335,15 +335,17 @@ def gemm_rs_stage_bytes(world: int, M: int, N: int) -> int:
 
 def gemm_rs(symm: Symm, M: int, K: int, N: int, a_off: int, b_off: int, stage_off: int,
             out_off: int, mode="sm", b_layout=B_KN, timeout_ns=0, owner_block=0,
-            partial_f32=False, stream=None, cluster=0, stages=0, order=0, red_rows=0):
+            partial_f32=False, stream=None, cluster=0, stages=0, order=0, red_rows=0, spare=0):
     """partial_f32: push fp32 partials (the staging area must then hold
     2 * gemm_rs_stage_bytes(world, M, N) bytes).  cluster / stages / order /
-    red_rows / owner_block choose the schedule (0: the default for the shape)."""
+    red_rows / owner_block / spare choose the schedule (0: the default for the
+    shape; spare=n > 0 lets CTA pairs on the SMs that 4-CTA clusters leave
+    idle take the last n of the world**2 groups of tiles)."""
     a = GemmRsArgs(world=symm.world, M=M, K=K, N=N, a_off=a_off, b_off=b_off,
                    stage_off=stage_off, out_off=out_off, b_layout=b_layout,
                    mode=MODES[mode], timeout_ns=timeout_ns, owner_block=owner_block,
                    partial_f32=1 if partial_f32 else 0, cluster=cluster, stages=stages,
-                   order=order, red_rows=red_rows)
+                   order=order, red_rows=red_rows, spare=spare)
     _check(lib().tdg_gemm_rs(symm.h, ctypes.byref(a), _stream(stream)), "tdg_gemm_rs")
 
 
