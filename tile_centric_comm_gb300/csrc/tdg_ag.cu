@@ -101,6 +101,7 @@ struct AgParams {
     uint32_t pchunk;  // bytes per bulk copy
     int pslots;       // ring slots per worker
     int full_n;       // N is a multiple of BN and no tile is split: every tile is full width
+    int edge_n;       // m-major order, no split, N not a multiple of BN: the last column's MMA width
 };
 
 template <int BMN, bool F32 = false> struct AgPolicy {
@@ -692,6 +693,13 @@ int launch_ag(const AgParams &p, int b_layout, int grid, bool coop, cudaStream_t
     if (q.tail_lo >= T)
         q.tail_lo = T + q.split; // every item goes to the GEMM CTAs
     q.full_n = (p.N % gm::BN) == 0 && q.split == 0 ? 1 : 0;
+    q.edge_n = 0;
+    if (!q.full_n && q.split == 0 && q.group_m <= 0) {
+        // m-major order (item = pm0 * n_tiles + pn): only the last column is narrow
+        const int q16 = p.pair ? 32 : 16;
+        const int nv = (int)(p.N - (int64_t)(p.n_tiles - 1) * gm::BN);
+        q.edge_n = (nv + q16 - 1) / q16 * q16;
+    }
     void *args[] = {&q};
     cudaError_t e = launch(fn, dim3(grid), dim3(gm::NUM_THREADS), gm::SMEM_BYTES, s, args, coop, p.cl);
     if (e != cudaSuccess && coop && p.cl > 1) {

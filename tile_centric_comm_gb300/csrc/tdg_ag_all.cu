@@ -52,6 +52,7 @@ struct AgAllParams {
     int c_f32; // 1: C_r is fp32
     int stages; // GEMM ring stages in use
     int full_n; // N is a multiple of BN: every tile is full width
+    int edge_n;   // 0: the narrow-last-column fast path is not used here
     int steps;  // 1: push order (items step by step, see tile()); 0: rank by rank
 };
 

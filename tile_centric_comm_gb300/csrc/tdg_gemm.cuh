@@ -102,10 +102,12 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p)
 
 // Policy P provides:
 //   struct Params { ... DevStatus *status; uint32_t epoch; uint64_t timeout_ns, pipe_timeout_ns;
-//                   int k_blocks; int stages; int full_n; };
+//                   int k_blocks; int stages; int full_n; int edge_n; int n_tiles; };
 //       (stages: ring stages in use, 2 .. Shape::STAGES; full_n: every item is
 //        a tile of the full BN columns -- N a multiple of BN, no null items --
-//        so the MMA issuer needs no per-tile arithmetic)
+//        so the MMA issuer needs no per-tile arithmetic; edge_n > 0: no null
+//        items, item i is in n-tile column i mod n_tiles, and only the last
+//        column is narrower, with an MMA of edge_n columns)
 //   static constexpr int B_MN;                                   // 1: B is K x N
 //   __device__ static int64_t num_items(const Params&);
 //   __device__ static void tile(const Params&, int64_t item, TileInfo&, int sub);
@@ -247,7 +249,10 @@ __device__ void gemm_consumer(const typename P::Params &p, uint8_t *smem, int un
             // common case) it skips the tile's index arithmetic (64-bit
             // divisions) and issues with a compile-time instruction
             // descriptor, which measured 1.5 % of the GEMM at 50 k-blocks per
-            // tile.  An N edge tile takes the general copy of the loop.
+            // tile.  Where only the last n-tile column is narrow (edge_n),
+            // the column is tracked without division and only that column's
+            // tiles take the general copy of the loop (+2 % at the Qwen-32B
+            // up-projection shape, N = 3200).
             auto k_loop = [&](auto full_width, uint32_t idesc_rt, uint32_t d_tmem) -> bool {
                 constexpr bool FULL = decltype(full_width)::value;
                 for (int kb = 0; kb < p.k_blocks; ++kb) {
@@ -288,9 +293,23 @@ __device__ void gemm_consumer(const typename P::Params &p, uint8_t *smem, int un
                 }
                 return true;
             };
+            // with edge_n, the column of this unit's items walks on by nunits
+            // mod n_tiles per item (no division in the loop)
+            int col = 0, col_step = 0;
+            if (!p.full_n && p.edge_n > 0) {
+                col = (int)((item_lo + unit) % p.n_tiles);
+                col_step = (int)(nunits % p.n_tiles);
+            }
             for (int64_t it = item_lo + unit; it < items && !ps->abort; it += nunits) {
                 uint32_t idesc_rt = 0;
-                if (!p.full_n) {
+                bool full = p.full_n != 0;
+                if (!full && p.edge_n > 0) {
+                    full = col != p.n_tiles - 1;
+                    idesc_rt = idesc_bf16(S::TILE_M, p.edge_n, P::B_MN);
+                    col += col_step;
+                    if (col >= p.n_tiles)
+                        col -= p.n_tiles;
+                } else if (!full) {
                     TileInfo ti;
                     P::tile(p, it, ti, crank);
                     if (ti.n_valid <= 0)
@@ -304,8 +323,8 @@ __device__ void gemm_consumer(const typename P::Params &p, uint8_t *smem, int un
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-                const bool ok = p.full_n ? k_loop(std::true_type{}, 0u, d_tmem)
-                                         : k_loop(std::false_type{}, idesc_rt, d_tmem);
+                const bool ok = full ? k_loop(std::true_type{}, 0u, d_tmem)
+                                     : k_loop(std::false_type{}, idesc_rt, d_tmem);
                 if (!ok)
                     break;
                 if (PAIR)

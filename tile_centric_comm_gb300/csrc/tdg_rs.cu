@@ -53,6 +53,7 @@ struct RsParams {
     int red_rows; // rows of owed reductions an epilogue warp works off per tile
     int stages;   // GEMM ring stages in use
     int full_n;   // N is a multiple of BN: every tile is full width
+    int edge_n;   // 0: the narrow-last-column fast path is not used here
     int64_t item_lo, item_hi; // this launch's items (item_hi < 0: all)
     int dep;      // 1: a second launch on the spare SMs follows this one;
                   // 2: this is that launch (it ends after the first)
