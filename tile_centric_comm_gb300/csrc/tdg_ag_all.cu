@@ -52,7 +52,7 @@ struct AgAllParams {
     int c_f32; // 1: C_r is fp32
     int stages; // GEMM ring stages in use
     int full_n; // N is a multiple of BN: every tile is full width
-    int edge_n;   // 0: the narrow-last-column fast path is not used here
+    int edge_n;   // > 0: only the last n-tile column is narrow, an MMA of edge_n columns
     int steps;  // 1: push order (items step by step, see tile()); 0: rank by rank
 };
 
@@ -343,6 +343,14 @@ extern "C" int tdg_ag_gemm_all_ranks(tdg_symm *h, const tdg_ag_gemm_all_args *a,
     // the GEMM follows the push steps when every shard is whole tiles (else it
     // keeps the rank-by-rank order: the same result, only the waits differ)
     p.steps = (a->push && a->mode == TDG_MODE_CE && inplace) ? 1 : 0;
+    // both orders without groups put item i in n-tile column i mod n_tiles
+    // (every block of the order is whole rows of n_tiles items)
+    p.edge_n = 0;
+    if (!p.full_n && p.group_m <= 0) {
+        const int q16 = p.pair ? 32 : 16;
+        const int nv = (int)(N - (int64_t)(p.n_tiles - 1) * gm::BN);
+        p.edge_n = (nv + q16 - 1) / q16 * q16;
+    }
 
     const void *fn = ag_all_kernel_fn(a->b_layout, cl, a->c_f32 != 0);
     if (cudaError_t e = set_smem(fn, gm::SMEM_BYTES); e != cudaSuccess)
