@@ -253,18 +253,21 @@ __device__ void gemm_consumer(const typename P::Params &p, uint8_t *smem, int un
             // the column is tracked without division and only that column's
             // tiles take the general copy of the loop (+2 % at the Qwen-32B
             // up-projection shape, N = 3200).
-            auto k_loop = [&](auto full_width, uint32_t idesc_rt, uint32_t d_tmem) -> bool {
+            // Returns the k-blocks consumed: all of them, or fewer when a wait
+            // ran out.  The stage's addresses are worked out before its wait,
+            // so that only the wait itself sits between two stages' MMAs.
+            auto k_loop = [&](auto full_width, uint32_t idesc_rt, uint32_t d_tmem) -> int {
                 constexpr bool FULL = decltype(full_width)::value;
                 for (int kb = 0; kb < p.k_blocks; ++kb) {
-                    if (!mbar_wait(&ps->full[stage], phase, tmo)) {
-                        report_fault(p.status, TDG_ERR_TIMEOUT, TDG_WHERE_PIPE, 2, p.epoch);
-                        ps->abort = 1;
-                        return false;
-                    }
-                    tc_fence_after();
                     const uint32_t idesc = FULL ? idesc_bf16(S::TILE_M, BN, P::B_MN) : idesc_rt;
                     const uint32_t a_addr = sbase + stage * S::STAGE_BYTES;
                     const uint32_t b_addr = a_addr + A_BYTES;
+                    if (!mbar_wait(&ps->full[stage], phase, tmo)) {
+                        report_fault(p.status, TDG_ERR_TIMEOUT, TDG_WHERE_PIPE, 2, p.epoch);
+                        ps->abort = 1;
+                        return kb;
+                    }
+                    tc_fence_after();
                     // MN-major B: 64-column chunks 8 KB apart (LBO), 8 K-rows 1 KB
                     // apart (SBO); a K step of 16 rows is 2 KB.  K-major B: same
                     // form as A (a K step of 16 elements is 32 bytes).  The start
@@ -285,13 +288,12 @@ __device__ void gemm_consumer(const typename P::Params &p, uint8_t *smem, int un
                         umma_commit_pair_mask(&ps->empty[stage], empty_mask);
                     else
                         umma_commit(&ps->empty[stage]);
-                    ++consumed;
                     if (++stage == NST) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
-                return true;
+                return p.k_blocks;
             };
             // with edge_n, the column of this unit's items walks on by nunits
             // mod n_tiles per item (no division in the loop)
@@ -323,9 +325,10 @@ __device__ void gemm_consumer(const typename P::Params &p, uint8_t *smem, int un
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-                const bool ok = full ? k_loop(std::true_type{}, 0u, d_tmem)
-                                     : k_loop(std::false_type{}, idesc_rt, d_tmem);
-                if (!ok)
+                const int done = full ? k_loop(std::true_type{}, 0u, d_tmem)
+                                      : k_loop(std::false_type{}, idesc_rt, d_tmem);
+                consumed += (uint32_t)done;
+                if (done < p.k_blocks)
                     break;
                 if (PAIR)
                     umma_commit_pair_mask(&ps->tfull[acc], pair_mask);
