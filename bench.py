@@ -49,9 +49,9 @@ WORKLOAD = ("qwen32b_mlp_tp8: AG-GEMM up-proj (W=8, A_r 1024x5120, B 5120x3200) 
 
 
 # DRAM traffic of one rs_gemm_kernel launch at this workload, dram__bytes_read.sum +
-# dram__bytes_write.sum from one ncu capture (2.443 GB read + 0.741 GB written).  It is
+# dram__bytes_write.sum from one ncu capture (1.585 GB read + 0.740 GB written).  It is
 # reported only while the kernel's sources still hash to the value the capture was taken with.
-RS_TRAFFIC = {"sources": "4044f4d8e3676e14", "bytes": 2_443_438_080 + 741_048_064}
+RS_TRAFFIC = {"sources": "f6b5e1cdf50517e2", "bytes": 1_584_866_048 + 740_150_016}
 RS_SOURCES = ["tdg_gemm.cuh", "tdg_rs.cu", "tdg_ptx.cuh"]
 
 
@@ -875,10 +875,10 @@ def leg_autotune(torch, tdg, args, flush, pk):
         tdg.gemm_rs(sym, M, K, N, a_off, b_off, s_off, o_off, **cfg)
     best, table = autotune.tune(("rs", W, M, K, N), rc, run_rs, warmup=2, iters=5, flush=flush.zero_,
                                 use_cache=False)
-    dflt = [r["ms"] for r in table if r["cfg"] == dict(owner_block=2, order=0, cluster=4, stages=0)]
+    dflt = [r["ms"] for r in table if r["cfg"] == dict(owner_block=W, order=0, cluster=4, stages=0)]
     out["gemm_rs_qwen32b_down"] = {"candidates": len(rc), "best": best,
                                    "best_tflops": RS_FLOP / min(r["ms"] for r in table) / 1e9,
-                                   "default": dict(owner_block=2, order=0, cluster=4, stages=0),
+                                   "default": dict(owner_block=W, order=0, cluster=4, stages=0),
                                    "default_tflops": RS_FLOP / dflt[0] / 1e9 if dflt else None,
                                    "table": [dict(r["cfg"], tflops=round(RS_FLOP / r["ms"] / 1e9, 1))
                                              for r in table]}

@@ -346,7 +346,9 @@ typedef struct {
     int mode;            /* TDG_MODE_SM (overlapped) or TDG_MODE_SERIAL      */
     uint64_t timeout_ns; /* bound of every device wait; 0 = 2 s             */
     int owner_block;     /* tile order: owners per block, each rank's tiles of
-                            a block back to back (0 = 2; must divide world)  */
+                            a block back to back (must divide world; 0 =
+                            world with bf16 partials, the largest divisor
+                            of world up to 4 with fp32 partials)             */
     int partial_f32;     /* 1: fp32 partials (twice the staging), 0: bf16     */
     /* schedule (0 = default for the shape) */
     int cluster;         /* CTAs per GEMM cluster: 1, 2 (needs (M/W) % 256
