@@ -283,6 +283,19 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, const void 
         : "memory");
 }
 
+// The same store with an L2 evict-first policy: for data that is read again
+// only long after, once it has left L2 anyway.
+__device__ __forceinline__ void tma_store_3d_evict_first(const CUtensorMap *map, const void *smem_src, int x,
+                                                         int y, int z)
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group.L2::cache_hint"
+                 " [%0, {%2, %3, %4}], [%1], %5;" ::"l"(map),
+                 "r"(smem_u32(smem_src)), "r"(x), "r"(y), "r"(z), "l"(pol)
+                 : "memory");
+}
+
 // 1-D bulk copies (16-byte aligned addresses, size a multiple of 16).
 __device__ __forceinline__ void bulk_load(void *smem_dst, const void *gsrc, uint32_t bytes,
                                           uint64_t *bar)
