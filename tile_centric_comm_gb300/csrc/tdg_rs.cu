@@ -141,7 +141,7 @@ __device__ void rs_reduce_rows(const RsParams &p, int o, int m_loc, int pn, int 
             w.y = pack_bf16x2(acc[a][2], acc[a][3]);
             w.z = pack_bf16x2(acc[a][4], acc[a][5]);
             w.w = pack_bf16x2(acc[a][6], acc[a][7]);
-            *reinterpret_cast<uint4 *>(out_base + ((uint64_t)orow * p.N + n0 + col) * 2) = w;
+            __stcs(reinterpret_cast<uint4 *>(out_base + ((uint64_t)orow * p.N + n0 + col) * 2), w); // not read here again
         }
     }
 }
