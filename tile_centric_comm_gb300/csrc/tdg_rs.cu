@@ -72,9 +72,11 @@ __device__ __forceinline__ uint8_t *rs_stage_row(const RsParams &p, int o, int r
 // [8l, 8l + 8) of the tile, which are one 16-byte unit of each bf16 partial
 // row or two units of each fp32 one (p.f32); the units are loaded one after
 // the other, so both forms keep the same 4 rows x 8 ranks in flight.  Each
-// partial is read here once, after the counter's acquire: streaming loads
-// (evict-first), so that the partials do not push the GEMM's operands out
-// of L2 (+0.8 % at the Qwen-32B down-projection shape).
+// partial is read here once, after the counter's acquire: bf16 partials with
+// streaming loads (evict-first), so that they do not push the GEMM's operands
+// out of L2 (+0.8 % at the Qwen-32B down-projection shape); fp32 partials,
+// reduced a few rows per tile from L2-warm blocks, with L2-only loads (the
+// streaming form measured 20 % slower there).
 __device__ void rs_reduce_rows(const RsParams &p, int o, int m_loc, int pn, int n_valid, int row0, int row1,
                                int lane)
 {
@@ -104,9 +106,11 @@ __device__ void rs_reduce_rows(const RsParams &p, int o, int m_loc, int pn, int 
                 for (int j = 0; j < 8; ++j) {
                     if (r0 + j < p.W) {
 #pragma unroll
-                        for (int a = 0; a < RR; ++a)
-                            v[a][j] = __ldcs(reinterpret_cast<const uint4 *>(
-                                rs_stage_row(p, o, r0 + j, m_loc, pn, rr + a) + lane_off + 16 * u));
+                        for (int a = 0; a < RR; ++a) {
+                            const uint4 *src = reinterpret_cast<const uint4 *>(
+                                rs_stage_row(p, o, r0 + j, m_loc, pn, rr + a) + lane_off + 16 * u);
+                            v[a][j] = f32 ? __ldcg(src) : __ldcs(src);
+                        }
                     }
                 }
 #pragma unroll
