@@ -215,11 +215,14 @@ template <int BMN, bool F32 = false> struct AgPolicy {
     {
         uint8_t *d = static_cast<uint8_t *>(dst);
         if constexpr (CL == 4) {
+            // B (K x N) stays in L2 for every m row of tiles and C leaves it
+            // first (+0.8 % at the Qwen-32B up-projection with the copy
+            // engine's traffic beside the GEMM)
             const uint16_t mask = (uint16_t)((1u << half) | (1u << (2 + half)));
             const int nch = BMN ? (cols + 63) >> 6 : 2;
             for (int j = pidx; j < nch; j += 2) {
                 if (BMN)
-                    tma_load_2d_pair_mc(d + j * 8192, &p.tmB, bar, col0 + 64 * j, kb * gm::BK, mask);
+                    tma_load_2d_pair_mc_evict_last(d + j * 8192, &p.tmB, bar, col0 + 64 * j, kb * gm::BK, mask);
                 else
                     tma_load_2d_pair_mc(d + j * 8192, &p.tmB, bar, kb * gm::BK, col0 + 64 * j, mask);
             }
@@ -246,7 +249,7 @@ template <int BMN, bool F32 = false> struct AgPolicy {
     {
         const int row = t.m0 + 32 * q;
         if (row < p.M)
-            tma_store_2d(&p.tmC, buf, t.n0 + 64 * ch, row);
+            tma_store_2d_evict_first(&p.tmC, buf, t.n0 + 64 * ch, row);
     }
 
     // (the second 32-column half of a 64-column chunk may start past N: skipped)

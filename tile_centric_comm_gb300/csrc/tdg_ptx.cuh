@@ -296,6 +296,19 @@ __device__ __forceinline__ void tma_store_3d_evict_first(const CUtensorMap *map,
                  : "memory");
 }
 
+// The same store with an L2 evict-first policy (an output this kernel does
+// not read again).
+__device__ __forceinline__ void tma_store_2d_evict_first(const CUtensorMap *map, const void *smem_src, int x,
+                                                         int y)
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group.L2::cache_hint"
+                 " [%0, {%2, %3}], [%1], %4;" ::"l"(map),
+                 "r"(smem_u32(smem_src)), "r"(x), "r"(y), "l"(pol)
+                 : "memory");
+}
+
 // 1-D bulk copies (16-byte aligned addresses, size a multiple of 16).
 __device__ __forceinline__ void bulk_load(void *smem_dst, const void *gsrc, uint32_t bytes,
                                           uint64_t *bar)
@@ -541,6 +554,20 @@ __device__ __forceinline__ void tma_load_2d_pair_mc(void *smem_dst, const CUtens
         "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
         ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(smem_dst)),
         "l"(map), "r"(bar_cluster), "r"(x), "r"(y), "h"(mask)
+        : "memory");
+}
+
+// tma_load_2d_pair_mc with an L2 evict-last policy: an operand that every
+// tile of the launch reads again (B of the AG-GEMM).
+__device__ __forceinline__ void tma_load_2d_pair_mc_evict_last(void *smem_dst, const CUtensorMap *map,
+                                                               uint32_t bar_cluster, int x, int y, uint16_t mask)
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        ".multicast::cluster.L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5, %6;" ::"r"(smem_u32(smem_dst)),
+        "l"(map), "r"(bar_cluster), "r"(x), "r"(y), "h"(mask), "l"(pol)
         : "memory");
 }
 
