@@ -5,9 +5,10 @@
 //
 // One persistent tcgen05 GEMM runs every rank's partial product.  Work items
 // are (owner block, rank r, owner o in the block, m tile inside o, n tile):
-// all ranks' items of one block of two owners run back to back, so every
-// output tile gathers its W partials close together in time while each B_r
-// is streamed once per block.  The epilogue pushes each partial tile (bf16,
+// all ranks' items of one block run back to back, so each B_r is streamed
+// once per block (by default one block of all owners: once per call), and
+// with smaller blocks every output tile gathers its W partials closer
+// together in time.  The epilogue pushes each partial tile (bf16,
 // or fp32 when asked; tile-contiguous, 128 x 256) into owner o's staging area
 // (region o) with TMA, waits for the write to complete, fences the async
 // proxy, and increments the owner's per-(tile, row-quarter) arrival counter
