@@ -105,6 +105,21 @@ def test_spare_sm_pairs_bit_exact(W, Mo, N, spare):
         assert np.array_equal(got, base), mode
 
 
+@pytest.mark.parametrize("W", [3, 5, 6, 8])
+def test_rs_default_owner_blocks_bit_exact(W):
+    # the default owner block: all W owners with bf16 partials, the largest
+    # divisor of W up to 4 with fp32 partials (3, 1, 3 and 4 here); also the
+    # order that keeps the pushes' L2 hint off (rank fastest)
+    inp = synth.rs_inputs(W, W * 256, 64, 264, "int2", seed=W * 77)
+    _, out16 = oracle.gemm_rs(inp.As, inp.Bs)
+    for f32 in (False, True):
+        case = RSCase(inp, f32=f32)
+        for mode in ("sm", "serial"):
+            for order in (0, 1):
+                got, _ = case.run(mode=mode, order=order)
+                assert np.array_equal(got, out16), (f32, mode, order)
+
+
 @pytest.mark.parametrize("warps,chunk", [(1, 4096), (1, 65536), (2, 16384), (3, 8192), (4, 16384), (4, 4096)])
 def test_producer_ring_shapes_bit_exact(warps, chunk):
     # unit sizes that are not a multiple of the chunk (K = 520: 1040-byte rows),
