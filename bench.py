@@ -879,7 +879,7 @@ def leg_autotune(torch, tdg, args, flush, pk):
 
     def run_rs(cfg):
         tdg.gemm_rs(sym, M, K, N, a_off, b_off, s_off, o_off, **cfg)
-    best, table = autotune.tune(("rs", W, M, K, N), rc, run_rs, warmup=2, iters=5, flush=flush.zero_,
+    best, table = autotune.tune(("rs", W, M, K, N), rc, run_rs, warmup=2, iters=10, flush=flush.zero_,
                                 use_cache=False)
     dflt = [r["ms"] for r in table if r["cfg"] == dict(owner_block=W, order=0, cluster=4, stages=0)]
     out["gemm_rs_qwen32b_down"] = {"candidates": len(rc), "best": best,

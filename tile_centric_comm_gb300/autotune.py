@@ -47,12 +47,16 @@ def choose(times: Sequence[float], group=None) -> Tuple[int, List[float]]:
 
 def time_candidate(run: Callable[[dict], None], cfg: dict, warmup: int = 2, iters: int = 5,
                    flush=None) -> float:
-    """Median device time (ms) of `run(cfg)` over `iters` launches."""
+    """Median device time (ms) of `run(cfg)` over `iters` launches, queued
+    back to back (the host waits once): the GPU stays busy as it does in use,
+    so a schedule that saves DRAM traffic, and with it power and clock, is
+    seen to; launches timed one at a time from an idle GPU start at full
+    clock and hide that."""
     import torch
     stream = torch.cuda.current_stream()
     for _ in range(warmup):
         run(cfg)
-    ts = []
+    evs = []
     for _ in range(iters):
         if flush is not None:
             flush()
@@ -60,9 +64,9 @@ def time_candidate(run: Callable[[dict], None], cfg: dict, warmup: int = 2, iter
         a.record(stream)
         run(cfg)
         b.record(stream)
-        b.synchronize()
-        ts.append(a.elapsed_time(b))
-    return statistics.median(ts)
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in evs)
 
 
 def tune(key: tuple, candidates: List[dict], run: Callable[[dict], None], group=None,
