@@ -856,8 +856,8 @@ def leg_autotune(torch, tdg, args, flush, pk):
 
     def run(cfg):
         tdg.ag_gemm(sym, 0, Ms, K, N, 0, g_off, B, C, side_stream=side, **cfg)
-    best, table = autotune.tune(("ag", W, Ms, K, N), cands, run, warmup=2, iters=7, flush=flush.zero_,
-                                use_cache=False)
+    best, table = autotune.tune(("ag", W, Ms, K, N), cands, run, warmup=2, iters=20, flush=flush.zero_,
+                                use_cache=False, pause=0.2)
     # the first candidate is the library's default schedule in CE mode (pull,
     # the default cluster shape and stage count)
     flop = 2 * W * Ms * K * N
@@ -879,8 +879,8 @@ def leg_autotune(torch, tdg, args, flush, pk):
 
     def run_rs(cfg):
         tdg.gemm_rs(sym, M, K, N, a_off, b_off, s_off, o_off, **cfg)
-    best, table = autotune.tune(("rs", W, M, K, N), rc, run_rs, warmup=2, iters=10, flush=flush.zero_,
-                                use_cache=False)
+    best, table = autotune.tune(("rs", W, M, K, N), rc, run_rs, warmup=2, iters=50, flush=flush.zero_,
+                                use_cache=False, pause=0.2)
     dflt = [r["ms"] for r in table if r["cfg"] == dict(owner_block=W, order=0, cluster=4, stages=0)]
     out["gemm_rs_qwen32b_down"] = {"candidates": len(rc), "best": best,
                                    "best_tflops": RS_FLOP / min(r["ms"] for r in table) / 1e9,

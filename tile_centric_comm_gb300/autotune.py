@@ -46,14 +46,20 @@ def choose(times: Sequence[float], group=None) -> Tuple[int, List[float]]:
 
 
 def time_candidate(run: Callable[[dict], None], cfg: dict, warmup: int = 2, iters: int = 5,
-                   flush=None) -> float:
+                   flush=None, pause: float = 0.0) -> float:
     """Median device time (ms) of `run(cfg)` over `iters` launches, queued
     back to back (the host waits once): the GPU stays busy as it does in use,
     so a schedule that saves DRAM traffic, and with it power and clock, is
     seen to; launches timed one at a time from an idle GPU start at full
-    clock and hide that."""
+    clock and hide that.  `pause` seconds of idle GPU before the timed
+    launches give every candidate the same starting temperature and power
+    state (a burst of work, as one serving step is)."""
+    import time
     import torch
     stream = torch.cuda.current_stream()
+    if pause > 0:
+        torch.cuda.synchronize()
+        time.sleep(pause)
     for _ in range(warmup):
         run(cfg)
     evs = []
@@ -71,7 +77,7 @@ def time_candidate(run: Callable[[dict], None], cfg: dict, warmup: int = 2, iter
 
 def tune(key: tuple, candidates: List[dict], run: Callable[[dict], None], group=None,
          warmup: int = 2, iters: int = 5, flush=None, use_cache: bool = True,
-         rounds: int = 3) -> Tuple[dict, List[dict]]:
+         rounds: int = 3, pause: float = 0.0) -> Tuple[dict, List[dict]]:
     """Time every candidate, agree on the best across ranks, cache it.
     The candidates are timed in `rounds` rounds, the order rotated every
     round, and each keeps the median of its rounds: a GPU's clock drifts over
@@ -85,7 +91,7 @@ def tune(key: tuple, candidates: List[dict], run: Callable[[dict], None], group=
         start = (r * n) // max(1, rounds)
         for j in range(n):
             i = (start + j) % n
-            per[i].append(time_candidate(run, candidates[i], warmup if r == 0 else 1, iters, flush))
+            per[i].append(time_candidate(run, candidates[i], warmup if r == 0 else 1, iters, flush, pause))
     times = [statistics.median(t) for t in per]
     best, combined = choose(times, group)
     table = [dict(cfg=c, ms=t) for c, t in zip(candidates, combined)]
