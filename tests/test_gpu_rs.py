@@ -85,10 +85,19 @@ def test_full_size_sampled():
     rows = np.concatenate([g.integers(0, M, 1000), [0, M - 1]])
     cols = np.concatenate([g.integers(0, N, 1000), [N - 1, 0]])
     ref = oracle.gemm_rs_sampled(inp.As, inp.Bs, rows, cols)
+    base = None
     for mode in ("sm", "serial"):
         got, _ = case.run(mode=mode)
         flat = got.reshape(M, N)
         assert_close(flat[rows, cols], ref)
+        if base is None:
+            base = got
+    # other schedules at the full size: the same partials summed in the same
+    # rank order, so the same bits (blocks of 2 owners, no L2 hints on the
+    # pushes; CTA pairs on the spare SMs; pairs-only clusters)
+    for kw in (dict(owner_block=2), dict(spare=2), dict(cluster=2)):
+        got, _ = case.run(mode="sm", **kw)
+        assert np.array_equal(got, base), kw
     del case
     torch.cuda.empty_cache()
 
