@@ -893,7 +893,8 @@ def leg_autotune(torch, tdg, args, flush, pk):
         raise RuntimeError(f"device fault in the autotune leg: {st}")
     del sym
     torch.cuda.empty_cache()
-    out["note"] = "candidates timed one after another (median of 7 / 5 calls, L2 flushed before each)"
+    out["note"] = ("each candidate timed as a burst of back-to-back calls (20 AG-GEMM / 50 GEMM-RS, L2 flushed "
+                   "before each) after a 0.2 s idle pause; 3 rounds with the order rotated, median per candidate")
     return out
 
 
