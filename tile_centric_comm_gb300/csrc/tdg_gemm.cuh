@@ -243,57 +243,91 @@ __device__ void gemm_consumer(const typename P::Params &p, uint8_t *smem, int un
             uint32_t acc_phase = 0;
             uint32_t consumed = 0; // kept in a register; published once for the abort drain
             const uint32_t sbase = smem_u32(smem);
-            // The issue loop, not the tensor pipe, is what the MMAs wait on
-            // (each stage's wait, descriptors and commit sit between its
-            // MMAs and the next stage's): with full-width tiles only (the
-            // common case) it skips the tile's index arithmetic (64-bit
-            // divisions) and issues with a compile-time instruction
-            // descriptor, which measured 1.5 % of the GEMM at 50 k-blocks per
-            // tile.  Where only the last n-tile column is narrow (edge_n),
-            // the column is tracked without division and only that column's
-            // tiles take the general copy of the loop (+2 % at the Qwen-32B
-            // up-projection shape, N = 3200).
+            // The issuing thread spends about 85 cycles on each MMA (256 x 256
+            // x 16, 128 cycles of tensor-pipe work), so what it does between a
+            // stage's MMAs and the next stage's decides whether the pipe's
+            // queue stays full: with full-width tiles only (the common case)
+            // it skips the tile's index arithmetic (64-bit divisions) and
+            // issues with a compile-time instruction descriptor, which
+            // measured 1.5 % of the GEMM at 50 k-blocks per tile.  Where only
+            // the last n-tile column is narrow (edge_n), the column is tracked
+            // without division and only that column's tiles take the general
+            // copy of the loop (+2 % at the Qwen-32B up-projection shape,
+            // N = 3200).  With every ring slot in use, the full-width loop
+            // runs whole rounds of the ring unrolled, so that each slot's
+            // barriers and descriptors are fixed offsets from hoisted bases
+            // (no stage arithmetic or wrap test between the stages' MMAs).
+            // The descriptors' start-address field counts 16-byte units, and
+            // the ring (under 256 KB of shared memory) never carries into the
+            // next field, so adding a slot's offset to the base descriptor
+            // equals building the descriptor at the slot.
+            // MN-major B: 64-column chunks 8 KB apart (LBO), 8 K-rows 1 KB
+            // apart (SBO); a K step of 16 rows is 2 KB.  K-major B: same form
+            // as A (a K step of 16 elements is 32 bytes).
+            const uint64_t a_desc0 = sdesc_sw128(sbase, 16, 1024);
+            const uint64_t b_desc0 =
+                P::B_MN ? sdesc_sw128(sbase + A_BYTES, 8192, 1024) : sdesc_sw128(sbase + A_BYTES, 16, 1024);
+            // one ring stage in slot st: wait for its data, issue its MMAs, free it
+            auto stage_mma = [&](int kb, int st, uint32_t ph, uint32_t idesc, uint32_t d_tmem) -> bool {
+                const uint64_t ad0 = a_desc0 + (uint64_t)(st * (S::STAGE_BYTES >> 4));
+                const uint64_t bd0 = b_desc0 + (uint64_t)(st * (S::STAGE_BYTES >> 4));
+                if (!mbar_wait(&ps->full[st], ph, tmo))
+                    return false;
+                tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < BK / 16; ++k) {
+                    const uint64_t ad = ad0 + (uint64_t)(k * 2);
+                    const uint64_t bd = bd0 + (uint64_t)(P::B_MN ? k * 128 : k * 2);
+                    if (PAIR)
+                        umma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+                    else
+                        umma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+                }
+                if (PAIR)
+                    umma_commit_pair_mask(&ps->empty[st], empty_mask);
+                else
+                    umma_commit(&ps->empty[st]);
+                return true;
+            };
             // Returns the k-blocks consumed: all of them, or fewer when a wait
-            // ran out.  The stage's addresses are worked out before its wait,
-            // so that only the wait itself sits between two stages' MMAs.
+            // ran out.
             auto k_loop = [&](auto full_width, uint32_t idesc_rt, uint32_t d_tmem) -> int {
                 constexpr bool FULL = decltype(full_width)::value;
-                for (int kb = 0; kb < p.k_blocks; ++kb) {
-                    const uint32_t idesc = FULL ? idesc_bf16(S::TILE_M, BN, P::B_MN) : idesc_rt;
-                    const uint32_t a_addr = sbase + stage * S::STAGE_BYTES;
-                    const uint32_t b_addr = a_addr + A_BYTES;
-                    if (!mbar_wait(&ps->full[stage], phase, tmo)) {
-                        report_fault(p.status, TDG_ERR_TIMEOUT, TDG_WHERE_PIPE, 2, p.epoch);
-                        ps->abort = 1;
-                        return kb;
+                const uint32_t idesc = FULL ? idesc_bf16(S::TILE_M, BN, P::B_MN) : idesc_rt;
+                int kb = 0;
+                if (FULL && NST == S::STAGES) {
+                    // up to slot 0, then whole rounds of the ring unrolled
+                    for (; kb < p.k_blocks && stage != 0; ++kb) {
+                        if (!stage_mma(kb, stage, phase, idesc, d_tmem))
+                            goto timed_out;
+                        if (++stage == NST) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
                     }
-                    tc_fence_after();
-                    // MN-major B: 64-column chunks 8 KB apart (LBO), 8 K-rows 1 KB
-                    // apart (SBO); a K step of 16 rows is 2 KB.  K-major B: same
-                    // form as A (a K step of 16 elements is 32 bytes).  The start
-                    // address field counts 16-byte units in the descriptor's low
-                    // bits, so the K steps are added to the stage's descriptors.
-                    const uint64_t ad0 = sdesc_sw128(a_addr, 16, 1024);
-                    const uint64_t bd0 = P::B_MN ? sdesc_sw128(b_addr, 8192, 1024) : sdesc_sw128(b_addr, 16, 1024);
+                    for (; kb + S::STAGES <= p.k_blocks; kb += S::STAGES) {
 #pragma unroll
-                    for (int k = 0; k < BK / 16; ++k) {
-                        const uint64_t ad = ad0 + (uint64_t)(k * 2);
-                        const uint64_t bd = bd0 + (uint64_t)(P::B_MN ? k * 128 : k * 2);
-                        if (PAIR)
-                            umma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
-                        else
-                            umma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+                        for (int st = 0; st < S::STAGES; ++st)
+                            if (!stage_mma(kb + st, st, phase, idesc, d_tmem)) {
+                                kb += st;
+                                goto timed_out;
+                            }
+                        phase ^= 1u;
                     }
-                    if (PAIR)
-                        umma_commit_pair_mask(&ps->empty[stage], empty_mask);
-                    else
-                        umma_commit(&ps->empty[stage]);
+                }
+                for (; kb < p.k_blocks; ++kb) {
+                    if (!stage_mma(kb, stage, phase, idesc, d_tmem))
+                        goto timed_out;
                     if (++stage == NST) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 return p.k_blocks;
+            timed_out:
+                report_fault(p.status, TDG_ERR_TIMEOUT, TDG_WHERE_PIPE, 2, p.epoch);
+                ps->abort = 1;
+                return kb;
             };
             // with edge_n, the column of this unit's items walks on by nunits
             // mod n_tiles per item (no division in the loop)
