@@ -125,6 +125,7 @@ template <int BMN, bool F32 = false> struct AgPolicy {
             tid = full + (item - full) / 2;
             nhalf = (int)((item - full) & 1);
         }
+        int64_t r64;
         // Two rasters.  group_m == 0: m-major (all n tiles of one m row, then
         // the next row), so the tiles of a wave follow the shards in arrival
         // order and wait on as few signals as possible (B stays in L2).
@@ -134,15 +135,15 @@ template <int BMN, bool F32 = false> struct AgPolicy {
         int pm0;
         const int GM = p.group_m;
         if (GM <= 0) {
-            pm0 = (int)(tid / p.n_tiles);
-            t.pn = (int)(tid % p.n_tiles);
+            pm0 = (int)divmod(tid, p.n_tiles, r64);
+            t.pn = (int)r64;
         } else {
             const int64_t per_group = (int64_t)GM * p.n_tiles;
-            const int grp = (int)(tid / per_group);
-            const int64_t in = tid % per_group;
+            int64_t in;
+            const int grp = (int)divmod(tid, per_group, in);
             const int rows = min(GM, p.m_tiles - grp * GM);
-            t.pn = (int)(in / rows);
-            pm0 = grp * GM + (int)(in % rows);
+            t.pn = (int)divmod(in, rows, r64);
+            pm0 = grp * GM + (int)r64;
         }
         // Triton-distributed's swizzle: pid_m = (pid_m + rank * tiles_per_pe) % total
         // (local shard first, then rank+1, rank+2, ...).  Push mode mirrors it,

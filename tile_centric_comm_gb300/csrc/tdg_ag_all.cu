@@ -77,30 +77,29 @@ template <int BMN, bool F32 = false> struct AgAllPolicy {
             // m tiles of shard (r - j) mod W, n inner
             const int64_t per_shard = (int64_t)p.tiles_per_shard * p.n_tiles;
             const int64_t per_step = (int64_t)p.W * per_shard;
-            const int j = (int)(item / per_step);
-            const int64_t rem = item % per_step;
-            const int r = (int)(rem / per_shard);
-            const int64_t in = rem % per_shard;
+            int64_t rem, in, pn;
+            const int j = (int)divmod(item, per_step, rem);
+            const int r = (int)divmod(rem, per_shard, in);
             const int shard = ((r - j) % p.W + p.W) % p.W;
-            const int pm = shard * p.tiles_per_shard + (int)(in / p.n_tiles);
-            t.pn = (int)(in % p.n_tiles);
+            const int pm = shard * p.tiles_per_shard + (int)divmod(in, p.n_tiles, pn);
+            t.pn = (int)pn;
             set_tile(p, t, r, pm, sub, tm);
             return;
         }
-        const int r = (int)(item / per_rank);
-        const int64_t tid = item % per_rank;
+        int64_t tid, r64;
+        const int r = (int)divmod(item, per_rank, tid);
         int pm0;
         const int GM = p.group_m;
         if (GM <= 0) {
-            pm0 = (int)(tid / p.n_tiles);
-            t.pn = (int)(tid % p.n_tiles);
+            pm0 = (int)divmod(tid, p.n_tiles, r64);
+            t.pn = (int)r64;
         } else {
             const int64_t per_group = (int64_t)GM * p.n_tiles;
-            const int grp = (int)(tid / per_group);
-            const int64_t in = tid % per_group;
+            int64_t in;
+            const int grp = (int)divmod(tid, per_group, in);
             const int rows = min(GM, p.m_tiles - grp * GM);
-            t.pn = (int)(in / rows);
-            pm0 = grp * GM + (int)(in % rows);
+            t.pn = (int)divmod(in, rows, r64);
+            pm0 = grp * GM + (int)r64;
         }
         // Triton-distributed's swizzle: pid_m = (pid_m + rank * tiles_per_pe) % total
         const int pm = (pm0 + (int)(((int64_t)r * p.Ms / tm) % p.m_tiles)) % p.m_tiles;

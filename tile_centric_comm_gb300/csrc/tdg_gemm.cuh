@@ -95,6 +95,22 @@ struct PipeSmem {
 };
 static_assert(sizeof(PipeSmem) <= gm::BAR_BYTES, "barrier block");
 
+// q = a / b and r = a % b for a >= 0, b > 0, in 32-bit arithmetic whenever
+// both fit (an unsigned 32-bit division is a short instruction sequence, a
+// 64-bit one a long software routine); the tile decoders of the policies run
+// once per tile in the loader and in every epilogue warp.
+__device__ __forceinline__ int64_t divmod(int64_t a, int64_t b, int64_t &r)
+{
+    if ((static_cast<uint64_t>(a) | static_cast<uint64_t>(b)) < 0x100000000ull) {
+        const uint32_t q = static_cast<uint32_t>(a) / static_cast<uint32_t>(b);
+        r = static_cast<int64_t>(static_cast<uint32_t>(a) - q * static_cast<uint32_t>(b));
+        return q;
+    }
+    const int64_t q = a / b;
+    r = a - q * b;
+    return q;
+}
+
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p)
 {
     return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));

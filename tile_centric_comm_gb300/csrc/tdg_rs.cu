@@ -185,28 +185,25 @@ template <int BMN> struct RsPolicy {
     {
         const int64_t per_rank = (int64_t)p.mtp * p.n_tiles;
         int o, r;
-        int64_t rem;
+        int64_t rem, x;
         if (p.order == 1) {
-            r = (int)(item % p.W);
-            const int64_t rest = item / p.W;
-            o = (int)(rest / per_rank);
-            rem = rest % per_rank;
+            const int64_t rest = divmod(item, p.W, x);
+            r = (int)x;
+            o = (int)divmod(rest, per_rank, rem);
         } else {
             // blocks of ob owners; inside a block every rank's tiles run back
             // to back, so B_r is streamed once per block and every output tile
             // of the block gathers its W partials within the block
             const int64_t per_block = (int64_t)p.W * p.ob * per_rank;
-            const int blk = (int)(item / per_block);
-            int64_t x = item % per_block;
-            r = (int)(x / (p.ob * per_rank));
-            x %= p.ob * per_rank;
-            o = blk * p.ob + (int)(x / per_rank);
-            rem = x % per_rank;
+            const int blk = (int)divmod(item, per_block, x);
+            r = (int)divmod(x, (int64_t)p.ob * per_rank, x);
+            o = blk * p.ob + (int)divmod(x, per_rank, rem);
         }
         t.owner = o;
         t.a_sel = r;
-        t.m_loc = (int)(rem / p.n_tiles) * p.cl + sub; // 128-row tile in the owner
-        t.pn = (int)(rem % p.n_tiles);
+        int64_t pn;
+        t.m_loc = (int)divmod(rem, p.n_tiles, pn) * p.cl + sub; // 128-row tile in the owner
+        t.pn = (int)pn;
         t.m0 = (o * p.mt + t.m_loc) * gm::BM;
         t.a_row = t.m0;
         t.n0 = t.pn * gm::BN;
