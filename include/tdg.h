@@ -347,8 +347,8 @@ typedef struct {
     uint64_t timeout_ns; /* bound of every device wait; 0 = 2 s             */
     int owner_block;     /* tile order: owners per block, each rank's tiles of
                             a block back to back (must divide world; 0 =
-                            world with bf16 partials, the largest divisor
-                            of world up to 4 with fp32 partials)             */
+                            world with bf16 partials, 2 with fp32 partials
+                            (1 for an odd world))                            */
     int partial_f32;     /* 1: fp32 partials (twice the staging), 0: bf16     */
     /* schedule (0 = default for the shape) */
     int cluster;         /* CTAs per GEMM cluster: 1, 2 (needs (M/W) % 256
@@ -358,7 +358,7 @@ typedef struct {
     int order;           /* 0: owner blocks (owner_block); 1: rank fastest   */
     int red_rows;        /* rows of an owed reduction an epilogue warp works
                             off after each tile: 4, 8, 16 or 32 (default 32
-                            for bf16 partials, 8 for fp32)                   */
+                            for bf16 partials, 4 for fp32)                   */
     int spare;           /* the SMs that 4-CTA clusters leave idle (order 0,
                             TDG_B_KN): a second launch of CTA pairs on them
                             takes the last `spare` of the W*W (owner block,

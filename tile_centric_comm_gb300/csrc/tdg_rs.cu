@@ -483,13 +483,11 @@ extern "C" int tdg_gemm_rs(tdg_symm *h, const tdg_gemm_rs_args *a, void *stream)
     // Default block, measured at the Qwen-32B down-projection shape: with bf16
     // partials all owners in one block (each B_r streamed once; 1.7-2.9 %
     // over blocks of 2), with fp32 partials (twice the bytes to keep warm)
-    // the largest divisor of W up to 4
+    // blocks of 2 owners (1 for odd W), whose reductions come every few
+    // tiles instead of in one late stretch (+4 % over blocks of 4)
     if (a->owner_block < 0 || (a->owner_block > 0 && W % a->owner_block))
         return TDG_ERR_INVALID;
-    int ob_default = W;
-    if (f32)
-        for (ob_default = W < 4 ? W : 4; W % ob_default; --ob_default) {
-        }
+    const int ob_default = f32 ? (W % 2 ? 1 : 2) : W;
     p.ob = a->owner_block > 0 ? a->owner_block : ob_default;
     // with one block of all owners a partial is reduced only after every
     // rank's GEMM reached its tile, long after it left L2: let the pushes
@@ -505,8 +503,10 @@ extern "C" int tdg_gemm_rs(tdg_symm *h, const tdg_gemm_rs_args *a, void *stream)
     p.f32 = f32;
     // measured at the Qwen-32B down-projection shape: a bf16 quarter's
     // reduction fits in the slack of one tile, so it is done at once; an fp32
-    // one (twice the bytes) goes fastest in slices of 8 rows per tile
-    p.red_rows = a->red_rows ? a->red_rows : (f32 ? 8 : 32);
+    // one (twice the bytes) goes fastest in slices of 4 rows per tile with
+    // blocks of 2 owners (1530-1550 TFLOP/s against 1080 at once and
+    // 1470 for blocks of 4 in slices of 8; the serial twin 1495-1500)
+    p.red_rows = a->red_rows ? a->red_rows : (f32 ? 4 : 32);
 
     const void *fn;
     if (a->b_layout == TDG_B_KN)
