@@ -83,6 +83,44 @@ def test_ring_stages_bit_exact(cluster, stages):
         assert np.array_equal(got[r], oracle.ag_gemm(aa.shards, aa.Bs[r])[1]), r
 
 
+@pytest.mark.parametrize("kb,cluster", [(1, 4), (5, 4), (6, 4), (7, 4), (13, 4), (7, 2), (5, 1), (13, 1)])
+def test_unrolled_ring_rounds_bit_exact(kb, cluster):
+    # With every ring slot in use and every tile full width, the MMA issuer
+    # runs whole rounds of its ring unrolled.  k-block counts below, at and
+    # past the ring's depth (6 slots for pairs and clusters, 4 for one CTA),
+    # with several tiles per cluster so that tiles start at every slot: the
+    # integer AG-GEMM equals the oracle bit for bit on sampled entries, and a
+    # ring one slot shorter (the per-stage loop) gives the same bits
+    # everywhere; the GEMM-RS likewise against its one-slot-shorter ring.
+    K = 64 * kb
+    depth = 4 if cluster == 1 else 6
+    inp = synth.ag_inputs(8, 2048, K, 2048, "int2", seed=100 + kb)
+    case = AGCase(inp)
+    g = np.random.default_rng(kb)
+    rows = np.concatenate([g.integers(0, case.M, 2000), [0, case.M - 1]])
+    cols = np.concatenate([g.integers(0, inp.N, 2000), [inp.N - 1, 0]])
+    want = oracle.f64_to_bf16(oracle.ag_gemm_sampled(inp.shards, inp.B, rows, cols))
+    for mode in ("serial", "ce"):
+        got, _ = case.run(rank=0, mode=mode, cluster=cluster)
+        assert np.array_equal(got[rows, cols], want), mode
+        short, _ = case.run(rank=0, mode=mode, cluster=cluster, stages=depth - 1)
+        assert np.array_equal(got, short), mode
+    del case
+    rs = synth.rs_inputs(8, 8192, K, 1024, "int2", seed=200 + kb)
+    rcase = RSCase(rs)
+    got, _ = rcase.run(mode="sm", cluster=cluster)
+    short, _ = rcase.run(mode="sm", cluster=cluster, stages=depth - 1)
+    assert np.array_equal(got, short)
+    if kb == 1:   # |partial| <= 4K = 256: every bf16 partial is exact
+        M, N = rs.M, rs.N
+        r_s = np.concatenate([g.integers(0, M, 2000), [0, M - 1]])
+        c_s = np.concatenate([g.integers(0, N, 2000), [N - 1, 0]])
+        ref = oracle.f64_to_bf16(oracle.gemm_rs_sampled(rs.As, rs.Bs, r_s, c_s))
+        assert np.array_equal(got.reshape(M, N)[r_s, c_s], ref)
+    del rcase
+    torch.cuda.empty_cache()
+
+
 @pytest.mark.parametrize("W,Mo,N,spare", [(2, 512, 520, 1), (2, 1024, 264, 3), (4, 512, 520, 5),
                                            (8, 512, 264, 63), (8, 1024, 8, 2)])
 def test_spare_sm_pairs_bit_exact(W, Mo, N, spare):
