@@ -141,14 +141,17 @@ def test_f32_partials_float_within_one_ulp(b_layout):
     assert np.max(np.abs(got64 - out64)) <= np.max(np.abs(b64 - out64))
 
 
+@pytest.mark.parametrize("W,M,N", [(8, 8192, 2048), (2, 8192, 4096)])
 @pytest.mark.parametrize("red_rows", [4, 8, 32])
-def test_owed_reductions_worked_off_in_slices(red_rows):
-    # many tiles per epilogue warp (W = 8, 2 x 8 quad tiles per owner), fp32
-    # partials: the last arriver queues its reduction and works it off a few
-    # rows per tile (with 4 rows a third owed reduction often finishes the
-    # oldest at once); every output must match the oracle and the separate
-    # reduction launch bit for bit (integer inputs: exact)
-    W, M, K, N = 8, 8192, 64, 2048
+def test_owed_reductions_worked_off_in_slices(red_rows, W, M, N):
+    # many tiles per epilogue warp, fp32 partials: the last arriver queues its
+    # reduction and works it off a few rows per tile.  With W = 2 and 128
+    # quad tiles per owner, about 7 last-rank tiles come to each cluster in a
+    # row, so a warp's queue fills (a fourth owed reduction finishes the
+    # oldest at once) and the pass after the last tile finishes up to four.
+    # Every output must match the oracle and the separate reduction launch
+    # bit for bit (integer inputs: exact), and every counter ends at zero.
+    K = 64
     inp = synth.rs_inputs(W, M, K, N, "int2", seed=41)
     case = RSCase(inp, f32=True)
     fused, _ = case.run(mode="sm", red_rows=red_rows)

@@ -284,13 +284,18 @@ template <int BMN> struct RsPolicy {
     }
 
     // The reductions an epilogue warp owes, oldest first: rows [row0, 32) of
-    // its quarter of tile (o0, m0, pn0), then all of tile 1.  At most two wait;
-    // a third finishes the oldest at once.
+    // its quarter of tile (o0, m0, pn0), then all of tiles 1 and 2.  At most
+    // three wait; a fourth finishes the oldest at once.  (With fp32 partials
+    // in blocks of 2 owners a block's last-rank pass can leave a warp three
+    // quarters to work off; finishing one of them at once stalled the next
+    // accumulator drain and made the call bimodal, 1440-1538 TFLOP/s at the
+    // Qwen-32B down-projection shape against a steady 1553-1562 now.)
     struct EpiState {
         int n;
         int o0, m0, pn0, nv0, row0;
         int o1, m1, pn1, nv1;
         int o2, m2, pn2, nv2;
+        int o3, m3, pn3, nv3;
     };
 
     // After each tile: signal the push (increment the tile quarter's arrival
@@ -303,7 +308,7 @@ template <int BMN> struct RsPolicy {
     {
         if (!p.fused_reduce)
             return;
-        int budget = tail ? 96 : p.red_rows;
+        int budget = tail ? 128 : p.red_rows;
         if (!tail) {
             uint32_t *ctr = p.counters + (uint64_t)t.owner * p.nsig +
                             ((uint64_t)t.m_loc * p.n_tiles + t.pn) * 4 + q;
@@ -320,8 +325,10 @@ template <int BMN> struct RsPolicy {
                     st.o0 = t.owner, st.m0 = t.m_loc, st.pn0 = t.pn, st.nv0 = t.n_valid, st.row0 = 0;
                 } else if (st.n == 1) {
                     st.o1 = t.owner, st.m1 = t.m_loc, st.pn1 = t.pn, st.nv1 = t.n_valid;
-                } else {
+                } else if (st.n == 2) {
                     st.o2 = t.owner, st.m2 = t.m_loc, st.pn2 = t.pn, st.nv2 = t.n_valid;
+                } else {
+                    st.o3 = t.owner, st.m3 = t.m_loc, st.pn3 = t.pn, st.nv3 = t.n_valid;
                     budget += 32 - st.row0; // the oldest is finished now
                 }
                 ++st.n;
@@ -340,6 +347,7 @@ template <int BMN> struct RsPolicy {
                                    0u);
                 st.o0 = st.o1, st.m0 = st.m1, st.pn0 = st.pn1, st.nv0 = st.nv1, st.row0 = 0;
                 st.o1 = st.o2, st.m1 = st.m2, st.pn1 = st.pn2, st.nv1 = st.nv2;
+                st.o2 = st.o3, st.m2 = st.m3, st.pn2 = st.pn3, st.nv2 = st.nv3;
                 --st.n;
             }
         }
