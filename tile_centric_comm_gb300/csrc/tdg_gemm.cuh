@@ -259,8 +259,8 @@ __device__ void gemm_consumer(const typename P::Params &p, uint8_t *smem, int un
             uint32_t acc_phase = 0;
             uint32_t consumed = 0; // kept in a register; published once for the abort drain
             const uint32_t sbase = smem_u32(smem);
-            // The issuing thread spends about 85 cycles on each MMA (256 x 256
-            // x 16, 128 cycles of tensor-pipe work), so what it does between a
+            // The issuing thread spends 60-85 cycles on each MMA (256 x 256 x
+            // 16, 128 cycles of tensor-pipe work), so what it does between a
             // stage's MMAs and the next stage's decides whether the pipe's
             // queue stays full: with full-width tiles only (the common case)
             // it skips the tile's index arithmetic (64-bit divisions) and
