@@ -168,15 +168,6 @@ __device__ __forceinline__ uint32_t atom_cas_acq_rel_gpu(uint32_t *p, uint32_t c
                  : "memory");
     return old;
 }
-__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t *p, uint32_t v)
-{
-    uint32_t old;
-    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;"
-                 : "=r"(old)
-                 : "l"(p), "r"(v)
-                 : "memory");
-    return old;
-}
 __device__ __forceinline__ void st_relaxed_gpu(uint32_t *p, uint32_t v)
 {
     asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
@@ -223,17 +214,7 @@ __device__ __forceinline__ bool wait_flag(const uint32_t *p, uint32_t epoch, uin
 }
 
 // ------------------------------------------------------------------ TMA ----
-__device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *map, uint64_t *bar,
-                                            int x, int y)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(smem_dst)),
-        "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y)
-        : "memory");
-}
-
-// same, with the barrier given as a shared-window address
+// 2-D tile load, with the barrier given as a shared-window address
 __device__ __forceinline__ void tma_load_2d_addr(void *smem_dst, const CUtensorMap *map, uint32_t bar,
                                                  int x, int y)
 {
@@ -251,16 +232,6 @@ __device__ __forceinline__ void tma_load_3d_addr(void *smem_dst, const CUtensorM
         "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(smem_dst)),
         "l"(map), "r"(bar), "r"(x), "r"(y), "r"(z)
-        : "memory");
-}
-
-__device__ __forceinline__ void tma_load_3d(void *smem_dst, const CUtensorMap *map, uint64_t *bar,
-                                            int x, int y, int z)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(smem_dst)),
-        "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
         : "memory");
 }
 
@@ -440,11 +411,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
-__device__ __forceinline__ void named_bar_sync(int id, int nthreads)
-{
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
 } // namespace tdg
 
 // ------------------------------------------------- CTA pairs (clusters of 2) ----
@@ -539,9 +505,6 @@ __device__ __forceinline__ void umma_commit_pair_mask(uint64_t *bar, uint16_t ma
         "h"(mask)
         : "memory");
 }
-
-// the same, on both CTAs of the pair formed by cluster ranks 0 and 1
-__device__ __forceinline__ void umma_commit_pair(uint64_t *bar) { umma_commit_pair_mask(bar, 3); }
 
 // Pair TMA loads multicast to the CTAs of `mask`: the tile lands at the same
 // shared offset in every destination CTA, and each destination's bytes are
