@@ -358,7 +358,9 @@ typedef struct {
     int order;           /* 0: owner blocks (owner_block); 1: rank fastest   */
     int red_rows;        /* rows of an owed reduction an epilogue warp works
                             off after each tile: 4, 8, 16 or 32 (default 32
-                            for bf16 partials, 4 for fp32)                   */
+                            for bf16 partials, 4 for fp32); a warp holds up
+                            to three owed quarters, and a fourth makes it
+                            finish the oldest at once                        */
     int spare;           /* the SMs that 4-CTA clusters leave idle (order 0,
                             TDG_B_KN): a second launch of CTA pairs on them
                             takes the last `spare` of the W*W (owner block,
